@@ -1,0 +1,163 @@
+"""The virtual-noise ES step, written out plainly in float64 on the CPU.
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``).
+
+Source: EvoX API page "evox.triton_kernels.kernels.virtual_noise": the module
+description (the model ``Y[i] = X[i] @ (W + sigma*N_i)^T + (b + sigma*nb_i)``
+and the estimate ``grad_W[j,k] = sum_i fitness_i*N_i[j,k] / (pop_size*sigma)``),
+"Noise indexing scheme", and the API entries ``_cpu_normal_noise``,
+``compute_offsets``, ``virtual_perturbed_linear``, ``virtual_weight_gradient``,
+``virtual_bias_gradient`` and ``virtual_reduce_metric``.
+
+Every function materialises the noise it needs (one individual at a time) and
+does its arithmetic in float64 from the exact input values; there is no
+blocking, fusion or reordering beyond the formula. The optional
+``individuals`` / ``rows`` arguments only select which outputs to
+evaluate, so that large shapes can be checked on windows; each selected output
+is computed from the same definition.
+
+Readings (see also ``splitmix``):
+  R6 ``bias=None`` means no bias term and no bias noise.
+  R7 ``offset`` means the weight block's offset in the forward (bias noise at
+     ``offset + out*in + j``) and the bias block's own offset in
+     ``bias_gradient`` (``virtual_bias_gradient`` says the caller passes the
+     offset of the bias region).
+  R8 ``pop_size`` must equal the number of seeds and of fitness values; the
+     divisor is ``pop_size``.
+  R12 activations between layers are not part of the method.
+"""
+
+from __future__ import annotations
+
+import math
+from typing import Iterable, Optional, Sequence
+
+import numpy as np
+
+from .splitmix import element_indices, noise_np, seeds_u64
+
+
+def _check_pop(seeds: np.ndarray, pop_size: int, other: Optional[np.ndarray] = None) -> None:
+    if pop_size != seeds.shape[0]:
+        raise ValueError(f"pop_size={pop_size} but {seeds.shape[0]} seeds")
+    if other is not None and other.shape[0] != pop_size:
+        raise ValueError(f"pop_size={pop_size} but {other.shape[0]} fitness values")
+
+
+def noise_dump(seeds, n_elements: int, offset: int) -> np.ndarray:
+    """``_cpu_normal_noise``: ``D[i, t] = PRNG(seed_i, offset + t)``, float32 [pop, n]."""
+    s = seeds_u64(seeds)
+    idx = element_indices(offset, n_elements)
+    out = np.empty((s.shape[0], n_elements), dtype=np.float32)
+    for i in range(s.shape[0]):
+        out[i] = noise_np(s[i], idx).astype(np.float32)
+    return out
+
+
+def compute_offsets(param_shapes: Sequence[Sequence[int]]) -> list:
+    """``compute_offsets``: start offset of each block = elements of all blocks before it."""
+    offsets, total = [], 0
+    for shape in param_shapes:
+        offsets.append(total)
+        total += math.prod(int(d) for d in shape)
+    return offsets
+
+
+def weight_noise(seed, out_f: int, in_f: int, offset: int,
+                 rows: Optional[Iterable[int]] = None) -> np.ndarray:
+    """N_i[j, k] = PRNG(seed_i, offset + j*in + k) ("Noise indexing scheme"), float64.
+
+    ``rows`` selects which j to return (default: all, in order)."""
+    s = seeds_u64([seed])[0]
+    rows = range(out_f) if rows is None else list(rows)
+    n = np.empty((len(rows), in_f), dtype=np.float64)
+    for r, j in enumerate(rows):
+        n[r] = noise_np(s, element_indices(offset + j * in_f, in_f))
+    return n
+
+
+def bias_noise(seed, out_f: int, bias_offset: int) -> np.ndarray:
+    """nb_i[j] = PRNG(seed_i, bias_offset + j), float64."""
+    s = seeds_u64([seed])[0]
+    return noise_np(s, element_indices(bias_offset, out_f))
+
+
+def perturbed_linear(x, weight, bias, seeds, sigma: float, offset: int,
+                     individuals: Optional[Iterable[int]] = None,
+                     rows: Optional[Iterable[int]] = None) -> np.ndarray:
+    """``virtual_perturbed_linear`` in float64.
+
+    x: [B, in] (shared by all individuals) or [pop, B, in]; weight: [out, in];
+    bias: [out] or None; seeds: [pop]. Returns [len(individuals), B, len(rows)]
+    (the full [pop, B, out] by default):
+        Y[i] = X[i] @ (W + sigma*N_i)^T + (b + sigma*nb_i),
+    N_i at ``offset + j*in + k`` and nb_i at ``offset + out*in + j``.
+    """
+    w = np.asarray(weight, dtype=np.float64)
+    out_f, in_f = w.shape
+    x = np.asarray(x, dtype=np.float64)
+    s = np.asarray(seeds)
+    pop = s.shape[0]
+    shared = x.ndim == 2
+    if x.shape[-1] != in_f or (not shared and x.shape[0] != pop):
+        raise ValueError("x / weight / seeds shapes disagree")
+    inds = range(pop) if individuals is None else list(individuals)
+    rows = list(range(out_f)) if rows is None else list(rows)
+    b = None if bias is None else np.asarray(bias, dtype=np.float64)
+    batch = x.shape[-2]
+    y = np.empty((len(inds), batch, len(rows)), dtype=np.float64)
+    for r, i in enumerate(inds):
+        n_i = weight_noise(s[i], out_f, in_f, offset, rows)          # [rows, in]
+        w_pert = w[rows] + sigma * n_i                                # W + sigma*N_i
+        xi = x if shared else x[i]                                    # [B, in]
+        yi = xi @ w_pert.T                                            # [B, rows]
+        if b is not None:
+            nb_i = bias_noise(s[i], out_f, offset + out_f * in_f)[rows]
+            yi = yi + (b[rows] + sigma * nb_i)[None, :]
+        y[r] = yi
+    return y
+
+
+def weight_gradient(fitness, seeds, weight_shape, sigma: float, pop_size: int,
+                    offset: int, rows: Optional[Iterable[int]] = None) -> np.ndarray:
+    """``virtual_weight_gradient`` in float64:
+    grad[j, k] = sum_i fitness_i * N_i[j, k] / (pop_size * sigma)."""
+    f = np.asarray(fitness, dtype=np.float64)
+    s = np.asarray(seeds)
+    _check_pop(s, pop_size, f)
+    out_f, in_f = (int(d) for d in weight_shape)
+    rows = list(range(out_f)) if rows is None else list(rows)
+    acc = np.zeros((len(rows), in_f), dtype=np.float64)
+    for i in range(pop_size):
+        acc += f[i] * weight_noise(s[i], out_f, in_f, offset, rows)
+    return acc / (pop_size * sigma)
+
+
+def bias_gradient(fitness, seeds, bias_shape, sigma: float, pop_size: int,
+                  offset: int) -> np.ndarray:
+    """``virtual_bias_gradient`` in float64; ``offset`` already points at the
+    bias region (reading R7): grad[j] = sum_i fitness_i * nb_i[j] / (pop_size*sigma)."""
+    f = np.asarray(fitness, dtype=np.float64)
+    s = np.asarray(seeds)
+    _check_pop(s, pop_size, f)
+    (out_f,) = (int(d) for d in bias_shape)
+    acc = np.zeros(out_f, dtype=np.float64)
+    for i in range(pop_size):
+        acc += f[i] * bias_noise(s[i], out_f, offset)
+    return acc / (pop_size * sigma)
+
+
+def reduce_metric(center, seeds, sigma: float, n_params: int, offset: int = 0,
+                  individuals: Optional[Iterable[int]] = None) -> np.ndarray:
+    """``virtual_reduce_metric`` in float64:
+    fitness[i] = mean_k | center[k] + sigma * PRNG(seed_i, offset + k) |."""
+    c = np.asarray(center, dtype=np.float64)
+    if c.shape != (n_params,):
+        raise ValueError("center must have n_params elements")
+    s = seeds_u64(seeds)
+    inds = range(s.shape[0]) if individuals is None else list(individuals)
+    idx = element_indices(offset, n_params)
+    out = np.empty(len(inds), dtype=np.float64)
+    for r, i in enumerate(inds):
+        out[r] = np.mean(np.abs(c + sigma * noise_np(s[i], idx)))
+    return out

@@ -1,0 +1,364 @@
+"""Pins for the CPU oracle: each test ties the oracle to something other than itself.
+
+The EvoX API page "evox.triton_kernels.kernels.virtual_noise" prints no noise
+values, so the hash is pinned through mathematics: an inverse of the finalizer
+derived here step by step, closed-form special states, the generator's stream
+property, and the statistics the page states. The method is pinned by brute
+force on tiny shapes, exact one-hot recoveries, an expectation identity of the
+ES estimate, and the page's worked example for ``compute_offsets``.
+"""
+
+import json
+import math
+import os
+import random
+
+import numpy as np
+import pytest
+
+from oracle import es, splitmix as sm
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+M64 = (1 << 64) - 1
+
+
+# ---------------------------------------------------------------------------
+# An inverse of the printed finalizer, derived independently of the oracle:
+# undo "x ^= x >> r" by re-applying the shift until the top bits propagate, and
+# undo "x *= G" with the multiplicative inverse of the odd constant mod 2**64.
+# ---------------------------------------------------------------------------
+
+def _unxorshift_right(y: int, r: int) -> int:
+    x = y
+    for _ in range(64 // r + 1):
+        x = y ^ (x >> r)
+    return x & M64
+
+
+def _inverse_finalizer(y: int, gamma: int) -> int:
+    g_inv = pow(gamma, -1, 1 << 64)
+    y = _unxorshift_right(y, 31)
+    y = (y * g_inv) & M64
+    y = _unxorshift_right(y, 27)
+    y = (y * g_inv) & M64
+    y = _unxorshift_right(y, 30)
+    return y
+
+
+GAMMA_PAGE = int(json.load(open(os.path.join(GOLDEN, "gamma.json")))["gamma_decimal"])
+EDGE = [0, 1, 2, (1 << 32) - 1, 1 << 32, (1 << 63) - 1, 1 << 63, M64, 0x9E3779B97F4A7C15]
+
+
+def _rand_u64(rng, n):
+    return [rng.getrandbits(64) for _ in range(n)]
+
+
+def test_gamma_is_the_printed_constant():
+    assert sm.GAMMA == GAMMA_PAGE
+    assert GAMMA_PAGE == 0x9E3779B97F4A7C15  # the golden ratio constant of splitmix64
+    assert GAMMA_PAGE % 2 == 1               # odd, so the multiply is a bijection mod 2**64
+
+
+def test_finalizer_inverts_with_independent_inverse():
+    rng = random.Random(1)
+    for z in EDGE + _rand_u64(rng, 20000):
+        y = sm.mix64(z)
+        assert 0 <= y <= M64
+        assert _inverse_finalizer(y, GAMMA_PAGE) == z
+        assert sm.mix64(_inverse_finalizer(z, GAMMA_PAGE)) == z
+
+
+def test_finalizer_numpy_matches_python_int():
+    rng = random.Random(2)
+    zs = EDGE + _rand_u64(rng, 100000)
+    got = sm.mix64_np(np.array(zs, dtype=np.uint64))
+    assert [int(v) for v in got] == [sm.mix64(z) for z in zs]
+
+
+def test_noise_numpy_matches_python_int_including_wrapping():
+    rng = random.Random(3)
+    seeds = [0, 1, -1, -(2 ** 63), 2 ** 63 - 1] + [rng.randrange(-2 ** 63, 2 ** 63) for _ in range(40)]
+    offsets = [0, 123456789, (1 << 32) - 3, (1 << 64) - 5]
+    for off in offsets:
+        d = es.noise_dump(np.array(seeds, dtype=np.int64), 9, off)
+        for r, s in enumerate(seeds):
+            for t in range(9):
+                assert d[r, t] == np.float32(sm.noise(s, off + t))
+
+
+def test_zero_state_gives_minus_half():
+    # mix(0) == 0 by inspection of the finalizer (xor-shifts and products of 0).
+    assert sm.mix64(0) == 0
+    assert sm.noise(0, M64) == -0.5          # state = 0 + (2**64) * G = 0 mod 2**64
+    rng = random.Random(4)
+    for idx in [0, 1, 77, 1 << 40] + [rng.getrandbits(64) for _ in range(100)]:
+        seed = (-(idx + 1) * GAMMA_PAGE) & M64  # makes the state exactly 0
+        assert sm.noise(seed, idx) == -0.5
+
+
+def test_stream_property_of_the_state():
+    # Reading R1: element idx of seed s is element idx-k of seed s + k*G.
+    rng = random.Random(5)
+    for _ in range(2000):
+        s, idx, k = rng.getrandbits(64), rng.getrandbits(64), rng.randrange(1, 1000)
+        assert sm.noise(s, idx) == sm.noise((s + k * GAMMA_PAGE) & M64, (idx - k) & M64)
+
+
+def test_low_32_bits_map_to_the_uniform():
+    """Choose the hash output, invert it to a state, and check the value read off it.
+
+    Pins that the low (not high) 32 bits are used, that the top 23 of them make
+    the mantissa, and the -0.5 shift."""
+    rng = random.Random(6)
+    cases = [
+        (0x00000000_00000000, -0.5),
+        (0xFFFFFFFF_00000000, -0.5),               # high half ignored
+        (0x00000000_000001FF, -0.5),               # bits below 9 dropped
+        (0x00000000_FFFFFFFF, 0.5 - 2 ** -23),     # the largest value, < 0.5
+        (0x12345678_80000000, 0.0),
+        (0x00000000_00000200, -0.5 + 2 ** -23),
+    ]
+    for _ in range(2000):
+        h = rng.getrandbits(64)
+        cases.append((h, ((h & 0xFFFFFFFF) >> 9) / 2 ** 23 - 0.5))
+    for h, want in cases:
+        state = _inverse_finalizer(h, GAMMA_PAGE)
+        idx = rng.getrandbits(64)
+        seed = (state - (idx + 1) * GAMMA_PAGE) & M64
+        assert sm.noise(seed, idx) == want
+
+
+def test_noise_statistics_stated_on_the_page():
+    n = 1_000_000
+    seeds = np.array([7, -3], dtype=np.int64)
+    d = es.noise_dump(seeds, n // 2, 999).astype(np.float64).ravel()
+    assert np.all(np.isfinite(d))
+    assert d.min() >= -0.5 and d.max() < 0.5
+    m = d * 2 ** 23
+    assert np.all(m == np.round(m))                     # multiples of 2**-23
+    assert abs(d.mean()) < 5 * math.sqrt(1 / 12 / n)     # mean ~ 0
+    assert abs(d.var() - 1 / 12) < 5 * 7.5e-5           # variance 1/12
+    counts, _ = np.histogram(d, bins=64, range=(-0.5, 0.5))
+    chi2 = ((counts - n / 64) ** 2 / (n / 64)).sum()
+    assert chi2 < 63 + 6 * math.sqrt(2 * 63)            # uniform, 63 dof
+
+
+def test_signed_and_int32_seeds():
+    a = es.noise_dump(np.array([-1, 5, -7], dtype=np.int32), 33, 10)
+    b = es.noise_dump(np.array([-1, 5, -7], dtype=np.int64), 33, 10)
+    c = es.noise_dump(np.array([M64, 5, M64 - 6], dtype=np.uint64), 33, 10)
+    assert np.array_equal(a, b) and np.array_equal(b, c)
+
+
+def test_dump_window_identity():
+    seeds = np.arange(5, dtype=np.int64) * 1000003 - 2
+    full = es.noise_dump(seeds, 300, 77)
+    for t0, t1 in [(0, 1), (17, 123), (250, 300)]:
+        assert np.array_equal(full[:, t0:t1], es.noise_dump(seeds, t1 - t0, 77 + t0))
+
+
+def test_compute_offsets_worked_example():
+    g = json.load(open(os.path.join(GOLDEN, "compute_offsets.json")))
+    assert es.compute_offsets([tuple(s) for s in g["param_shapes"]]) == g["offsets"]
+    # The ES MLP policy 64 -> 256 -> 256 -> 8, weights then bias per layer.
+    shapes = [(256, 64), (256,), (256, 256), (256,), (8, 256), (8,)]
+    assert es.compute_offsets(shapes) == [0, 16384, 16640, 82176, 82432, 84480]
+    assert es.compute_offsets([]) == []
+
+
+# ---------------------------------------------------------------------------
+# Forward
+# ---------------------------------------------------------------------------
+
+def _brute_forward(x, w, b, seeds, sigma, offset):
+    """Pure-Python loops, one noise element at a time from the Python-int hash."""
+    pop = len(seeds)
+    out_f, in_f = len(w), len(w[0])
+    shared = not isinstance(x[0][0], list)
+    batch = len(x) if shared else len(x[0])
+    y = [[[0.0] * out_f for _ in range(batch)] for _ in range(pop)]
+    for i in range(pop):
+        xi = x if shared else x[i]
+        for r in range(batch):
+            for j in range(out_f):
+                acc = 0.0
+                for k in range(in_f):
+                    acc += xi[r][k] * (w[j][k] + sigma * sm.noise(seeds[i], offset + j * in_f + k))
+                if b is not None:
+                    acc += b[j] + sigma * sm.noise(seeds[i], offset + out_f * in_f + j)
+                y[i][r][j] = acc
+    return y
+
+
+@pytest.mark.parametrize("shared", [False, True])
+@pytest.mark.parametrize("with_bias", [False, True])
+def test_forward_matches_brute_force(shared, with_bias):
+    rng = np.random.default_rng(10)
+    pop, batch, in_f, out_f = 3, 2, 5, 4
+    x = rng.standard_normal((batch, in_f) if shared else (pop, batch, in_f))
+    w = rng.standard_normal((out_f, in_f))
+    b = rng.standard_normal(out_f) if with_bias else None
+    seeds = [3, -9, 2 ** 40 + 1]
+    sigma, offset = 0.37, (1 << 32) - 7
+    got = es.perturbed_linear(x, w, b, np.array(seeds), sigma, offset)
+    want = np.array(_brute_forward(x.tolist(), w.tolist(), None if b is None else b.tolist(),
+                                   seeds, sigma, offset))
+    assert got.shape == (pop, batch, out_f)
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
+def test_forward_sigma_zero_is_plain_linear():
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((4, 3, 6))
+    w = rng.standard_normal((5, 6))
+    b = rng.standard_normal(5)
+    got = es.perturbed_linear(x, w, b, np.arange(4), 0.0, 0)
+    want = np.einsum("ibk,jk->ibj", x, w) + b
+    np.testing.assert_allclose(got, want, rtol=1e-13, atol=1e-13)
+
+
+def test_forward_one_hot_reads_noise_columns_exactly():
+    """X rows = e_k, W = 0, b = 0, sigma = 1 gives Y[i, r, :] = N_i[:, k_r] + nb_i, exactly;
+    N_i comes from the dump reshaped row-major ("Noise indexing scheme")."""
+    pop, in_f, out_f, offset = 3, 6, 5, 1000
+    seeds = np.array([11, 12, -13])
+    x = np.zeros((pop, in_f, in_f))
+    for i in range(pop):
+        x[i] = np.eye(in_f)
+    y = es.perturbed_linear(x, np.zeros((out_f, in_f)), np.zeros(out_f), seeds, 1.0, offset)
+    dump = es.noise_dump(seeds, out_f * in_f + out_f, offset).astype(np.float64)
+    for i in range(pop):
+        n_i = dump[i, : out_f * in_f].reshape(out_f, in_f)
+        nb_i = dump[i, out_f * in_f:]
+        assert np.array_equal(y[i], (n_i + nb_i[:, None]).T)
+    # Without a bias there is no bias noise either (reading R6).
+    y0 = es.perturbed_linear(x, np.zeros((out_f, in_f)), None, seeds, 1.0, offset)
+    for i in range(pop):
+        assert np.array_equal(y0[i], dump[i, : out_f * in_f].reshape(out_f, in_f).T)
+
+
+def test_forward_noise_identity():
+    """(Y - X W^T - b) / sigma = X N_i^T + nb_i."""
+    rng = np.random.default_rng(12)
+    pop, batch, in_f, out_f, sigma, offset = 4, 3, 7, 6, 0.01, 55
+    seeds = np.array([1, 2, 3, 4]) * 7919
+    x = rng.standard_normal((pop, batch, in_f))
+    w = rng.standard_normal((out_f, in_f))
+    b = rng.standard_normal(out_f)
+    y = es.perturbed_linear(x, w, b, seeds, sigma, offset)
+    dump = es.noise_dump(seeds, out_f * in_f + out_f, offset).astype(np.float64)
+    for i in range(pop):
+        n_i = dump[i, : out_f * in_f].reshape(out_f, in_f)
+        nb_i = dump[i, out_f * in_f:]
+        lhs = (y[i] - x[i] @ w.T - b) / sigma
+        np.testing.assert_allclose(lhs, x[i] @ n_i.T + nb_i, rtol=1e-8, atol=1e-10)
+
+
+def test_forward_shared_x_equals_broadcast_x():
+    rng = np.random.default_rng(13)
+    x = rng.standard_normal((3, 8))
+    w = rng.standard_normal((4, 8))
+    seeds = np.array([5, 6, 7, 8, 9])
+    a = es.perturbed_linear(x, w, None, seeds, 0.1, 3)
+    b = es.perturbed_linear(np.broadcast_to(x, (5, 3, 8)), w, None, seeds, 0.1, 3)
+    assert np.array_equal(a, b)
+
+
+def test_forward_windows_match_full():
+    rng = np.random.default_rng(14)
+    x = rng.standard_normal((6, 2, 9))
+    w = rng.standard_normal((7, 9))
+    b = rng.standard_normal(7)
+    seeds = np.arange(6) + 100
+    full = es.perturbed_linear(x, w, b, seeds, 0.2, 9)
+    win = es.perturbed_linear(x, w, b, seeds, 0.2, 9, individuals=[0, 5], rows=[1, 6])
+    assert np.array_equal(win, full[[0, 5]][:, :, [1, 6]])
+
+
+# ---------------------------------------------------------------------------
+# Gradients
+# ---------------------------------------------------------------------------
+
+def test_weight_gradient_one_hot_fitness_recovers_noise_exactly():
+    """f = e_m * pop * sigma with pop and sigma powers of two gives grad_W == N_m exactly."""
+    pop, sigma, out_f, in_f, offset = 8, 2.0 ** -7, 5, 6, 123456789
+    seeds = np.arange(1, pop + 1)
+    dump = es.noise_dump(seeds, out_f * in_f, offset).astype(np.float64)
+    for m in (0, 3, 7):
+        f = np.zeros(pop)
+        f[m] = pop * sigma
+        g = es.weight_gradient(f, seeds, (out_f, in_f), sigma, pop, offset)
+        assert np.array_equal(g, dump[m].reshape(out_f, in_f))
+
+
+def test_weight_gradient_equals_fitness_weighted_dump():
+    rng = np.random.default_rng(15)
+    pop, out_f, in_f, sigma, offset = 16, 4, 5, 0.05, 31
+    seeds = rng.integers(-2 ** 40, 2 ** 40, pop)
+    f = rng.standard_normal(pop)
+    g = es.weight_gradient(f, seeds, (out_f, in_f), sigma, pop, offset)
+    dump = es.noise_dump(seeds, out_f * in_f, offset).astype(np.float64)
+    np.testing.assert_allclose(g, (f @ dump).reshape(out_f, in_f) / (pop * sigma), rtol=1e-12, atol=1e-14)
+    # Linearity in the fitness.
+    f2 = rng.standard_normal(pop)
+    g2 = es.weight_gradient(f2, seeds, (out_f, in_f), sigma, pop, offset)
+    g12 = es.weight_gradient(2 * f - 3 * f2, seeds, (out_f, in_f), sigma, pop, offset)
+    np.testing.assert_allclose(g12, 2 * g - 3 * g2, rtol=1e-10, atol=1e-12)
+    # Row windows are the same definition.
+    gr = es.weight_gradient(f, seeds, (out_f, in_f), sigma, pop, offset, rows=[3, 1])
+    assert np.array_equal(gr, g[[3, 1]])
+
+
+def test_weight_gradient_expectation_on_a_linear_objective():
+    """f_i = <C, W + sigma N_i> with W = 0 gives E[grad_W] = Var(noise) * C = C / 12.
+
+    Catches a wrong scale (sigma, pop), a wrong sign, or noise regenerated at the
+    wrong index between the objective and the estimate."""
+    rng = np.random.default_rng(16)
+    out_f, in_f, pop, sigma, offset = 3, 4, 40000, 0.03, 500
+    c = rng.standard_normal((out_f, in_f))
+    seeds = np.arange(pop, dtype=np.int64) * 3 + 1
+    dump = es.noise_dump(seeds, out_f * in_f, offset).astype(np.float64)
+    f = sigma * dump @ c.ravel()
+    g = es.weight_gradient(f, seeds, (out_f, in_f), sigma, pop, offset)
+    terms = (f[:, None] * dump) / sigma                     # per-individual contributions
+    se = terms.std(axis=0) / math.sqrt(pop)
+    assert np.all(np.abs(g.ravel() - c.ravel() / 12) < 5 * se)
+
+
+def test_bias_gradient_matches_forward_bias_noise():
+    """virtual_bias_gradient at offset + out*in regenerates the forward's bias noise."""
+    pop, sigma, out_f, in_f, offset = 4, 0.25, 6, 3, 40
+    seeds = np.array([9, -8, 7, -6])
+    y = es.perturbed_linear(np.zeros((pop, 1, in_f)), np.zeros((out_f, in_f)), np.zeros(out_f),
+                            seeds, 1.0, offset)                      # Y = nb_i exactly
+    for m in range(pop):
+        f = np.zeros(pop)
+        f[m] = pop * sigma
+        g = es.bias_gradient(f, seeds, (out_f,), sigma, pop, offset + out_f * in_f)
+        assert np.array_equal(g, y[m, 0])
+
+
+def test_gradients_refuse_mismatched_population():
+    with pytest.raises(ValueError):
+        es.weight_gradient(np.ones(3), np.arange(4), (2, 2), 0.1, 4, 0)
+    with pytest.raises(ValueError):
+        es.bias_gradient(np.ones(4), np.arange(4), (2,), 0.1, 5, 0)
+
+
+# ---------------------------------------------------------------------------
+# Mean-abs reduction metric
+# ---------------------------------------------------------------------------
+
+def test_reduce_metric_special_cases_and_brute_force():
+    rng = np.random.default_rng(17)
+    center = rng.standard_normal(50)
+    seeds = np.array([1, 2, 3])
+    np.testing.assert_allclose(es.reduce_metric(center, seeds, 0.0, 50, 0), np.abs(center).mean(), rtol=1e-14)
+    dump = es.noise_dump(seeds, 50, 7).astype(np.float64)
+    np.testing.assert_allclose(es.reduce_metric(np.zeros(50), seeds, 1.0, 50, 7),
+                               np.abs(dump).mean(axis=1), rtol=1e-14)
+    got = es.reduce_metric(center, seeds, 0.3, 50, 7)
+    for i, s in enumerate(seeds.tolist()):
+        want = sum(abs(center[k] + 0.3 * sm.noise(s, 7 + k)) for k in range(50)) / 50
+        assert abs(got[i] - want) < 1e-13
