@@ -1,0 +1,179 @@
+/*
+ * vn.h -- C ABI of the virtual-noise evolution-strategies library (libvn.so).
+ *
+ * The library computes, on one CUDA device, the population evolution-strategies
+ * step with virtual (never materialised) weight noise described on the EvoX API
+ * page "evox.triton_kernels.kernels.virtual_noise":
+ *
+ *   forward   Y[i] = X[i] @ (W + sigma*N_i)^T + (b + sigma*nb_i)      (module description)
+ *   gradient  grad_W[j,k] = sum_i f_i * N_i[j,k] / (pop*sigma)        (module description)
+ *   noise     N_i[j,k] = PRNG(seed_i, offset + j*in + k),             ("Noise indexing scheme")
+ *             nb_i[j]  = PRNG(seed_i, offset + out*in + j)
+ *
+ * PRNG(seed, idx) -- the definition every entry point follows, bit for bit:
+ *   GAMMA = 0x9E3779B97F4A7C15 (11400714819323198485, "_SPLITMIX64_GAMMA");
+ *   z = seed + (idx + 1) * GAMMA                         (mod 2^64)
+ *   z = (z ^ (z >> 30)) * GAMMA; z = (z ^ (z >> 27)) * GAMMA; z ^= z >> 31
+ *       (logical shifts, products mod 2^64; "_splitmix64_step" as printed)
+ *   PRNG = (lo32(z) >> 9) * 2^-23 - 0.5,  a float32 value in [-0.5, 0.5)
+ *       (low 32 bits of the hash, "_cpu_normal_noise"; the top 23 of them, so
+ *        the value is exact in float32 and never reaches 0.5).
+ * The state formula (the idx-th output of a splitmix64 generator seeded with
+ * seed) is this library's reading: the page does not say how seed and index
+ * are combined. Seeds are signed 64-bit integers taken mod 2^64. The element
+ * index offset + j*in + k is evaluated in unsigned 64-bit arithmetic and wraps.
+ *
+ * Conventions shared by every entry point
+ *   - Every tensor pointer is a CUDA device pointer owned by the caller, to a
+ *     dense row-major array on the current device. Nothing is copied, retained
+ *     or freed. fp32 arrays must be 4-byte aligned, bf16 arrays 2-byte aligned,
+ *     seeds 8-byte aligned (else VN_ERR_ALIGN).
+ *   - All work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and is asynchronous: a VN_OK return means the arguments were
+ *     valid and the kernel was launched, not that it has finished.
+ *   - Arguments are validated on the host before anything is launched. A call
+ *     that fails validation returns its status and launches nothing.
+ *   - A size of 0 in an output dimension is valid and launches nothing (the
+ *     pointers of empty arrays may then be NULL).
+ *   - Kernels that wait on on-chip barriers bound every wait. A wait that runs
+ *     out records VN_ERR_TIMEOUT in a device-side status word, which
+ *     vn_device_status() reports; the kernel returns without hanging the GPU.
+ *   - The library allocates no device memory at call time.
+ */
+#ifndef VN_H
+#define VN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum vn_status {
+  VN_OK = 0,
+  VN_ERR_NULL = 1,     /* a required pointer is NULL                                */
+  VN_ERR_SHAPE = 2,    /* a size is negative, or pop < 1 where an estimate needs it   */
+  VN_ERR_DTYPE = 3,    /* unsupported dtype or dtype combination                    */
+  VN_ERR_VALUE = 4,    /* sigma not finite, or sigma == 0 for a gradient            */
+  VN_ERR_ALIGN = 5,    /* a pointer is not aligned to its element size              */
+  VN_ERR_OVERFLOW = 6, /* a size product does not fit in int64                      */
+  VN_ERR_TIMEOUT = 7,  /* a device-side bounded wait ran out (vn_device_status)     */
+  VN_ERR_CUDA = 8,     /* a CUDA runtime call failed (vn_last_error_message)        */
+  VN_ERR_DEVICE = 9,   /* the requested path needs a compute-capability 10.x GPU    */
+  VN_ERR_PATH = 10     /* the forced forward path cannot run these arguments        */
+} vn_status;
+
+typedef enum vn_dtype { VN_F32 = 0, VN_BF16 = 1 } vn_dtype;
+
+/* Forward kernel selection for vn_perturbed_linear_ex. */
+typedef enum vn_path {
+  VN_PATH_AUTO = 0,  /* tensor-core path when it applies, else the FFMA path      */
+  VN_PATH_FFMA = 1,  /* CUDA-core path: any dtypes, any batch                     */
+  VN_PATH_TC = 2     /* tcgen05/TMEM path: x bf16, in % 8 == 0, 16-byte aligned   */
+} vn_path;
+
+/* Element-wise activation applied to Y after the bias (vn_perturbed_linear_ex). */
+typedef enum vn_act { VN_ACT_NONE = 0, VN_ACT_TANH = 1 } vn_act;
+
+/*
+ * vn_perturbed_linear -- "virtual_perturbed_linear" (API entry of the page):
+ *     Y[i, r, :] = X[i, r, :] @ (W + sigma*N_i)^T + (b + sigma*nb_i)
+ * x       [pop, batch, in] of x_dt, or [batch, in] when x_shared != 0 (the same
+ *         input for every individual).
+ * w       [out, in] of w_dt.                 b  [out] of b_dt, or NULL: then
+ *         there is no bias term and no bias noise.
+ * seeds   [pop] int64.                       y  [pop, batch, out] of y_dt.
+ * offset  flat element offset of this weight block (compute_offsets); the bias
+ *         noise is read at offset + out*in + j.
+ * dtypes  x, w, b: VN_F32 or VN_BF16. y_dt must be VN_BF16 when x and w are
+ *         both bf16 and VN_F32 otherwise (torch's result type of x and w).
+ * Arithmetic: W + sigma*N_i is formed in fp32 per element. On the tensor-core
+ * path it is rounded to bf16 and contracted with bf16 x, accumulating in fp32;
+ * on the FFMA path everything is fp32. in == 0 gives Y = b + sigma*nb_i.
+ */
+vn_status vn_perturbed_linear(const void* x, vn_dtype x_dt, int x_shared,
+                              const void* w, vn_dtype w_dt,
+                              const void* b, vn_dtype b_dt,
+                              const int64_t* seeds, int64_t pop, int64_t batch,
+                              int64_t in, int64_t out, double sigma, uint64_t offset,
+                              void* y, vn_dtype y_dt, void* stream);
+
+/* vn_perturbed_linear with an explicit kernel choice and a fused activation
+ * (applied after the bias). VN_PATH_TC returns VN_ERR_PATH when its conditions
+ * do not hold and VN_ERR_DEVICE on a device that is not compute capability 10.x. */
+vn_status vn_perturbed_linear_ex(const void* x, vn_dtype x_dt, int x_shared,
+                                 const void* w, vn_dtype w_dt,
+                                 const void* b, vn_dtype b_dt,
+                                 const int64_t* seeds, int64_t pop, int64_t batch,
+                                 int64_t in, int64_t out, double sigma, uint64_t offset,
+                                 void* y, vn_dtype y_dt, vn_path path, vn_act act,
+                                 void* stream);
+
+/*
+ * vn_weight_gradient -- "virtual_weight_gradient" (API entry of the page):
+ *     grad_w[j, k] = sum_i fitness[i] * N_i[j, k] / (pop * sigma)
+ * fitness [pop] fp32, seeds [pop] int64, grad_w [out, in] fp32 (written, not
+ * accumulated into). N_i[j,k] is read at offset + j*in + k, the same elements
+ * vn_perturbed_linear perturbs. pop >= 1; sigma finite and nonzero. The sum
+ * over individuals is accumulated in fp32 in a fixed order (deterministic) and
+ * multiplied by fp32(1 / (pop*sigma)).
+ */
+vn_status vn_weight_gradient(const float* fitness, const int64_t* seeds, int64_t pop,
+                             int64_t out, int64_t in, double sigma, uint64_t offset,
+                             float* grad_w, void* stream);
+
+/*
+ * vn_bias_gradient -- "virtual_bias_gradient" (API entry of the page):
+ *     grad_b[j] = sum_i fitness[i] * nb_i[j] / (pop * sigma),  nb_i[j] at offset + j.
+ * `offset` already points at the bias region: pass weight_offset + out*in to
+ * match the bias noise of vn_perturbed_linear. Same conventions as
+ * vn_weight_gradient.
+ */
+vn_status vn_bias_gradient(const float* fitness, const int64_t* seeds, int64_t pop,
+                           int64_t out, double sigma, uint64_t offset,
+                           float* grad_b, void* stream);
+
+/*
+ * vn_noise_dump -- the "_cpu_normal_noise" contract (API entry of the page):
+ *     out[i, t] = PRNG(seed_i, offset + t),  out [pop, n] fp32.
+ * Bit-exact with the definition above.
+ */
+vn_status vn_noise_dump(const int64_t* seeds, int64_t pop, int64_t n, uint64_t offset,
+                        float* out, void* stream);
+
+/*
+ * vn_reduce_metric -- "virtual_reduce_metric" (API entry of the page):
+ *     fitness[i] = mean_k | center[k] + sigma * PRNG(seed_i, offset + k) |
+ * center [n_params] fp32, seeds [pop] int64, fitness [pop] fp32. n_params >= 1;
+ * sigma finite. The sum over k is accumulated in fp32 in a fixed order and
+ * multiplied by fp32(1 / n_params).
+ */
+vn_status vn_reduce_metric(const float* center, const int64_t* seeds, int64_t pop,
+                           int64_t n_params, double sigma, uint64_t offset,
+                           float* fitness, void* stream);
+
+/* Synchronises `stream`, then reads and clears the current device's status
+ * word: VN_ERR_TIMEOUT if a kernel of this library recorded an expired wait
+ * since the last call, VN_ERR_CUDA if synchronisation failed, else VN_OK. */
+vn_status vn_device_status(void* stream);
+
+/* A static, human-readable name for a status code. */
+const char* vn_status_string(vn_status status);
+
+/* The CUDA error text behind the calling thread's last VN_ERR_CUDA ("" if none). */
+const char* vn_last_error_message(void);
+
+/* The forward path vn_perturbed_linear would take for these arguments on the
+ * current device (VN_PATH_FFMA or VN_PATH_TC); launches nothing. */
+vn_path vn_perturbed_linear_path(const void* x, vn_dtype x_dt, int x_shared,
+                                 const void* w, vn_dtype w_dt, int64_t batch,
+                                 int64_t in, int64_t out);
+
+/* ABI version: (major << 16) | minor. */
+int vn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VN_H */

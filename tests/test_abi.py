@@ -1,0 +1,100 @@
+"""The C ABI without a GPU: the library builds, loads and exports every symbol the
+header declares, and argument validation refuses bad calls before touching the
+device (every call below returns from host-side checks; none launches)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from virtual_noise_perturbed_gb300 import _lib, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "vn.h")
+P = ctypes.c_void_p
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(vn_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ["vn_perturbed_linear", "vn_weight_gradient", "vn_bias_gradient", "vn_noise_dump"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in _lib.SIGNATURES, f"binding lacks {name}"
+
+
+def test_status_strings(lib):
+    for code, name in _lib.STATUS_NAMES.items():
+        assert lib.vn_status_string(code).decode().startswith(name)
+    assert lib.vn_version() >> 16 == 1
+
+
+def _dump(lib, seeds, pop, n, out):
+    return lib.vn_noise_dump(P(seeds), pop, n, 0, P(out), P(0))
+
+
+def test_validation_refuses_before_launch(lib):
+    fake = 0x1000  # never dereferenced: every call below fails validation first
+    assert _dump(lib, fake, -1, 4, fake) == 2                      # VN_ERR_SHAPE
+    assert _dump(lib, 0, 4, 4, fake) == 1                          # VN_ERR_NULL
+    assert _dump(lib, fake + 4, 4, 4, fake) == 5                   # VN_ERR_ALIGN (seeds)
+    assert _dump(lib, fake, 1 << 40, 1 << 40, fake) == 6           # VN_ERR_OVERFLOW
+    # gradients: pop >= 1, sigma finite and nonzero
+    g = lib.vn_weight_gradient
+    assert g(P(fake), P(fake), 0, 4, 4, 0.1, 0, P(fake), P(0)) == 2
+    assert g(P(fake), P(fake), 4, 4, 4, 0.0, 0, P(fake), P(0)) == 4
+    assert g(P(fake), P(fake), 4, 4, 4, float("nan"), 0, P(fake), P(0)) == 4
+    assert g(P(fake), P(fake), 4, 4, 4, 1e300, 0, P(fake), P(0)) == 4
+    assert g(P(fake), P(0), 4, 4, 4, 0.1, 0, P(fake), P(0)) == 1
+    assert g(P(fake + 2), P(fake), 4, 4, 4, 0.1, 0, P(fake), P(0)) == 5
+    assert lib.vn_bias_gradient(P(fake), P(fake), 4, -1, 0.1, 0, P(fake), P(0)) == 2
+    # reduce metric: n_params >= 1
+    assert lib.vn_reduce_metric(P(fake), P(fake), 4, 0, 0.1, 0, P(fake), P(0)) == 2
+    assert lib.vn_reduce_metric(P(fake), P(fake), 4, 8, float("inf"), 0, P(fake), P(0)) == 4
+    # forward: dtype rules, shapes, enums
+    f = lib.vn_perturbed_linear_ex
+    args = lambda **k: dict(dict(x=fake, xd=0, sh=0, w=fake, wd=0, b=0, bd=0, s=fake, pop=2, batch=2,
+                                 i=4, o=4, sig=0.1, off=0, y=fake, yd=0, path=0, act=0), **k)
+
+    def call(**k):
+        a = args(**k)
+        return f(P(a["x"]), a["xd"], a["sh"], P(a["w"]), a["wd"], P(a["b"]), a["bd"], P(a["s"]),
+                 a["pop"], a["batch"], a["i"], a["o"], a["sig"], a["off"], P(a["y"]), a["yd"],
+                 a["path"], a["act"], P(0))
+    assert call(xd=7) == 3                         # unknown dtype
+    assert call(xd=1, wd=1, yd=0) == 3             # bf16 x bf16 must give bf16
+    assert call(xd=1, wd=0, yd=1) == 3             # mixed gives fp32
+    assert call(path=9) == 10                      # unknown path
+    assert call(act=5) == 4                        # unknown activation
+    assert call(batch=-1) == 2
+    assert call(sig=float("nan")) == 4
+    assert call(pop=1 << 40, batch=1 << 40) == 6
+    assert call(s=0) == 1
+    assert call(y=fake + 1) == 5
+    assert call(x=0) == 1
+    assert call(w=0) == 1
+
+
+def test_empty_outputs_are_valid_and_launch_nothing(lib):
+    assert _dump(lib, 0, 0, 100, 0) == 0
+    assert _dump(lib, 0, 100, 0, 0) == 0
+    assert lib.vn_weight_gradient(P(0), P(0), 3, 0, 5, 0.1, 0, P(0), P(0)) == 0
+    assert lib.vn_reduce_metric(P(0), P(0), 0, 5, 0.1, 0, P(0), P(0)) == 0
+    assert lib.vn_perturbed_linear(P(0), 0, 0, P(0), 0, P(0), 0, P(0), 0, 4, 4, 4, 0.1, 0,
+                                   P(0), 0, P(0)) == 0

@@ -1,0 +1,27 @@
+"""Virtual-noise evolution strategies on one GB300 (sm_103a).
+
+The population ES step of the EvoX API page
+"evox.triton_kernels.kernels.virtual_noise" -- the perturbed linear forward,
+the weight / bias gradient estimates, the noise dump and the mean-abs metric --
+as a C-ABI CUDA library (``libvn.so``, declared in ``include/vn.h``) with a thin
+Python binding. The noise is regenerated on the fly from (seed, element index)
+and never materialised.
+"""
+
+from .api import (  # noqa: F401
+    VNError,
+    compute_offsets,
+    device_status,
+    noise_dump,
+    perturbed_linear_path,
+    virtual_bias_gradient,
+    virtual_perturbed_linear,
+    virtual_reduce_metric,
+    virtual_weight_gradient,
+)
+
+__all__ = [
+    "VNError", "compute_offsets", "device_status", "noise_dump", "perturbed_linear_path",
+    "virtual_bias_gradient", "virtual_perturbed_linear", "virtual_reduce_metric",
+    "virtual_weight_gradient",
+]

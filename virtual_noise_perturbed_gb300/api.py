@@ -1,0 +1,197 @@
+"""Python API with the EvoX page's names and signatures, over the C ABI.
+
+EvoX API page "evox.triton_kernels.kernels.virtual_noise": API entries
+``virtual_perturbed_linear``, ``virtual_weight_gradient``,
+``virtual_bias_gradient``, ``virtual_reduce_metric``, ``compute_offsets`` and
+the ``_cpu_normal_noise`` contract (here ``noise_dump``).
+
+These functions only check and marshal arguments (contiguity, integer seeds
+widened to int64, output allocation) and call ``libvn.so`` on the current
+CUDA stream; all arithmetic runs in the library's kernels. Tensors must be on
+a CUDA device; there is no CPU path.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+from typing import Optional, Sequence
+
+import torch
+
+from . import _lib
+from ._lib import VNError, check, load
+
+_DT = {torch.float32: _lib.VN_F32, torch.bfloat16: _lib.VN_BF16}
+_PATHS = {"auto": _lib.VN_PATH_AUTO, "ffma": _lib.VN_PATH_FFMA, "tc": _lib.VN_PATH_TC}
+_ACTS = {None: _lib.VN_ACT_NONE, "none": _lib.VN_ACT_NONE, "tanh": _lib.VN_ACT_TANH}
+_M64 = (1 << 64) - 1
+
+
+def _cuda(t: torch.Tensor, name: str) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    return t.contiguous()
+
+
+def _dt(t: torch.Tensor, name: str) -> int:
+    try:
+        return _DT[t.dtype]
+    except KeyError:
+        raise TypeError(f"{name}: dtype {t.dtype} is not supported (float32 or bfloat16)") from None
+
+
+def _seeds(seeds: torch.Tensor) -> torch.Tensor:
+    seeds = _cuda(seeds, "seeds")
+    if seeds.dim() != 1:
+        raise ValueError("seeds must be 1-D")
+    if seeds.dtype not in (torch.int64, torch.int32, torch.int16, torch.int8, torch.uint8):
+        raise TypeError(f"seeds must be an integer tensor, got {seeds.dtype}")
+    return seeds.to(torch.int64)
+
+
+def _stream(t: torch.Tensor) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> ctypes.c_void_p:
+    return ctypes.c_void_p(0 if t is None or t.numel() == 0 else t.data_ptr())
+
+
+def virtual_perturbed_linear(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Tensor],
+                             seeds: torch.Tensor, sigma: float, offset: int, *,
+                             activation: Optional[str] = None, path: str = "auto",
+                             out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Y[i] = X[i] @ (W + sigma*N_i)^T + (b + sigma*nb_i), shape (pop, batch, out).
+
+    x is (batch, in) (shared by every individual) or (pop, batch, in). The
+    result dtype is torch.result_type(x, weight). ``activation="tanh"`` applies
+    tanh to Y in the kernel's epilogue; ``path`` forces "ffma" or "tc"."""
+    lib = load()
+    x = _cuda(x, "x")
+    weight = _cuda(weight, "weight")
+    seeds = _seeds(seeds)
+    if weight.dim() != 2:
+        raise ValueError("weight must be (out_features, in_features)")
+    out_f, in_f = weight.shape
+    pop = seeds.numel()
+    if x.dim() == 2:
+        shared, batch = 1, x.shape[0]
+    elif x.dim() == 3:
+        if x.shape[0] != pop:
+            raise ValueError(f"x has {x.shape[0]} individuals but there are {pop} seeds")
+        shared, batch = 0, x.shape[1]
+    else:
+        raise ValueError("x must be (batch, in) or (pop, batch, in)")
+    if x.shape[-1] != in_f:
+        raise ValueError(f"x has {x.shape[-1]} features, weight expects {in_f}")
+    if bias is not None:
+        bias = _cuda(bias, "bias")
+        if bias.shape != (out_f,):
+            raise ValueError(f"bias must have shape ({out_f},)")
+    ydt = torch.bfloat16 if (x.dtype == torch.bfloat16 and weight.dtype == torch.bfloat16) else torch.float32
+    if out is None:
+        out = torch.empty((pop, batch, out_f), dtype=ydt, device=x.device)
+    elif out.shape != (pop, batch, out_f) or out.dtype != ydt or not out.is_contiguous():
+        raise ValueError("out has the wrong shape, dtype or layout")
+    if activation not in _ACTS or path not in _PATHS:
+        raise ValueError("activation must be None/'tanh'; path 'auto'/'ffma'/'tc'")
+    st = lib.vn_perturbed_linear_ex(
+        _ptr(x), _dt(x, "x"), shared, _ptr(weight), _dt(weight, "weight"),
+        _ptr(bias), _dt(bias, "bias") if bias is not None else 0,
+        _ptr(seeds), pop, batch, in_f, out_f, float(sigma), int(offset) & _M64,
+        _ptr(out), _DT[ydt], _PATHS[path], _ACTS[activation], _stream(x))
+    check(st, "vn_perturbed_linear")
+    return out
+
+
+def _fitness(fitness: torch.Tensor, pop_size: int, seeds: torch.Tensor) -> torch.Tensor:
+    fitness = _cuda(fitness, "fitness").reshape(-1).to(torch.float32)
+    if fitness.numel() != pop_size or seeds.numel() != pop_size:
+        raise ValueError(f"pop_size={pop_size} but {seeds.numel()} seeds and "
+                         f"{fitness.numel()} fitness values")
+    return fitness
+
+
+def virtual_weight_gradient(fitness: torch.Tensor, seeds: torch.Tensor, weight_shape: Sequence[int],
+                            sigma: float, pop_size: int, offset: int) -> torch.Tensor:
+    """grad[j, k] = sum_i fitness_i * N_i[j, k] / (pop_size * sigma), fp32, weight_shape."""
+    lib = load()
+    seeds = _seeds(seeds)
+    fitness = _fitness(fitness, pop_size, seeds)
+    out_f, in_f = (int(d) for d in weight_shape)
+    g = torch.empty((out_f, in_f), dtype=torch.float32, device=fitness.device)
+    st = lib.vn_weight_gradient(_ptr(fitness), _ptr(seeds), pop_size, out_f, in_f, float(sigma),
+                                int(offset) & _M64, _ptr(g), _stream(g))
+    check(st, "vn_weight_gradient")
+    return g
+
+
+def virtual_bias_gradient(fitness: torch.Tensor, seeds: torch.Tensor, bias_shape: Sequence[int],
+                          sigma: float, pop_size: int, offset: int) -> torch.Tensor:
+    """grad[j] = sum_i fitness_i * nb_i[j] / (pop_size * sigma); ``offset`` points at the bias region."""
+    lib = load()
+    seeds = _seeds(seeds)
+    fitness = _fitness(fitness, pop_size, seeds)
+    (out_f,) = (int(d) for d in bias_shape)
+    g = torch.empty((out_f,), dtype=torch.float32, device=fitness.device)
+    st = lib.vn_bias_gradient(_ptr(fitness), _ptr(seeds), pop_size, out_f, float(sigma),
+                              int(offset) & _M64, _ptr(g), _stream(g))
+    check(st, "vn_bias_gradient")
+    return g
+
+
+def noise_dump(seeds: torch.Tensor, n_elements: int, offset: int) -> torch.Tensor:
+    """(pop, n) fp32 centered-uniform noise, D[i, t] = PRNG(seed_i, offset + t)."""
+    lib = load()
+    seeds = _seeds(seeds)
+    d = torch.empty((seeds.numel(), int(n_elements)), dtype=torch.float32, device=seeds.device)
+    st = lib.vn_noise_dump(_ptr(seeds), seeds.numel(), int(n_elements), int(offset) & _M64,
+                           _ptr(d), _stream(d))
+    check(st, "vn_noise_dump")
+    return d
+
+
+def virtual_reduce_metric(center: torch.Tensor, seeds: torch.Tensor, sigma: float, n_params: int,
+                          offset: int = 0) -> torch.Tensor:
+    """fitness[i] = mean_k |center[k] + sigma * noise[i, k]|, (pop,) fp32."""
+    lib = load()
+    center = _cuda(center, "center").reshape(-1).to(torch.float32)
+    if center.numel() != n_params:
+        raise ValueError(f"center has {center.numel()} elements, n_params={n_params}")
+    seeds = _seeds(seeds)
+    f = torch.empty((seeds.numel(),), dtype=torch.float32, device=center.device)
+    st = lib.vn_reduce_metric(_ptr(center), _ptr(seeds), seeds.numel(), int(n_params), float(sigma),
+                              int(offset) & _M64, _ptr(f), _stream(f))
+    check(st, "vn_reduce_metric")
+    return f
+
+
+def compute_offsets(param_shapes: Sequence[Sequence[int]]) -> list:
+    """Start offset of each parameter block: the element count of all blocks before it."""
+    offsets, total = [], 0
+    for shape in param_shapes:
+        offsets.append(total)
+        total += math.prod(int(d) for d in shape)
+    return offsets
+
+
+def perturbed_linear_path(x: torch.Tensor, weight: torch.Tensor) -> str:
+    """"tc" or "ffma": the kernel ``virtual_perturbed_linear`` would use (no launch)."""
+    lib = load()
+    batch = x.shape[-2]
+    p = lib.vn_perturbed_linear_path(_ptr(x), _dt(x, "x"), int(x.dim() == 2), _ptr(weight),
+                                     _dt(weight, "weight"), batch, weight.shape[1], weight.shape[0])
+    return "tc" if p == _lib.VN_PATH_TC else "ffma"
+
+
+def device_status(device=None) -> None:
+    """Synchronise the current stream and raise VNError if a kernel recorded an expired wait."""
+    lib = load()
+    s = torch.cuda.current_stream(device)
+    check(lib.vn_device_status(ctypes.c_void_p(s.cuda_stream)), "vn_device_status")
+
+
+__all__ = ["virtual_perturbed_linear", "virtual_weight_gradient", "virtual_bias_gradient",
+           "noise_dump", "virtual_reduce_metric", "compute_offsets", "perturbed_linear_path",
+           "device_status", "VNError"]

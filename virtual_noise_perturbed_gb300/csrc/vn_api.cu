@@ -1,0 +1,226 @@
+// vn_api.cu -- the C ABI declared in include/vn.h: host-side validation,
+// path selection and launch. Every argument is checked here, before anything
+// touches the device; a failing check returns its status and launches nothing.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "vn.h"
+#include "vn_internal.h"
+
+namespace vn {
+
+cudaError_t device_info(DeviceInfo* info) {
+  constexpr int kMaxDevices = 64;
+  static DeviceInfo cache[kMaxDevices];
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  DeviceInfo& c = cache[dev];
+  if (c.device != dev) {
+    DeviceInfo d;
+    d.device = dev;
+    if ((err = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+        (err = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (err = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (err = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
+      return err;
+    c = d;
+  }
+  *info = c;
+  return cudaSuccess;
+}
+
+}  // namespace vn
+
+namespace {
+
+thread_local char g_last_error[256] = "";
+
+vn_status cuda_failure(cudaError_t err) {
+  std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s", cudaGetErrorName(err),
+                cudaGetErrorString(err));
+  return VN_ERR_CUDA;
+}
+
+vn_status launched(cudaError_t err) { return err == cudaSuccess ? VN_OK : cuda_failure(err); }
+
+bool dtype_ok(vn_dtype d) { return d == VN_F32 || d == VN_BF16; }
+size_t dtype_size(vn_dtype d) { return d == VN_BF16 ? 2 : 4; }
+bool aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
+
+// r = a * b, false when it does not fit in int64 (inputs are >= 0).
+bool mul(int64_t a, int64_t b, int64_t* r) { return !__builtin_mul_overflow(a, b, r); }
+
+bool float_sigma(double sigma, float* out) {
+  if (!std::isfinite(sigma)) return false;
+  const float f = static_cast<float>(sigma);
+  if (!std::isfinite(f)) return false;
+  *out = f;
+  return true;
+}
+
+bool device_is_cc10(const vn::DeviceInfo& d) { return d.cc_major == 10; }
+
+}  // namespace
+
+extern "C" {
+
+const char* vn_status_string(vn_status s) {
+  switch (s) {
+    case VN_OK: return "VN_OK";
+    case VN_ERR_NULL: return "VN_ERR_NULL: a required pointer is NULL";
+    case VN_ERR_SHAPE: return "VN_ERR_SHAPE: invalid size";
+    case VN_ERR_DTYPE: return "VN_ERR_DTYPE: unsupported dtype or dtype combination";
+    case VN_ERR_VALUE: return "VN_ERR_VALUE: invalid value (sigma, enum)";
+    case VN_ERR_ALIGN: return "VN_ERR_ALIGN: pointer not aligned to its element size";
+    case VN_ERR_OVERFLOW: return "VN_ERR_OVERFLOW: size product does not fit in int64";
+    case VN_ERR_TIMEOUT: return "VN_ERR_TIMEOUT: a device-side bounded wait ran out";
+    case VN_ERR_CUDA: return "VN_ERR_CUDA: a CUDA runtime call failed";
+    case VN_ERR_DEVICE: return "VN_ERR_DEVICE: this path needs a compute capability 10.x GPU";
+    case VN_ERR_PATH: return "VN_ERR_PATH: the forced path cannot run these arguments";
+  }
+  return "unknown vn_status";
+}
+
+const char* vn_last_error_message(void) { return g_last_error; }
+
+int vn_version(void) { return (1 << 16) | 0; }
+
+vn_status vn_noise_dump(const int64_t* seeds, int64_t pop, int64_t n, uint64_t offset,
+                        float* out, void* stream) {
+  if (pop < 0 || n < 0) return VN_ERR_SHAPE;
+  int64_t total;
+  if (!mul(pop, n, &total)) return VN_ERR_OVERFLOW;
+  if (total == 0) return VN_OK;
+  if (seeds == nullptr || out == nullptr) return VN_ERR_NULL;
+  if (!aligned(seeds, 8) || !aligned(out, 4)) return VN_ERR_ALIGN;
+  return launched(vn::launch_noise_dump(seeds, pop, n, offset, out,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+static vn_status gradient(const float* fitness, const int64_t* seeds, int64_t pop, int64_t m_rows,
+                          int64_t m_cols, double sigma, uint64_t offset, float* grad,
+                          void* stream) {
+  if (pop < 1 || m_rows < 0 || m_cols < 0) return VN_ERR_SHAPE;
+  int64_t m;
+  if (!mul(m_rows, m_cols, &m)) return VN_ERR_OVERFLOW;
+  float sig;
+  if (!float_sigma(sigma, &sig) || sig == 0.f) return VN_ERR_VALUE;
+  const double inv = 1.0 / (static_cast<double>(pop) * sigma);
+  const float scale = static_cast<float>(inv);
+  if (!std::isfinite(scale) || scale == 0.f) return VN_ERR_VALUE;
+  if (m == 0) return VN_OK;
+  if (fitness == nullptr || seeds == nullptr || grad == nullptr) return VN_ERR_NULL;
+  if (!aligned(fitness, 4) || !aligned(seeds, 8) || !aligned(grad, 4)) return VN_ERR_ALIGN;
+  return launched(vn::launch_grad(fitness, seeds, pop, m, offset, scale, grad,
+                                  static_cast<cudaStream_t>(stream)));
+}
+
+vn_status vn_weight_gradient(const float* fitness, const int64_t* seeds, int64_t pop,
+                             int64_t out, int64_t in, double sigma, uint64_t offset,
+                             float* grad_w, void* stream) {
+  return gradient(fitness, seeds, pop, out, in, sigma, offset, grad_w, stream);
+}
+
+vn_status vn_bias_gradient(const float* fitness, const int64_t* seeds, int64_t pop,
+                           int64_t out, double sigma, uint64_t offset, float* grad_b,
+                           void* stream) {
+  return gradient(fitness, seeds, pop, out, 1, sigma, offset, grad_b, stream);
+}
+
+vn_status vn_reduce_metric(const float* center, const int64_t* seeds, int64_t pop,
+                           int64_t n_params, double sigma, uint64_t offset, float* fitness,
+                           void* stream) {
+  if (pop < 0 || n_params < 1) return VN_ERR_SHAPE;
+  float sig;
+  if (!float_sigma(sigma, &sig)) return VN_ERR_VALUE;
+  int64_t total;
+  if (!mul(pop, n_params, &total)) return VN_ERR_OVERFLOW;
+  if (pop == 0) return VN_OK;
+  if (center == nullptr || seeds == nullptr || fitness == nullptr) return VN_ERR_NULL;
+  if (!aligned(center, 4) || !aligned(seeds, 8) || !aligned(fitness, 4)) return VN_ERR_ALIGN;
+  const float inv_n = static_cast<float>(1.0 / static_cast<double>(n_params));
+  return launched(vn::launch_reduce_metric(center, seeds, pop, n_params, sig, inv_n, offset,
+                                           fitness, static_cast<cudaStream_t>(stream)));
+}
+
+vn_path vn_perturbed_linear_path(const void* x, vn_dtype x_dt, int x_shared, const void* w,
+                                 vn_dtype w_dt, int64_t batch, int64_t in, int64_t out) {
+  (void)x_shared;
+  vn::DeviceInfo dev;
+  if (vn::device_info(&dev) != cudaSuccess || !device_is_cc10(dev)) return VN_PATH_FFMA;
+  return vn::linear_tc_applies(x, x_dt, w, w_dt, batch, in, out) ? VN_PATH_TC : VN_PATH_FFMA;
+}
+
+vn_status vn_perturbed_linear_ex(const void* x, vn_dtype x_dt, int x_shared, const void* w,
+                                 vn_dtype w_dt, const void* b, vn_dtype b_dt,
+                                 const int64_t* seeds, int64_t pop, int64_t batch, int64_t in,
+                                 int64_t out, double sigma, uint64_t offset, void* y,
+                                 vn_dtype y_dt, vn_path path, vn_act act, void* stream) {
+  if (!dtype_ok(x_dt) || !dtype_ok(w_dt) || (b != nullptr && !dtype_ok(b_dt)) || !dtype_ok(y_dt))
+    return VN_ERR_DTYPE;
+  const vn_dtype want_y = (x_dt == VN_BF16 && w_dt == VN_BF16) ? VN_BF16 : VN_F32;
+  if (y_dt != want_y) return VN_ERR_DTYPE;
+  if (path != VN_PATH_AUTO && path != VN_PATH_FFMA && path != VN_PATH_TC) return VN_ERR_PATH;
+  if (act != VN_ACT_NONE && act != VN_ACT_TANH) return VN_ERR_VALUE;
+  if (pop < 0 || batch < 0 || in < 0 || out < 0) return VN_ERR_SHAPE;
+  float sig;
+  if (!float_sigma(sigma, &sig)) return VN_ERR_VALUE;
+  int64_t x_elems, y_elems, w_elems, t;
+  if (!mul(batch, in, &x_elems) || (!x_shared && !mul(x_elems, pop, &x_elems)) ||
+      !mul(pop, batch, &t) || !mul(t, out, &y_elems) || !mul(out, in, &w_elems))
+    return VN_ERR_OVERFLOW;
+  if (y_elems == 0) return VN_OK;
+  if (seeds == nullptr || y == nullptr || (x_elems > 0 && x == nullptr) ||
+      (w_elems > 0 && w == nullptr))
+    return VN_ERR_NULL;
+  if (!aligned(seeds, 8) || !aligned(y, dtype_size(y_dt)) || !aligned(x, dtype_size(x_dt)) ||
+      !aligned(w, dtype_size(w_dt)) || (b != nullptr && !aligned(b, dtype_size(b_dt))))
+    return VN_ERR_ALIGN;
+
+  vn::LinearArgs a;
+  a.x = x; a.x_dt = x_dt; a.x_shared = x_shared ? 1 : 0;
+  a.w = w; a.w_dt = w_dt; a.b = b; a.b_dt = b_dt;
+  a.seeds = seeds; a.pop = pop; a.batch = batch; a.in = in; a.out = out;
+  a.sigma = sig; a.offset = offset; a.y = y; a.y_dt = y_dt; a.act = act;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  if (path == VN_PATH_FFMA) return launched(vn::launch_linear_ffma(a, s));
+  vn::DeviceInfo dev;
+  cudaError_t err = vn::device_info(&dev);
+  if (err != cudaSuccess) return cuda_failure(err);
+  const bool tc_ok = vn::linear_tc_applies(x, x_dt, w, w_dt, batch, in, out);
+  if (path == VN_PATH_TC) {
+    if (!device_is_cc10(dev)) return VN_ERR_DEVICE;
+    if (!tc_ok) return VN_ERR_PATH;
+    return launched(vn::launch_linear_tc(a, s));
+  }
+  if (tc_ok && device_is_cc10(dev)) return launched(vn::launch_linear_tc(a, s));
+  return launched(vn::launch_linear_ffma(a, s));
+}
+
+vn_status vn_perturbed_linear(const void* x, vn_dtype x_dt, int x_shared, const void* w,
+                              vn_dtype w_dt, const void* b, vn_dtype b_dt, const int64_t* seeds,
+                              int64_t pop, int64_t batch, int64_t in, int64_t out, double sigma,
+                              uint64_t offset, void* y, vn_dtype y_dt, void* stream) {
+  return vn_perturbed_linear_ex(x, x_dt, x_shared, w, w_dt, b, b_dt, seeds, pop, batch, in, out,
+                                sigma, offset, y, y_dt, VN_PATH_AUTO, VN_ACT_NONE, stream);
+}
+
+vn_status vn_device_status(void* stream) {
+  cudaError_t err = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_failure(err);
+  unsigned int status = 0;
+  err = vn::take_device_status(&status, static_cast<cudaStream_t>(stream));
+  if (err != cudaSuccess) return cuda_failure(err);
+  return status ? VN_ERR_TIMEOUT : VN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,66 @@
+// vn_internal.h -- launchers shared between the C-ABI layer (vn_api.cu) and
+// the kernel translation units. Arguments reaching these functions have been
+// validated by the C-ABI layer: pointers non-null and aligned, sizes >= 1 and
+// their products below 2^63.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "vn.h"
+
+namespace vn {
+
+// Cached per-device facts (SM count, compute capability, opt-in shared memory).
+struct DeviceInfo {
+  int device = -1;
+  int sm_count = 0;
+  int cc_major = 0;
+  int cc_minor = 0;
+  int smem_optin = 0;
+};
+cudaError_t device_info(DeviceInfo* info);
+
+// out[i, t] = PRNG(seed_i, offset + t), t < n.
+cudaError_t launch_noise_dump(const int64_t* seeds, int64_t pop, int64_t n, uint64_t offset,
+                              float* out, cudaStream_t stream);
+
+// out[e] = scale * sum_i fitness[i] * PRNG(seed_i, offset + e), e < m.
+cudaError_t launch_grad(const float* fitness, const int64_t* seeds, int64_t pop, int64_t m,
+                        uint64_t offset, float scale, float* out, cudaStream_t stream);
+
+// fitness[i] = inv_n * sum_k |center[k] + sigma * PRNG(seed_i, offset + k)|.
+cudaError_t launch_reduce_metric(const float* center, const int64_t* seeds, int64_t pop,
+                                 int64_t n, float sigma, float inv_n, uint64_t offset,
+                                 float* fitness, cudaStream_t stream);
+
+struct LinearArgs {
+  const void* x;
+  vn_dtype x_dt;
+  int x_shared;
+  const void* w;
+  vn_dtype w_dt;
+  const void* b;  // may be null
+  vn_dtype b_dt;
+  const int64_t* seeds;
+  int64_t pop, batch, in, out;
+  float sigma;
+  uint64_t offset;
+  void* y;
+  vn_dtype y_dt;
+  vn_act act;
+};
+
+// CUDA-core forward: any dtypes, any batch.
+cudaError_t launch_linear_ffma(const LinearArgs& a, cudaStream_t stream);
+
+// Whether the tcgen05 forward can run these arguments (shape/alignment/dtype).
+bool linear_tc_applies(const void* x, vn_dtype x_dt, const void* w, vn_dtype w_dt,
+                       int64_t batch, int64_t in, int64_t out);
+// tcgen05/TMEM forward (x bf16).
+cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream);
+
+// Reads and clears the device status word of the bounded-wait kernels (0 = fine).
+cudaError_t take_device_status(unsigned int* status, cudaStream_t stream);
+
+}  // namespace vn

@@ -1,0 +1,138 @@
+// vn_noise.cu -- the noise dump and the mean-abs reduction metric.
+//
+// Noise dump: the "_cpu_normal_noise" contract of the EvoX API page
+// "evox.triton_kernels.kernels.virtual_noise": out[i, t] = PRNG(seed_i, offset + t).
+// Reduction metric: the page's "virtual_reduce_metric":
+//   fitness[i] = mean_k |center[k] + sigma * PRNG(seed_i, offset + k)|.
+//
+// Both are bound by the integer hash (about 20 32-bit integer operations per
+// element) and, for the dump, by the 4-byte store per element. Each thread
+// works on groups of 4 consecutive elements so that the state of the next
+// element is the previous one plus GAMMA (a two-operation 64-bit add) and the
+// dump writes one 16-byte store per group.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "vn_hash.cuh"
+#include "vn_internal.h"
+
+namespace vn {
+namespace {
+
+constexpr int kDumpThreads = 256;
+constexpr int kDumpGroups = 4;                                  // groups of 4 per thread
+constexpr int64_t kDumpChunk = kDumpThreads * 4 * kDumpGroups;  // elements per CTA step
+
+// Grid-stride over (row i, chunk of kDumpChunk columns). vec4: every row starts
+// 16-byte aligned (out aligned and n % 4 == 0), so groups are stored as float4.
+__global__ void __launch_bounds__(kDumpThreads)
+noise_dump_kernel(const int64_t* __restrict__ seeds, int64_t n, uint64_t offset,
+                  float* __restrict__ out, int64_t chunks_per_row, int64_t total_chunks,
+                  int vec4) {
+  for (int64_t c = blockIdx.x; c < total_chunks; c += gridDim.x) {
+    const int64_t i = c / chunks_per_row;
+    const int64_t t_base = (c - i * chunks_per_row) * kDumpChunk;
+    const uint64_t seed = static_cast<uint64_t>(__ldg(seeds + i));
+    float* row = out + i * n;
+#pragma unroll
+    for (int g = 0; g < kDumpGroups; ++g) {
+      const int64_t t = t_base + g * (kDumpThreads * 4) + threadIdx.x * 4;
+      if (t < n) {
+        uint32_t lo, hi;
+        index_term(offset + static_cast<uint64_t>(t), lo, hi);
+        add64(lo, hi, static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
+        float v[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          v[q] = noise_from_bits(mix_to_one_plus_u(lo, hi));
+          add64(lo, hi, kGammaLo, kGammaHi);
+        }
+        if (vec4 && t + 4 <= n) {
+          __stcs(reinterpret_cast<float4*>(row + t), make_float4(v[0], v[1], v[2], v[3]));
+        } else {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (t + q < n) row[t + q] = v[q];
+        }
+      }
+    }
+  }
+}
+
+constexpr int kMetricThreads = 256;
+
+// One CTA per individual (grid-stride over individuals). Each thread sums
+// |center[k] + sigma*n| over k = 4*tid + 1024*g + q; the block then adds the
+// partial sums in a fixed order.
+__global__ void __launch_bounds__(kMetricThreads)
+reduce_metric_kernel(const float* __restrict__ center, const int64_t* __restrict__ seeds,
+                     int64_t pop, int64_t n, float sigma, float inv_n, uint64_t offset,
+                     float* __restrict__ fitness, int vec4) {
+  __shared__ float s_warp[kMetricThreads / 32];
+  for (int64_t i = blockIdx.x; i < pop; i += gridDim.x) {
+    const uint64_t seed = static_cast<uint64_t>(__ldg(seeds + i));
+    float acc = 0.f;
+    for (int64_t k = static_cast<int64_t>(threadIdx.x) * 4; k < n; k += kMetricThreads * 4) {
+      uint32_t lo, hi;
+      index_term(offset + static_cast<uint64_t>(k), lo, hi);
+      add64(lo, hi, static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
+      float c[4];
+      if (vec4 && k + 4 <= n) {
+        const float4 c4 = __ldg(reinterpret_cast<const float4*>(center + k));
+        c[0] = c4.x; c[1] = c4.y; c[2] = c4.z; c[3] = c4.w;
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) c[q] = (k + q < n) ? __ldg(center + k + q) : 0.f;
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float v = fabsf(fmaf(sigma, noise_from_bits(mix_to_one_plus_u(lo, hi)), c[q]));
+        if (k + q < n) acc += v;
+        add64(lo, hi, kGammaLo, kGammaHi);
+      }
+    }
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) acc += __shfl_down_sync(0xffffffffu, acc, s);
+    if ((threadIdx.x & 31) == 0) s_warp[threadIdx.x >> 5] = acc;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float total = 0.f;
+#pragma unroll
+      for (int w = 0; w < kMetricThreads / 32; ++w) total += s_warp[w];
+      fitness[i] = total * inv_n;
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_noise_dump(const int64_t* seeds, int64_t pop, int64_t n, uint64_t offset,
+                              float* out, cudaStream_t stream) {
+  DeviceInfo dev;
+  cudaError_t err = device_info(&dev);
+  if (err != cudaSuccess) return err;
+  const int64_t chunks_per_row = (n + kDumpChunk - 1) / kDumpChunk;
+  const int64_t total = pop * chunks_per_row;
+  const int vec4 = (n % 4 == 0) && (reinterpret_cast<uintptr_t>(out) % 16 == 0);
+  const int64_t grid = std::min<int64_t>(total, static_cast<int64_t>(dev.sm_count) * 8);
+  noise_dump_kernel<<<static_cast<unsigned>(grid), kDumpThreads, 0, stream>>>(
+      seeds, n, offset, out, chunks_per_row, total, vec4);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reduce_metric(const float* center, const int64_t* seeds, int64_t pop,
+                                 int64_t n, float sigma, float inv_n, uint64_t offset,
+                                 float* fitness, cudaStream_t stream) {
+  DeviceInfo dev;
+  cudaError_t err = device_info(&dev);
+  if (err != cudaSuccess) return err;
+  const int vec4 = (reinterpret_cast<uintptr_t>(center) % 16 == 0);
+  const int64_t grid = std::min<int64_t>(pop, static_cast<int64_t>(dev.sm_count) * 8);
+  reduce_metric_kernel<<<static_cast<unsigned>(grid), kMetricThreads, 0, stream>>>(
+      center, seeds, pop, n, sigma, inv_n, offset, fitness, vec4);
+  return cudaGetLastError();
+}
+
+}  // namespace vn
