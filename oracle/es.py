@@ -69,11 +69,11 @@ def weight_noise(seed, out_f: int, in_f: int, offset: int,
 
     ``rows`` selects which j to return (default: all, in order)."""
     s = seeds_u64([seed])[0]
-    rows = range(out_f) if rows is None else list(rows)
-    n = np.empty((len(rows), in_f), dtype=np.float64)
-    for r, j in enumerate(rows):
-        n[r] = noise_np(s, element_indices(offset + j * in_f, in_f))
-    return n
+    rows = np.arange(out_f, dtype=np.uint64) if rows is None else np.asarray(list(rows), dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        idx = (np.uint64(offset & ((1 << 64) - 1)) + rows[:, None] * np.uint64(in_f)
+               + np.arange(in_f, dtype=np.uint64)[None, :])        # offset + j*in + k
+    return noise_np(s, idx)
 
 
 def bias_noise(seed, out_f: int, bias_offset: int) -> np.ndarray:

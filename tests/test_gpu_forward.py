@@ -1,0 +1,138 @@
+"""GPU parity of the perturbed linear forward against the CPU oracle.
+
+fp32 (FFMA) path within 1e-4 of the oracle's RMS; bf16 tensor-core path within
+2e-2; one-hot inputs recover the noise bit for bit."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import es
+from tests.parity import TOL_BF16, TOL_FP32, assert_close, to_np
+from virtual_noise_perturbed_gb300 import (VNError, noise_dump, perturbed_linear_path,
+                                           virtual_perturbed_linear, workloads)
+from virtual_noise_perturbed_gb300.build import build
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build()
+
+
+def _case(pop, batch, in_f, out_f, *, shared=False, bias=True, xdt=torch.float32, wdt=torch.float32,
+          bdt=torch.float32, sigma=0.05, offset=12345, seed=0):
+    g = torch.Generator().manual_seed(seed + 17 * pop + batch)
+    x = torch.randn((batch, in_f) if shared else (pop, batch, in_f), generator=g).to(xdt)
+    w = (torch.randn((out_f, in_f), generator=g) / max(in_f, 1) ** 0.5).to(wdt)
+    b = (torch.randn(out_f, generator=g) * 0.1).to(bdt) if bias else None
+    seeds = torch.arange(pop, dtype=torch.int64) * 5 - 7
+    return x, w, b, seeds, sigma, offset
+
+
+def _run_and_check(x, w, b, seeds, sigma, offset, tol, path="auto", individuals=None, act=None):
+    y = virtual_perturbed_linear(x.to(DEV), w.to(DEV), None if b is None else b.to(DEV),
+                                 seeds.to(DEV), sigma, offset, path=path, activation=act)
+    want = es.perturbed_linear(x.float().numpy(), w.float().numpy(),
+                               None if b is None else b.float().numpy(), seeds.numpy(), sigma,
+                               offset, individuals=individuals)
+    if act == "tanh":
+        want = np.tanh(want)
+    got = to_np(y) if individuals is None else to_np(y)[individuals]
+    return assert_close(got, want, tol, f"forward {tuple(x.shape)}->{w.shape[0]} {path}")
+
+
+@pytest.mark.parametrize("pop,batch,in_f,out_f", [
+    (1, 1, 1, 1), (8, 4, 32, 16), (9, 1, 64, 256), (13, 3, 67, 33), (3, 8, 200, 5),
+    (5, 11, 130, 40), (17, 2, 1, 70), (2, 17, 257, 31)])
+def test_ffma_forward_matches_oracle(pop, batch, in_f, out_f):
+    _run_and_check(*_case(pop, batch, in_f, out_f), TOL_FP32, path="ffma")
+
+
+@pytest.mark.parametrize("shared,bias", [(True, True), (True, False), (False, False)])
+def test_ffma_forward_shared_x_and_no_bias(shared, bias):
+    _run_and_check(*_case(11, 3, 96, 45, shared=shared, bias=bias), TOL_FP32, path="ffma")
+
+
+@pytest.mark.parametrize("xdt,wdt,bdt", [(torch.bfloat16, torch.float32, torch.float32),
+                                         (torch.float32, torch.bfloat16, torch.bfloat16),
+                                         (torch.bfloat16, torch.bfloat16, torch.bfloat16)])
+def test_ffma_forward_bf16_inputs(xdt, wdt, bdt):
+    x, w, b, s, sig, off = _case(10, 2, 80, 50, xdt=xdt, wdt=wdt, bdt=bdt)
+    tol = TOL_BF16 if (xdt == torch.bfloat16 and wdt == torch.bfloat16) else TOL_FP32
+    _run_and_check(x, w, b, s, sig, off, tol, path="ffma")
+
+
+def test_ffma_forward_tanh_epilogue():
+    _run_and_check(*_case(12, 2, 64, 48), TOL_FP32, path="ffma", act="tanh")
+
+
+def test_forward_in_zero_is_bias_plus_bias_noise():
+    pop, out_f, off = 6, 9, 4242
+    b = torch.randn(out_f)
+    seeds = torch.arange(pop, dtype=torch.int64)
+    y = virtual_perturbed_linear(torch.empty((pop, 2, 0), device=DEV), torch.empty((out_f, 0), device=DEV),
+                                 b.to(DEV), seeds.to(DEV), 0.5, off, path="ffma")
+    nb = es.noise_dump(seeds.numpy(), out_f, off).astype(np.float64)
+    want = b.numpy().astype(np.float64)[None, None, :] + 0.5 * nb[:, None, :]
+    assert_close(to_np(y), np.broadcast_to(want, (pop, 2, out_f)), TOL_FP32, "in=0")
+
+
+@pytest.mark.parametrize("path", ["ffma"])
+def test_forward_one_hot_is_bit_exact(path):
+    """X rows = e_k, W = 0, b = 0, sigma = 1: Y[i, k, :] = N_i[:, k] + nb_i exactly."""
+    pop, in_f, out_f, off = 5, 64, 40, (1 << 32) - 300
+    x = torch.eye(in_f).repeat(pop, 1, 1)
+    seeds = torch.tensor([3, -4, 5, -6, 2 ** 62], dtype=torch.int64)
+    y = virtual_perturbed_linear(x.to(DEV), torch.zeros(out_f, in_f, device=DEV),
+                                 torch.zeros(out_f, device=DEV), seeds.to(DEV), 1.0, off, path=path)
+    dump = es.noise_dump(seeds.numpy(), out_f * in_f + out_f, off)
+    for i in range(pop):
+        n_i = dump[i, : out_f * in_f].reshape(out_f, in_f)
+        want = (n_i + dump[i, out_f * in_f:][:, None]).T
+        assert np.array_equal(y[i].cpu().numpy(), want)
+    # and the forward's noise is the dump's noise on the GPU as well
+    gdump = noise_dump(seeds.to(DEV), out_f * in_f, off).cpu().numpy()
+    y0 = virtual_perturbed_linear(x.to(DEV), torch.zeros(out_f, in_f, device=DEV), None,
+                                  seeds.to(DEV), 1.0, off, path=path)
+    for i in range(pop):
+        assert np.array_equal(y0[i].cpu().numpy(), gdump[i].reshape(out_f, in_f).T)
+
+
+def test_workload1_forward():
+    w = workloads.make(1)
+    l = w.layers[0]
+    _run_and_check(w.x, l.weight, l.bias, w.seeds, w.sigma, l.offset, TOL_FP32)
+
+
+def test_workload2_policy_forward():
+    """Three perturbed layers with tanh between, as the ES MLP policy step runs them."""
+    w = workloads.make(2)
+    h = w.x.to(DEV)
+    want = w.x.numpy().astype(np.float64)
+    for li, l in enumerate(w.layers):
+        act = "tanh" if li < len(w.layers) - 1 else None
+        h = virtual_perturbed_linear(h, l.weight.to(DEV), l.bias.to(DEV), w.seeds.to(DEV), w.sigma,
+                                     l.offset, activation=act)
+        want = es.perturbed_linear(want, l.weight.numpy(), l.bias.numpy(), w.seeds.numpy(), w.sigma,
+                                   l.offset)
+        if act:
+            want = np.tanh(want)
+        assert_close(to_np(h), want, TOL_FP32, f"w2 layer {li}")
+
+
+def test_invalid_forward_calls_raise():
+    x = torch.randn(2, 3, 8, device=DEV)
+    w = torch.randn(4, 8, device=DEV)
+    s = torch.arange(2, device=DEV)
+    with pytest.raises(ValueError):
+        virtual_perturbed_linear(x, torch.randn(4, 9, device=DEV), None, s, 0.1, 0)
+    with pytest.raises(ValueError):
+        virtual_perturbed_linear(x, w, None, torch.arange(3, device=DEV), 0.1, 0)
+    with pytest.raises(VNError):
+        virtual_perturbed_linear(x, w, None, s, float("inf"), 0)
+    with pytest.raises(TypeError):
+        virtual_perturbed_linear(x.half(), w, None, s, 0.1, 0)
+    assert perturbed_linear_path(x, w) == "ffma"  # fp32 x never takes the tensor-core path
