@@ -67,9 +67,10 @@ typedef enum vn_dtype { VN_F32 = 0, VN_BF16 = 1 } vn_dtype;
 
 /* Forward kernel selection for vn_perturbed_linear_ex. */
 typedef enum vn_path {
-  VN_PATH_AUTO = 0,  /* tensor-core path when it applies, else the FFMA path      */
-  VN_PATH_FFMA = 1,  /* CUDA-core path: any dtypes, any batch                     */
-  VN_PATH_TC = 2     /* tcgen05/TMEM path: x bf16, in % 8 == 0, 16-byte aligned   */
+  VN_PATH_AUTO = 0,  /* VN_PATH_TC when it applies and batch >= 16, else FFMA      */
+  VN_PATH_FFMA = 1,  /* CUDA-core path: any dtypes, any batch                       */
+  VN_PATH_TC = 2     /* tcgen05/TMEM path: x bf16, in % 8 == 0, x and w 16-byte     */
+                     /* aligned, pop, batch and in below 2^31                       */
 } vn_path;
 
 /* Element-wise activation applied to Y after the bias (vn_perturbed_linear_ex). */

@@ -136,3 +136,86 @@ def test_invalid_forward_calls_raise():
     with pytest.raises(TypeError):
         virtual_perturbed_linear(x.half(), w, None, s, 0.1, 0)
     assert perturbed_linear_path(x, w) == "ffma"  # fp32 x never takes the tensor-core path
+
+
+# ---------------------------------------------------------------------------
+# Tensor-core (tcgen05/TMEM) path
+# ---------------------------------------------------------------------------
+
+TC_CASES = [
+    # pop, batch, in, out, w dtype, shared, bias   (what each case exercises)
+    (3, 32, 128, 200, torch.bfloat16, False, True),    # two M tiles, ragged out
+    (5, 16, 64, 128, torch.float32, False, True),      # fp32 W, minimum N
+    (2, 40, 136, 130, torch.bfloat16, False, True),    # ragged batch (N=48) and K (136)
+    (11, 32, 192, 64, torch.float32, True, False),     # shared x, no bias, G=8 with a partial group
+    (2, 256, 128, 256, torch.bfloat16, False, True),   # N=256, two 128-row halves per unit
+    (1, 300, 64, 160, torch.bfloat16, False, True),    # batch > 256: two N tiles
+    (20, 24, 1032, 40, torch.float32, False, True),    # many k chunks, ragged last chunk
+]
+
+
+@pytest.mark.parametrize("pop,batch,in_f,out_f,wdt,shared,bias", TC_CASES)
+def test_tc_forward_matches_oracle(pop, batch, in_f, out_f, wdt, shared, bias):
+    x, w, b, s, sig, off = _case(pop, batch, in_f, out_f, shared=shared, bias=bias,
+                                 xdt=torch.bfloat16, wdt=wdt, bdt=wdt)
+    _run_and_check(x, w, b, s, sig, off, TOL_BF16, path="tc")
+
+
+def test_tc_forward_one_hot_reads_bf16_noise_exactly():
+    """X rows = e_k, W = 0, b = 0, sigma = 1 on the tensor-core path: the perturbed
+    weight is bf16(N_i[j, k]) and the fp32 accumulation of one product is exact, so
+    Y[i, k, :] = bf16(N_i[:, k]) + nb_i bit for bit. Pins the swizzled operand layout,
+    the descriptors and the TMEM addressing to the noise indexing."""
+    pop, in_f, out_f, off = 3, 64, 160, 777
+    x = torch.eye(in_f).repeat(pop, 1, 1).to(torch.bfloat16)
+    seeds = torch.tensor([9, -10, 11], dtype=torch.int64)
+    y = virtual_perturbed_linear(x.to(DEV), torch.zeros(out_f, in_f, dtype=torch.bfloat16, device=DEV),
+                                 torch.zeros(out_f, dtype=torch.bfloat16, device=DEV), seeds.to(DEV),
+                                 1.0, off, path="tc")
+    dump = torch.from_numpy(es.noise_dump(seeds.numpy(), out_f * in_f + out_f, off))
+    for i in range(pop):
+        n_bf = dump[i, : out_f * in_f].reshape(out_f, in_f).to(torch.bfloat16).float()
+        nb = dump[i, out_f * in_f:]
+        want = (n_bf + nb[:, None]).T.to(torch.bfloat16)   # Y is bf16 for bf16 x and W
+        assert torch.equal(y[i].cpu(), want)
+
+
+def test_tc_and_auto_path_selection():
+    x = torch.randn(2, 32, 64, device=DEV).to(torch.bfloat16)
+    w = torch.randn(16, 64, device=DEV)
+    assert perturbed_linear_path(x, w) == "tc"
+    assert perturbed_linear_path(x[:, :8], w) == "ffma"          # batch < 16
+    with pytest.raises(VNError):
+        virtual_perturbed_linear(torch.randn(2, 32, 60, device=DEV).to(torch.bfloat16),
+                                 torch.randn(16, 60, device=DEV), None, torch.arange(2, device=DEV),
+                                 0.1, 0, path="tc")                 # in % 8 != 0
+
+
+def test_tc_repeated_calls_are_identical_and_status_clean():
+    x, w, b, s, sig, off = _case(9, 32, 256, 256, xdt=torch.bfloat16, wdt=torch.float32)
+    args = (x.to(DEV), w.to(DEV), b.to(DEV), s.to(DEV), sig, off)
+    y1 = virtual_perturbed_linear(*args, path="tc")
+    y2 = virtual_perturbed_linear(*args, path="tc")
+    assert torch.equal(y1, y2)
+    from virtual_noise_perturbed_gb300 import device_status
+    device_status()
+
+
+def _workload_tc(number, individuals):
+    w = workloads.make(number)
+    l = w.layers[0]
+    y = virtual_perturbed_linear(w.x.to(DEV), l.weight.to(DEV), l.bias.to(DEV), w.seeds.to(DEV),
+                                 w.sigma, l.offset)
+    assert perturbed_linear_path(w.x.to(DEV)[:1], l.weight.to(DEV)) == "tc"
+    got = to_np(y[individuals])
+    want = es.perturbed_linear(w.x[individuals].float().numpy(), l.weight.float().numpy(),
+                               l.bias.float().numpy(), w.seeds[individuals].numpy(), w.sigma, l.offset)
+    return assert_close(got, want, TOL_BF16, f"workload {number}")
+
+
+def test_workload3_forward_full_size_windows():
+    _workload_tc(3, [0, 1, 7, 8, 2047, 4094, 4095])
+
+
+def test_workload5_forward_full_size_windows():
+    _workload_tc(5, [0, 128, 255])

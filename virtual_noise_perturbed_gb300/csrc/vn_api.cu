@@ -68,6 +68,10 @@ bool float_sigma(double sigma, float* out) {
 
 bool device_is_cc10(const vn::DeviceInfo& d) { return d.cc_major == 10; }
 
+// VN_PATH_AUTO takes the tensor-core path from this per-individual batch on:
+// below it the MMA's N of 16 would be mostly padding.
+constexpr int64_t kAutoTcMinBatch = 16;
+
 }  // namespace
 
 extern "C" {
@@ -156,7 +160,9 @@ vn_path vn_perturbed_linear_path(const void* x, vn_dtype x_dt, int x_shared, con
   (void)x_shared;
   vn::DeviceInfo dev;
   if (vn::device_info(&dev) != cudaSuccess || !device_is_cc10(dev)) return VN_PATH_FFMA;
-  return vn::linear_tc_applies(x, x_dt, w, w_dt, batch, in, out) ? VN_PATH_TC : VN_PATH_FFMA;
+  return (batch >= kAutoTcMinBatch && vn::linear_tc_applies(x, x_dt, w, w_dt, batch, in, out))
+             ? VN_PATH_TC
+             : VN_PATH_FFMA;
 }
 
 vn_status vn_perturbed_linear_ex(const void* x, vn_dtype x_dt, int x_shared, const void* w,
@@ -202,7 +208,8 @@ vn_status vn_perturbed_linear_ex(const void* x, vn_dtype x_dt, int x_shared, con
     if (!tc_ok) return VN_ERR_PATH;
     return launched(vn::launch_linear_tc(a, s));
   }
-  if (tc_ok && device_is_cc10(dev)) return launched(vn::launch_linear_tc(a, s));
+  if (tc_ok && batch >= kAutoTcMinBatch && device_is_cc10(dev))
+    return launched(vn::launch_linear_tc(a, s));
   return launched(vn::launch_linear_ffma(a, s));
 }
 

@@ -1,18 +1,636 @@
-// vn_linear_tc.cu -- tcgen05/TMEM perturbed linear (placeholder until the
-// tensor-core kernel lands): reports that the path does not apply.
+// vn_linear_tc.cu -- the perturbed linear on 5th-generation tensor cores
+// (tcgen05.mma, fp32 accumulators in TMEM, X staged by TMA).
+//
+// EvoX API page "evox.triton_kernels.kernels.virtual_noise", entry
+// "virtual_perturbed_linear" and the module description:
+//   Y[i] = X[i] @ (W + sigma*N_i)^T + (b + sigma*nb_i)
+// N_i[j,k] at offset + j*in + k, nb_i[j] at offset + out*in + j. The noise is
+// generated on the fly and added to the weight tile before the contraction
+// (the page's "added to the weight tile in registers"); no noise tensor exists.
+//
+// Per individual the product is D = W'_i X_i^T with D[j, n] = Y_i[n, j]:
+//   A = W'_i tile, 128 output rows x 64 k (bf16, K-major), written into shared
+//       memory by "hashing" warps in the 128-byte-swizzled canonical layout;
+//   B = X_i tile, NT batch rows x 64 k (bf16, K-major), loaded by TMA with the
+//       same 128-byte swizzle;
+//   D = fp32 accumulator in TMEM, 128 lanes (output rows) x NT columns (batch).
+// The contraction is tiny next to the hash work (one 64-bit splitmix64 hash per
+// weight element per individual, about 20 integer operations), so the kernel is
+// built around keeping the integer pipes busy:
+//   warp 0      TMA producer for X tiles (one thread);
+//   warp 1      TMEM allocator and MMA issuer (one thread);
+//   warps 2..5  epilogue: TMEM -> registers -> + b + sigma*nb -> Y (one per TMEM lane quarter);
+//   warps 6..13 hashing: W'_i = bf16(W + sigma*N_i), 16 bytes (8 k) per store.
+// A work unit is (group of G individuals, N tile, M tile of 128*MH output rows);
+// per k-chunk of 64 the unit's W elements are read once from L2 and perturbed
+// for each of the G individuals, whose accumulators sit side by side in TMEM
+// (G*MH*NT <= 256 columns, so two units can be in flight: double-buffered TMEM).
+// Every barrier wait is bounded; a wait that runs out records a status word,
+// makes the other roles stop, drains what was issued, frees TMEM and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+#include <type_traits>
+
+#include "vn_hash.cuh"
 #include "vn_internal.h"
 
 namespace vn {
 
+// Nonzero after a bounded wait ran out in a kernel of this file (read and
+// cleared by take_device_status). Bits: 1 = barrier wait timed out.
 __device__ unsigned int g_device_status = 0;
 
-bool linear_tc_applies(const void*, vn_dtype, const void*, vn_dtype, int64_t, int64_t, int64_t) {
-  return false;
+namespace {
+
+constexpr int kHashWarps = 8;
+constexpr int kFirstHashWarp = 6;
+constexpr int kThreads = (kFirstHashWarp + kHashWarps) * 32;  // 448
+constexpr int kHashThreads = kHashWarps * 32;                 // 256
+constexpr int kKC = 64;                                       // k per stage (128 bytes of bf16)
+constexpr uint32_t kHalfBytes = 128 * 128;                    // 128 rows x 128 bytes
+constexpr int kTmemCols = 512;
+constexpr unsigned long long kTimeoutNs = 4000000000ull;      // 4 s per wait
+
+struct TcParams {
+  const void* w;
+  const void* b;
+  const int64_t* seeds;
+  void* y;
+  int64_t pop, batch, in, out;
+  int64_t m_tiles, n_tiles, units;
+  uint64_t offset;
+  float sigma;
+  int b_bf16, act;
+  int nt, g, nbuf, stages, k_chunks, x_shared;
+  uint32_t stage_bytes, a_bytes, idesc;
+};
+
+// ---------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait on the phase with the given parity. Returns false if the wait
+// ran out (the status word and the CTA's abort flag are then set) or if
+// another role of the CTA has already aborted.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 15) == 0) {
+      if (*abort_flag) return false;
+      if (global_ns() - t0 > kTimeoutNs) {
+        atomicOr(&g_device_status, 1u);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulate, M=128.
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive on the mbarrier once every tcgen05 operation issued so far by this thread completes.
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+// 32 TMEM lanes x 16 consecutive 32-bit columns: thread t gets lane base+t.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
 }
 
-cudaError_t launch_linear_tc(const LinearArgs&, cudaStream_t) { return cudaErrorNotSupported; }
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row
+// groups 1024 bytes apart (stride byte offset), descriptor version 1.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+  uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(1) << 16;            // leading byte offset (unused for this layout)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;    // stride byte offset
+  d |= static_cast<uint64_t>(1) << 46;            // version
+  d |= static_cast<uint64_t>(2) << 61;            // 128-byte swizzle
+  return d;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// W elements of one 16-byte output chunk (8 k): fp32 (two float4) or bf16 (one uint4).
+struct RawF32 { float4 a, b; };
+struct RawBf16 { uint4 a; };
+
+struct Unit {
+  int64_t i0;   // first individual of the group
+  int gcount;   // individuals in the group
+  int64_t n0;   // first batch row
+  int64_t m0;   // first output row
+};
+__device__ __forceinline__ Unit decode(const TcParams& p, int64_t u, int mh) {
+  Unit r;
+  const int64_t mt = u % p.m_tiles;
+  const int64_t rest = u / p.m_tiles;
+  const int64_t ntile = rest % p.n_tiles;
+  const int64_t g = rest / p.n_tiles;
+  r.i0 = g * p.g;
+  r.gcount = static_cast<int>(min(static_cast<int64_t>(p.g), p.pop - r.i0));
+  r.n0 = ntile * p.nt;
+  r.m0 = mt * 128 * mh;
+  return r;
+}
+
+// ---------------------------------------------------------------- the kernel
+template <int MH, bool kWBf16, bool kYBf16>
+__global__ void __launch_bounds__(kThreads, 1)
+linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const int S = p.stages;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(S) * p.stage_bytes);
+  // barriers: full_a[S], full_x[S], empty[S], tmem_full[2], tmem_empty[2], drain
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_a = [&](int s) { return bar0 + 8u * s; };
+  auto full_x = [&](int s) { return bar0 + 8u * (S + s); };
+  auto empty = [&](int s) { return bar0 + 8u * (2 * S + s); };
+  auto tmem_full = [&](int b) { return bar0 + 8u * (3 * S + b); };
+  auto tmem_empty = [&](int b) { return bar0 + 8u * (3 * S + 2 + b); };
+  const uint32_t drain = bar0 + 8u * (3 * S + 4);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 3 * S + 5);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+  const uint32_t stage0 = smem_u32(smem);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_a(s), kHashThreads);
+      mbar_init(full_x(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tmem_full(b), 1);
+      mbar_init(tmem_empty(b), 128);
+    }
+    mbar_init(drain, 1);
+    *s_abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(s_tmem), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  const uint32_t cols_per_buf = kTmemCols / p.nbuf;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      const uint32_t x_bytes = static_cast<uint32_t>(p.nt) * 128u;
+      for (int64_t u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
+        const Unit un = decode(p, u, MH);
+        for (int kc = 0; ok && kc < p.k_chunks; ++kc) {
+          for (int ii = 0; ii < un.gcount; ++ii, ++it) {
+            const int s = static_cast<int>(it % S);
+            const uint32_t ph = (it / S) & 1u;
+            if (!(ok = mbar_wait(empty(s), ph ^ 1u, s_abort))) break;
+            mbar_expect_tx(full_x(s), x_bytes);
+            const int ind = p.x_shared ? 0 : static_cast<int>(un.i0 + ii);
+            tma_load_3d(stage0 + s * p.stage_bytes + p.a_bytes, &xmap, full_x(s), kc * kKC,
+                        static_cast<int>(un.n0), ind);
+          }
+        }
+      }
+      if (!ok) {
+        // Drain: every load issued lands on its full_x barrier; wait for the
+        // last S of them (bounded) so no copy is in flight at exit.
+        for (uint32_t k = 0; k < static_cast<uint32_t>(S) && k < it; ++k) {
+          const uint32_t j = it - 1 - k;
+          const uint64_t t0 = global_ns();
+          while (!mbar_try_wait(full_x(static_cast<int>(j % S)), (j / S) & 1u) &&
+                 global_ns() - t0 < kTimeoutNs) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      uint32_t it = 0, ut = 0;
+      bool ok = true;
+      for (int64_t u = blockIdx.x; ok && u < p.units; u += gridDim.x, ++ut) {
+        const Unit un = decode(p, u, MH);
+        const int b = static_cast<int>(ut % p.nbuf);
+        if (!(ok = mbar_wait(tmem_empty(b), ((ut / p.nbuf) & 1u) ^ 1u, s_abort))) break;
+        tc_fence_after();
+        const uint32_t dcol = tmem + b * cols_per_buf;
+        for (int kc = 0; ok && kc < p.k_chunks; ++kc) {
+          for (int ii = 0; ii < un.gcount; ++ii, ++it) {
+            const int s = static_cast<int>(it % S);
+            const uint32_t ph = (it / S) & 1u;
+            if (!(ok = mbar_wait(full_x(s), ph, s_abort))) break;
+            if (!(ok = mbar_wait(full_a(s), ph, s_abort))) break;
+            tc_fence_after();
+            const uint32_t a0 = stage0 + s * p.stage_bytes;
+            const uint32_t b0 = a0 + p.a_bytes;
+#pragma unroll
+            for (int ks = 0; ks < kKC / 16; ++ks) {
+              const uint64_t bdesc = sdesc_sw128(b0 + ks * 32);
+#pragma unroll
+              for (int h = 0; h < MH; ++h) {
+                umma_bf16(dcol + (ii * MH + h) * p.nt, sdesc_sw128(a0 + h * kHalfBytes + ks * 32),
+                          bdesc, p.idesc, (kc | ks) != 0);
+              }
+            }
+            umma_commit(empty(s));
+          }
+        }
+        if (ok) umma_commit(tmem_full(b));
+      }
+      // All issued MMAs have completed once this commit arrives.
+      umma_commit(drain);
+      const uint64_t t0 = global_ns();
+      while (!mbar_try_wait(drain, 0) && global_ns() - t0 < kTimeoutNs) {
+      }
+    }
+  } else if (warp < kFirstHashWarp) {
+    // ---------------------------------------------------------------- epilogue
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    uint32_t ut = 0;
+    for (int64_t u = blockIdx.x; u < p.units; u += gridDim.x, ++ut) {
+      const Unit un = decode(p, u, MH);
+      const int b = static_cast<int>(ut % p.nbuf);
+      if (!mbar_wait(tmem_full(b), (ut / p.nbuf) & 1u, s_abort)) break;
+      tc_fence_after();
+      const uint32_t dcol = tmem + b * cols_per_buf + (static_cast<uint32_t>(quarter * 32) << 16);
+      for (int ii = 0; ii < un.gcount; ++ii) {
+        const int64_t i = un.i0 + ii;
+        const uint64_t seed = static_cast<uint64_t>(__ldg(p.seeds + i));
+#pragma unroll
+        for (int h = 0; h < MH; ++h) {
+          const int64_t j = un.m0 + h * 128 + row;
+          const bool jok = j < p.out;
+          float bias = 0.f;
+          if (jok && p.b != nullptr) {
+            const float bj = p.b_bf16
+                                 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.b)[j])
+                                 : reinterpret_cast<const float*>(p.b)[j];
+            const uint64_t bidx =
+                p.offset + static_cast<uint64_t>(p.out) * static_cast<uint64_t>(p.in) +
+                static_cast<uint64_t>(j);
+            bias = fmaf(p.sigma, noise_at(seed, bidx), bj);
+          }
+          for (int c0 = 0; c0 < p.nt; c0 += 16) {
+            uint32_t v[16];
+            tmem_ld16(dcol + (ii * MH + h) * p.nt + c0, v);
+            tmem_wait_ld();
+            if (jok) {
+#pragma unroll
+              for (int q = 0; q < 16; ++q) {
+                const int64_t n = un.n0 + c0 + q;
+                if (n < p.batch) {
+                  float val = __uint_as_float(v[q]) + bias;
+                  if (p.act == VN_ACT_TANH) val = tanhf(val);
+                  const int64_t o = (i * p.batch + n) * p.out + j;
+                  if constexpr (kYBf16) {
+                    const __nv_bfloat16 hv = __float2bfloat16_rn(val);
+                    __stcs(reinterpret_cast<unsigned short*>(p.y) + o,
+                           *reinterpret_cast<const unsigned short*>(&hv));
+                  } else {
+                    __stcs(reinterpret_cast<float*>(p.y) + o, val);
+                  }
+                }
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(tmem_empty(b));
+    }
+  } else {
+    // ----------------------------------------------------------------- hashing
+    // Thread t writes 16-byte chunk (t & 7) of rows (t >> 3) + 32q of each
+    // 128-row half, q < 4: one 128-byte row per 8 lanes, so each quarter-warp
+    // store covers all 32 banks once (the swizzle permutes chunks within a row).
+    constexpr int kCPT = MH * 4;  // chunks per thread per stage
+    using Raw = typename std::conditional<kWBf16, RawBf16, RawF32>::type;
+    const int t = threadIdx.x - kFirstHashWarp * 32;
+    const int cc = t & 7;
+    const int r8 = (t >> 3) & 7;
+    // Chunk q: half h = q >> 2, row r = (t >> 3) + 32 * (q & 3) of that half;
+    // byte offset in the A tile = h*16K + (r >> 3)*1024 + (r & 7)*128 + ((cc ^ (r & 7)) << 4).
+    const uint32_t soff0 = static_cast<uint32_t>(t >> 6) * 1024u + r8 * 128u + ((cc ^ r8) << 4);
+    const int row0 = t >> 3;
+    auto soff = [&](int q) { return soff0 + (q >> 2) * kHalfBytes + (q & 3) * 4096u; };
+    auto rowq = [&](int q) { return row0 + (q >> 2) * 128 + (q & 3) * 32; };
+    const float sigma = p.sigma;
+    const float shift = -1.5f * sigma;
+
+    // W for chunk q of the stage group (u, kc): 8 consecutive k of one row.
+    auto load_chunk = [&](const Unit& un, int kc, int q, Raw& r) {
+      const int64_t j = un.m0 + rowq(q);
+      const int64_t k = static_cast<int64_t>(kc) * kKC + cc * 8;
+      if (j < p.out && k < p.in) {
+        if constexpr (kWBf16) {
+          r.a = __ldg(reinterpret_cast<const uint4*>(
+              reinterpret_cast<const __nv_bfloat16*>(p.w) + j * p.in + k));
+        } else {
+          const float4* src =
+              reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.w) + j * p.in + k);
+          r.a = __ldg(src);
+          r.b = __ldg(src + 1);
+        }
+      }
+    };
+
+    // One register buffer per chunk: chunk q of the next stage group is loaded
+    // right after chunk q's last use in this one, so its latency is covered by
+    // the rest of the stage.
+    Raw raw[kCPT];
+    uint32_t it = 0;
+    bool ok = true;
+    int64_t u = blockIdx.x;
+    if (u < p.units) {
+      const Unit first = decode(p, u, MH);
+#pragma unroll
+      for (int q = 0; q < kCPT; ++q) load_chunk(first, 0, q, raw[q]);
+    }
+    for (; ok && u < p.units; u += gridDim.x) {
+      const Unit un = decode(p, u, MH);
+      for (int kc = 0; ok && kc < p.k_chunks; ++kc) {
+        const bool has_next = (kc + 1 < p.k_chunks) || (u + gridDim.x < p.units);
+        const Unit nun = (kc + 1 < p.k_chunks || !has_next) ? un : decode(p, u + gridDim.x, MH);
+        const int nkc = (kc + 1 < p.k_chunks) ? kc + 1 : 0;
+        const int64_t k = static_cast<int64_t>(kc) * kKC + cc * 8;
+        uint32_t blo[kCPT], bhi[kCPT];
+        uint32_t live = 0;  // bit q: chunk q holds real weights (row < out, k < in)
+#pragma unroll
+        for (int q = 0; q < kCPT; ++q) {
+          const int64_t j = un.m0 + rowq(q);
+          if ((j < p.out) && (k < p.in)) live |= 1u << q;
+          index_term(p.offset + static_cast<uint64_t>(j) * static_cast<uint64_t>(p.in) +
+                         static_cast<uint64_t>(k),
+                     blo[q], bhi[q]);
+        }
+        for (int ii = 0; ii < un.gcount; ++ii, ++it) {
+          const int s = static_cast<int>(it % S);
+          const uint32_t ph = (it / S) & 1u;
+          const bool last = (ii + 1 == un.gcount);
+          const uint64_t seed = static_cast<uint64_t>(__ldg(p.seeds + un.i0 + ii));
+          if (!(ok = mbar_wait(empty(s), ph ^ 1u, s_abort))) break;
+          const uint32_t a0 = stage0 + s * p.stage_bytes;
+#pragma unroll
+          for (int q = 0; q < kCPT; ++q) {
+            uint32_t out4[4] = {0u, 0u, 0u, 0u};
+            if (live & (1u << q)) {
+              float wv[8];
+              if constexpr (kWBf16) {
+                const uint32_t wr[4] = {raw[q].a.x, raw[q].a.y, raw[q].a.z, raw[q].a.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  wv[2 * e] = __uint_as_float(wr[e] << 16);
+                  wv[2 * e + 1] = __uint_as_float(wr[e] & 0xFFFF0000u);
+                }
+              } else {
+                wv[0] = raw[q].a.x; wv[1] = raw[q].a.y; wv[2] = raw[q].a.z; wv[3] = raw[q].a.w;
+                wv[4] = raw[q].b.x; wv[5] = raw[q].b.y; wv[6] = raw[q].b.z; wv[7] = raw[q].b.w;
+              }
+              uint32_t lo = blo[q], hi = bhi[q];
+              add64(lo, hi, static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
+              float pv[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                pv[e] = fmaf(sigma, __uint_as_float(mix_to_one_plus_u(lo, hi)), wv[e] + shift);
+                add64(lo, hi, kGammaLo, kGammaHi);
+              }
+#pragma unroll
+              for (int e = 0; e < 4; ++e) out4[e] = pack_bf16x2(pv[2 * e], pv[2 * e + 1]);
+            }
+            if (last && has_next) load_chunk(nun, nkc, q, raw[q]);
+            st_shared_v4(a0 + soff(q), out4[0], out4[1], out4[2], out4[3]);
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(full_a(s));
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+template <int MH, bool kW, bool kY>
+cudaError_t launch_typed(const CUtensorMap& xmap, const TcParams& p, int grid, size_t smem,
+                         cudaStream_t stream) {
+  auto fn = linear_tc_kernel<MH, kW, kY>;
+  static size_t configured = 0;
+  if (configured < smem) {
+    cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    configured = smem;
+  }
+  fn<<<grid, kThreads, smem, stream>>>(xmap, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool linear_tc_applies(const void* x, vn_dtype x_dt, const void* w, vn_dtype w_dt, int64_t batch,
+                       int64_t in, int64_t out) {
+  (void)w_dt;
+  const int64_t kMaxCoord = (int64_t{1} << 31) - 1;
+  return x_dt == VN_BF16 && batch >= 1 && batch <= kMaxCoord && in >= 8 && in % 8 == 0 &&
+         in <= kMaxCoord && out >= 1 && reinterpret_cast<uintptr_t>(x) % 16 == 0 &&
+         reinterpret_cast<uintptr_t>(w) % 16 == 0;
+}
+
+cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
+  DeviceInfo dev;
+  cudaError_t err = device_info(&dev);
+  if (err != cudaSuccess) return err;
+  if (a.pop > (int64_t{1} << 31) - 1) return cudaErrorInvalidValue;
+  PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn();
+  if (encode == nullptr) return cudaErrorNotSupported;
+
+  TcParams p;
+  std::memset(&p, 0, sizeof(p));
+  const int64_t nt = std::min<int64_t>(256, (a.batch + 15) / 16 * 16);
+  const bool wbf = a.w_dt == VN_BF16;
+  const int mh = (nt >= 128 && a.out > 128 && wbf) ? 2 : 1;
+  int g = static_cast<int>(std::max<int64_t>(1, 256 / (mh * nt)));
+  g = static_cast<int>(std::min<int64_t>(g, a.pop));
+  p.w = a.w; p.b = a.b; p.seeds = a.seeds; p.y = a.y;
+  p.pop = a.pop; p.batch = a.batch; p.in = a.in; p.out = a.out;
+  p.offset = a.offset; p.sigma = a.sigma;
+  p.b_bf16 = (a.b != nullptr && a.b_dt == VN_BF16) ? 1 : 0;
+  p.act = a.act;
+  p.nt = static_cast<int>(nt);
+  p.g = g;
+  p.nbuf = (static_cast<int64_t>(g) * mh * nt <= kTmemCols / 2) ? 2 : 1;
+  p.a_bytes = static_cast<uint32_t>(mh) * kHalfBytes;
+  p.stage_bytes = p.a_bytes + static_cast<uint32_t>(nt) * 128u;
+  const size_t fixed = 1024 + 8 * (3 * 16 + 5) + 16;
+  const int stages = static_cast<int>(std::min<int64_t>(
+      8, (static_cast<int64_t>(dev.smem_optin) - static_cast<int64_t>(fixed)) / p.stage_bytes));
+  if (stages < 2) return cudaErrorInvalidConfiguration;
+  p.stages = stages;
+  p.k_chunks = static_cast<int>((a.in + kKC - 1) / kKC);
+  p.m_tiles = (a.out + 128 * mh - 1) / (128 * mh);
+  p.n_tiles = (a.batch + nt - 1) / nt;
+  const int64_t groups = (a.pop + g - 1) / g;
+  p.units = groups * p.n_tiles * p.m_tiles;
+  p.x_shared = a.x_shared;
+  // Instruction descriptor: fp32 accumulator, bf16 A and B, both K-major,
+  // N = nt (bits 17-22, N >> 3), M = 128 (bits 24-28, M >> 4).
+  p.idesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(nt >> 3) << 17) |
+            (static_cast<uint32_t>(128 >> 4) << 24);
+
+  // X as a 3-D tensor [pop or 1][batch][in] of bf16; box = 64 k x nt rows x 1.
+  CUtensorMap xmap;
+  std::memset(&xmap, 0, sizeof(xmap));
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(a.in), static_cast<cuuint64_t>(a.batch),
+                              static_cast<cuuint64_t>(a.x_shared ? 1 : a.pop)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(a.in) * 2,
+                                 static_cast<cuuint64_t>(a.in) * 2 * static_cast<cuuint64_t>(a.batch)};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kKC), static_cast<cuuint32_t>(nt), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult cr = encode(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.x),
+                             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+
+  const size_t smem = fixed + static_cast<size_t>(stages) * p.stage_bytes;
+  const int grid = static_cast<int>(std::min<int64_t>(p.units, dev.sm_count));
+  const bool ybf = a.y_dt == VN_BF16;
+  if (mh == 2) {
+    return ybf ? launch_typed<2, true, true>(xmap, p, grid, smem, stream)
+               : launch_typed<2, true, false>(xmap, p, grid, smem, stream);
+  }
+  if (wbf) {
+    return ybf ? launch_typed<1, true, true>(xmap, p, grid, smem, stream)
+               : launch_typed<1, true, false>(xmap, p, grid, smem, stream);
+  }
+  return launch_typed<1, false, false>(xmap, p, grid, smem, stream);
+}
 
 cudaError_t take_device_status(unsigned int* status, cudaStream_t stream) {
   cudaError_t err = cudaMemcpyFromSymbolAsync(status, g_device_status, sizeof(unsigned int), 0,
@@ -22,8 +640,8 @@ cudaError_t take_device_status(unsigned int* status, cudaStream_t stream) {
   if (err != cudaSuccess) return err;
   if (*status != 0) {
     const unsigned int zero = 0;
-    err = cudaMemcpyToSymbolAsync(g_device_status, &zero, sizeof(zero), 0,
-                                  cudaMemcpyHostToDevice, stream);
+    err = cudaMemcpyToSymbolAsync(g_device_status, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice,
+                                  stream);
     if (err == cudaSuccess) err = cudaStreamSynchronize(stream);
   }
   return err;
