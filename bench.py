@@ -1,0 +1,497 @@
+#!/usr/bin/env python
+"""Benchmark of the virtual-noise ES step on one node.
+
+Default workload: the ES MLP policy step (pop 1024, batch 1, 64 -> 256 -> 256 -> 8
+with tanh, fp32, sigma 0.02, centered-rank fitness). One step is one pass of the
+whole hot path over one population:
+  * forward: three perturbed linears (the tanh between layers fused into the
+    epilogue of the first two),
+  * gradients: grad_W and grad_b of all three layers (six reductions over the
+    population),
+  * noise dump: the centered-uniform noise of the whole flat parameter vector
+    (84,488 elements) for every individual,
+so each step regenerates the population's parameter noise three times.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl vn|reference]
+                       [--workload es_mlp|tiny|mid|grad_only|large_tc]
+For N > 1 launch with torch.distributed.run: every rank runs its own population
+(seeds offset by rank * pop), no data-path collective (weak scaling).
+
+Timing: W untimed warm-up steps, then K steps between barriers and device
+synchronisations; every kernel launch is bracketed by CUDA events on the
+launching stream and a 256 MiB buffer is rewritten between steps (outside the
+events) so that each step starts with a cold L2. Rank 0 prints one JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "virtual-noise elem/s"
+UNIT = "noise elements/s"
+
+# 32-bit operations per noise element in the definition, on 32-bit halves:
+# state add 2, xor-shift 30: 4, multiply by GAMMA: 3, xor-shift 27: 4,
+# multiply by GAMMA: 3, final xor-shift 31 + top-23-bit extraction: 3  (19 integer)
+# + the float conversion (1 FADD) and the one FMA that consumes the noise (2 fp).
+OPS_PER_ELEMENT = 21
+SMS_NOMINAL = 152
+SM_CLOCK_MAX_HZ = 2.07e9
+ISSUE_LANES_PER_SM = 128          # 4 schedulers x 32 lanes, one instruction per clock each
+L2_FLUSH_BYTES = 256 << 20
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    p = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+    if os.path.exists(path):
+        with open(path) as f:
+            m = json.load(f)
+        p = {"hbm_gbs": float(m["hbm_gbs"]), "bf16_tflops": float(m["bf16_tflops"]),
+             "bf16_tflops_sustained": float(m.get("bf16_tflops_sustained", m["bf16_tflops"])),
+             "source": "measured"}
+    p["alu_ops"] = SMS_NOMINAL * ISSUE_LANES_PER_SM * SM_CLOCK_MAX_HZ
+    return p
+
+
+# ---------------------------------------------------------------------------
+# Workload -> list of launches through the C ABI
+# ---------------------------------------------------------------------------
+
+class Launch:
+    """One C-ABI call with its arguments fixed; ``kernel`` names the kernel it runs."""
+
+    def __init__(self, kernel, fn, args, elements, flops=0.0, hbm_bytes=0.0):
+        self.kernel, self.fn, self.args = kernel, fn, args
+        self.elements, self.flops, self.hbm_bytes = elements, flops, hbm_bytes
+
+    def __call__(self):
+        st = self.fn(*self.args)
+        if st != 0:
+            from virtual_noise_perturbed_gb300._lib import VNError
+            raise VNError(st, self.kernel)
+
+
+def build_step(wl, dev, stream_ptr):
+    """Device buffers and the launches of one step of workload ``wl`` (on ``dev``)."""
+    import torch
+    from virtual_noise_perturbed_gb300 import _lib
+
+    lib = _lib.load()
+    P = ctypes.c_void_p
+    s = P(stream_ptr)
+    d = wl.to(dev)
+    bufs = {"seeds": d.seeds, "fitness": d.fitness}
+    launches = []
+    outputs = []
+    pop, batch = wl.pop, wl.batch
+    dt = {torch.float32: _lib.VN_F32, torch.bfloat16: _lib.VN_BF16}
+
+    if wl.forward:
+        h = d.x
+        bufs["x"] = d.x
+        for li, l in enumerate(d.layers):
+            act = _lib.VN_ACT_TANH if (wl.activation == "tanh" and li < len(d.layers) - 1) else _lib.VN_ACT_NONE
+            ydt = torch.bfloat16 if (h.dtype == torch.bfloat16 and l.weight.dtype == torch.bfloat16) else torch.float32
+            y = torch.empty((pop, batch, l.out_f), dtype=ydt, device=dev)
+            bufs[f"w{li}"], bufs[f"b{li}"] = l.weight, l.bias
+            path = lib.vn_perturbed_linear_path(P(h.data_ptr()), dt[h.dtype], 0, P(l.weight.data_ptr()),
+                                                dt[l.weight.dtype], batch, l.in_f, l.out_f)
+            kernel = "linear_tc" if path == _lib.VN_PATH_TC else "linear_ffma"
+            args = (P(h.data_ptr()), dt[h.dtype], 0, P(l.weight.data_ptr()), dt[l.weight.dtype],
+                    P(l.bias.data_ptr()), dt[l.bias.dtype], P(d.seeds.data_ptr()), pop, batch,
+                    l.in_f, l.out_f, float(wl.sigma), l.offset, P(y.data_ptr()), dt[ydt],
+                    _lib.VN_PATH_AUTO, act, s)
+            el = pop * l.out_f * l.in_f
+            hbm = h.numel() * h.element_size() + y.numel() * y.element_size() + l.weight.numel() * l.weight.element_size()
+            launches.append(Launch(kernel, lib.vn_perturbed_linear_ex, args, el,
+                                   flops=2.0 * el * batch, hbm_bytes=hbm))
+            h = y
+        outputs.append(h)
+
+    for li, l in enumerate(d.layers):
+        gw = torch.empty((l.out_f, l.in_f), dtype=torch.float32, device=dev)
+        gb = torch.empty((l.out_f,), dtype=torch.float32, device=dev)
+        launches.append(Launch("grad", lib.vn_weight_gradient,
+                               (P(d.fitness.data_ptr()), P(d.seeds.data_ptr()), pop, l.out_f, l.in_f,
+                                float(wl.sigma), l.offset, P(gw.data_ptr()), s),
+                               pop * l.out_f * l.in_f, hbm_bytes=gw.numel() * 4))
+        launches.append(Launch("grad", lib.vn_bias_gradient,
+                               (P(d.fitness.data_ptr()), P(d.seeds.data_ptr()), pop, l.out_f,
+                                float(wl.sigma), l.offset + l.out_f * l.in_f, P(gb.data_ptr()), s),
+                               pop * l.out_f, hbm_bytes=gb.numel() * 4))
+        outputs += [gw, gb]
+
+    n_params = sum(l.out_f * l.in_f + l.out_f for l in wl.layers)
+    if wl.number in (1, 2):
+        dump = torch.empty((pop, n_params), dtype=torch.float32, device=dev)
+        launches.append(Launch("noise_dump", lib.vn_noise_dump,
+                               (P(d.seeds.data_ptr()), pop, n_params, wl.layers[0].offset,
+                                P(dump.data_ptr()), s),
+                               pop * n_params, hbm_bytes=dump.numel() * 4))
+        outputs.append(dump)
+    return launches, bufs, outputs
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# Distributed plumbing (one process per GPU; rank 0 reports)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The maximum of ``value`` over all ranks (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def traffic_for(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel's source
+    is unchanged since the capture (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(kernel)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "virtual_noise_perturbed_gb300", "csrc", rec["source"])
+    if not os.path.exists(src):
+        return None
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return rec["bytes_per_launch"] if h == rec["source_sha256_16"] else None
+
+
+# ---------------------------------------------------------------------------
+# The oracle leg (cpu_baseline and --impl reference)
+# ---------------------------------------------------------------------------
+
+def oracle_step(wl, individuals: int) -> int:
+    """The oracle's pass over the first ``individuals`` of the population: forward,
+    the gradients' sums over those individuals, and their noise dump. Returns the
+    noise elements regenerated."""
+    import numpy as np
+    from oracle import es
+
+    s = slice(0, individuals)
+    seeds = wl.seeds[s].numpy()
+    fit = wl.fitness[s].numpy()
+    n = 0
+    if wl.forward:
+        h = wl.x[s].float().numpy().astype(np.float64)
+        for li, l in enumerate(wl.layers):
+            h = es.perturbed_linear(h, l.weight.float().numpy(), l.bias.float().numpy(), seeds, wl.sigma, l.offset)
+            if wl.activation == "tanh" and li < len(wl.layers) - 1:
+                h = np.tanh(h)
+            n += individuals * l.out_f * l.in_f
+    for l in wl.layers:
+        es.weight_gradient(fit, seeds, (l.out_f, l.in_f), wl.sigma, individuals, l.offset)
+        es.bias_gradient(fit, seeds, (l.out_f,), wl.sigma, individuals, l.offset + l.out_f * l.in_f)
+        n += individuals * (l.out_f * l.in_f + l.out_f)
+    if wl.number in (1, 2):
+        n_params = sum(l.out_f * l.in_f + l.out_f for l in wl.layers)
+        es.noise_dump(seeds, n_params, wl.layers[0].offset)
+        n += individuals * n_params
+    return n
+
+
+def cpu_cores_used() -> int:
+    # numpy element-wise work is single-threaded; the oracle's matmuls are tiny here.
+    return 1
+
+
+def time_oracle(wl, budget_s: float, steps: int = 1):
+    """Run ``steps`` oracle passes, each on as many individuals as fit ``budget_s``."""
+    t = time.perf_counter()
+    oracle_step(wl, 1)
+    per_ind = max(time.perf_counter() - t, 1e-4)
+    inds = int(max(1, min(wl.pop, budget_s / per_ind)))
+    total_el, total_t = 0, 0.0
+    for _ in range(steps):
+        t = time.perf_counter()
+        total_el += oracle_step(wl, inds)
+        total_t += time.perf_counter() - t
+    return total_el / total_t, inds, total_t
+
+
+# ---------------------------------------------------------------------------
+
+def config_for(wl, world):
+    return {"workload": wl.name, "description": wl.description, "pop": wl.pop, "batch": wl.batch,
+            "layers": [[l.in_f, l.out_f] for l in wl.layers], "sigma": wl.sigma,
+            "noise_elements_per_step": None, "l2": "256 MiB buffer rewritten between timed steps",
+            "parallelism": f"population shards x{world} (independent per rank)"}
+
+
+def run_reference(args, wl, world, rank):
+    if rank != 0:
+        return 0
+    from virtual_noise_perturbed_gb300 import workloads  # noqa: F401
+    budget = min(2.0, 150.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        time_oracle(wl, budget / 4)
+    rate, inds, total_t = time_oracle(wl, budget, steps=args.steps)
+    cfg = config_for(wl, 1)
+    line = {"metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
+            "impl": "reference",
+            "cpu_baseline": {"value": rate, "unit": UNIT, "cores": cpu_cores_used(), "kind": "oracle",
+                             "sample": f"each step: the oracle's pass over the first {inds} of {wl.pop} "
+                                       f"individuals (forward, gradient sums, noise dump)"},
+            "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None) -> int:
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["vn", "reference"], default="vn")
+    ap.add_argument("--workload", default="es_mlp",
+                    choices=["tiny", "es_mlp", "mid", "grad_only", "large_tc"])
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    from virtual_noise_perturbed_gb300 import workloads
+    number = {v: k for k, v in workloads.NAMES.items()}[args.workload]
+    world, rank, local = dist_env()
+    wl = workloads.make(number)
+    if rank > 0:  # independent population per rank
+        wl.seeds = wl.seeds + rank * wl.pop
+
+    if args.impl == "reference":
+        return run_reference(args, wl, world, rank)
+
+    import torch
+    if not torch.cuda.is_available():
+        print(json.dumps({"metric": METRIC, "error": "no CUDA device"}))
+        return 1
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    from virtual_noise_perturbed_gb300 import _lib, build as vbuild
+    vbuild.build()
+    stream = torch.cuda.Stream(dev)
+    launches, bufs, outputs = build_step(wl, dev, stream.cuda_stream)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    el_step = sum(l.elements for l in launches)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            for l in launches:
+                l()
+            flush.zero_()
+        torch.cuda.synchronize(dev)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(launches))]
+              for _ in range(args.steps)]
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        sampler = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                               else local)
+        wall0 = time.perf_counter()
+        for k in range(args.steps):
+            for j, l in enumerate(launches):
+                ev[k][2 * j].record(stream)
+                l()
+                ev[k][2 * j + 1].record(stream)
+            flush.zero_()
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - wall0
+        clocks = sampler.stop()
+        barrier(world)
+    status = _lib.load().vn_device_status(ctypes.c_void_p(stream.cuda_stream))
+    if status != 0:
+        raise _lib.VNError(status, "bench")
+
+    step_ms = [ev[k][0].elapsed_time(ev[k][-1]) for k in range(args.steps)]
+    per_kernel = {}
+    for k in range(args.steps):
+        for j, l in enumerate(launches):
+            ms = ev[k][2 * j].elapsed_time(ev[k][2 * j + 1])
+            rec = per_kernel.setdefault(l.kernel, {"ms": 0.0, "launches": 0, "elements": 0, "flops": 0.0,
+                                                   "hbm_bytes": 0.0})
+            rec["ms"] += ms
+            rec["launches"] += 1
+            rec["elements"] += l.elements
+            rec["flops"] += l.flops
+            rec["hbm_bytes"] += l.hbm_bytes
+    total_ms = sum(step_ms)
+    total_ms_max = max_over_ranks(total_ms, world, dev)
+    value = el_step * args.steps * world / (total_ms_max * 1e-3)
+
+    # --- roofline of the dominant kernel
+    pk = peaks()
+    dom = max(per_kernel, key=lambda n: per_kernel[n]["ms"])
+    r = per_kernel[dom]
+    secs = r["ms"] * 1e-3
+    cands = {"alu": (r["elements"] * OPS_PER_ELEMENT / secs / 1e12, pk["alu_ops"] / 1e12, "Tops/s")}
+    if r["hbm_bytes"]:
+        cands["hbm"] = (r["hbm_bytes"] / secs / 1e9, pk["hbm_gbs"], "GB/s")
+    if r["flops"]:
+        cands["tensor"] = (r["flops"] / secs / 1e12, pk["bf16_tflops"], "TFLOP/s")
+    bound = max(cands, key=lambda b: cands[b][0] / cands[b][1])
+    ach, peak, unit = cands[bound]
+    roofline = {"bound": bound, "kernel": dom, "achieved": ach, "peak": peak, "unit": unit,
+                "frac": ach / peak, "traffic": traffic_for(dom),
+                "peak_source": ("derived: 152 SMs x 128 issue lanes x 2.07 GHz, 32-bit ops"
+                                if bound == "alu" else pk["source"]),
+                "ops_per_element": OPS_PER_ELEMENT if bound == "alu" else None,
+                "launches": r["launches"], "avg_launch_us": 1e3 * r["ms"] / r["launches"]}
+    kernels = {n: {"launches": v["launches"], "share": v["ms"] / sum(x["ms"] for x in per_kernel.values()),
+                   "avg_us": 1e3 * v["ms"] / v["launches"],
+                   "noise_elem_per_s": v["elements"] / (v["ms"] * 1e-3)} for n, v in per_kernel.items()}
+
+    # --- secondary metrics of the step (per phase)
+    fwd = [x for x in launches if x.kernel.startswith("linear")]
+    fwd_ms = sum(per_kernel[n]["ms"] for n in per_kernel if n.startswith("linear"))
+    grad_w_elems = sum(x.elements // wl.pop for x in launches if x.kernel == "grad" and x.fn.__name__ == "vn_weight_gradient")
+    extra = {
+        "perturbed_linear_tflops": (sum(x.flops for x in fwd) * args.steps / (fwd_ms * 1e-3) / 1e12) if fwd else None,
+        "grad_w_elem_per_s": (grad_w_elems * args.steps / (per_kernel["grad"]["ms"] * 1e-3)) if "grad" in per_kernel else None,
+        "noise_elements_per_step": el_step,
+    }
+
+    # --- end to end: host buffers, copies inside the timed region
+    e2e = run_e2e(wl, dev, stream, launches, bufs, outputs, args.e2e_steps, world, el_step)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, inds, tt = time_oracle(wl, args.cpu_baseline_seconds)
+        cpu = {"value": rate, "unit": UNIT, "cores": cpu_cores_used(), "kind": "oracle",
+               "sample": f"one oracle pass over the first {inds} of {wl.pop} individuals "
+                         f"(forward, gradient sums, noise dump), {tt:.1f} s"}
+
+    if rank == 0:
+        cfg = config_for(wl, world)
+        cfg["noise_elements_per_step"] = el_step
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": total_ms_max / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f32" if wl.number in (1, 2) else "bf16",
+                "data": "synthetic", "config": cfg, "roofline": roofline, "cpu_baseline": cpu,
+                "e2e": e2e, "gpu_launches": len(launches) * args.steps, "clocks": clocks,
+                "kernels": kernels, **extra, "wall_s_timed_region": wall}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(wl, dev, stream, launches, bufs, outputs, steps, world, el_step):
+    """The same step through the C ABI with inputs in pinned host memory: each step
+    copies its inputs host -> device, runs, and copies every result back."""
+    import torch
+    host_in = {k: v.detach().cpu().pin_memory() for k, v in bufs.items() if v is not None and v.numel()}
+    host_out = [o.detach().cpu().pin_memory() for o in outputs]
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out)
+    with torch.cuda.stream(stream):
+        def one():
+            for k, v in host_in.items():
+                bufs[k].copy_(v, non_blocking=True)
+            for l in launches:
+                l()
+            for o, h in zip(outputs, host_out):
+                h.copy_(o, non_blocking=True)
+        one()
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            one()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+    ms = max_over_ranks(a.elapsed_time(b), world, dev)
+    return {"value": el_step * steps * world / (ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": ms / steps}
+
+
+if __name__ == "__main__":
+    sys.exit(main())
