@@ -25,12 +25,16 @@ events) so that each step starts with a cold L2. Rank 0 prints one JSON line.
 
 from __future__ import annotations
 
+import os
+
+# The oracle legs report the threads they use: keep every BLAS / OpenMP pool at one.
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
 import argparse
 import ctypes
 import hashlib
 import json
-import math
-import os
 import statistics
 import subprocess
 import sys
@@ -121,7 +125,7 @@ def build_step(wl, dev, stream_ptr):
             h = y
         outputs.append(h)
 
-    for li, l in enumerate(d.layers):
+    for li, l in enumerate(d.layers if wl.grads else []):
         gw = torch.empty((l.out_f, l.in_f), dtype=torch.float32, device=dev)
         gb = torch.empty((l.out_f,), dtype=torch.float32, device=dev)
         launches.append(Launch("grad", lib.vn_weight_gradient,
@@ -197,6 +201,16 @@ class ClockSampler:
 # Distributed plumbing (one process per GPU; rank 0 reports)
 # ---------------------------------------------------------------------------
 
+def gpu_id(dev) -> str:
+    """nvidia-smi's name for the torch device (PCI bus id; independent of CUDA_VISIBLE_DEVICES)."""
+    import torch
+    p = torch.cuda.get_device_properties(dev)
+    try:
+        return f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+    except AttributeError:
+        return "0"
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -260,7 +274,7 @@ def oracle_step(wl, individuals: int) -> int:
             if wl.activation == "tanh" and li < len(wl.layers) - 1:
                 h = np.tanh(h)
             n += individuals * l.out_f * l.in_f
-    for l in wl.layers:
+    for l in (wl.layers if wl.grads else []):
         es.weight_gradient(fit, seeds, (l.out_f, l.in_f), wl.sigma, individuals, l.offset)
         es.bias_gradient(fit, seeds, (l.out_f,), wl.sigma, individuals, l.offset + l.out_f * l.in_f)
         n += individuals * (l.out_f * l.in_f + l.out_f)
@@ -272,7 +286,8 @@ def oracle_step(wl, individuals: int) -> int:
 
 
 def cpu_cores_used() -> int:
-    # numpy element-wise work is single-threaded; the oracle's matmuls are tiny here.
+    # numpy element-wise work is single-threaded and the BLAS pools are pinned to
+    # one thread at the top of this file.
     return 1
 
 
@@ -371,8 +386,7 @@ def main(argv=None) -> int:
               for _ in range(args.steps)]
         barrier(world)
         torch.cuda.synchronize(dev)
-        sampler = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
-                               else local)
+        sampler = ClockSampler(gpu_id(dev))
         wall0 = time.perf_counter()
         for k in range(args.steps):
             for j, l in enumerate(launches):

@@ -43,6 +43,7 @@ class Workload:
     fitness: torch.Tensor              # (pop,) fp32
     activation: Optional[str] = None   # between layers
     forward: bool = True               # the workload runs the forward
+    grads: bool = True                 # the workload runs the gradient estimates
 
     def to(self, device) -> "Workload":
         d = dataclasses.replace(self)
@@ -130,5 +131,6 @@ def make(number: int) -> Workload:
         b = _normal((out_f,), 0.01, g).to(torch.bfloat16)
         f = _normal((pop,), 1.0, g)
         return Workload(5, NAMES[5], DESCRIPTIONS[5], pop, batch, 0.01,
-                        torch.arange(pop, dtype=torch.int64), x, [Layer(in_f, out_f, w, b, 0)], f)
+                        torch.arange(pop, dtype=torch.int64), x, [Layer(in_f, out_f, w, b, 0)], f,
+                        grads=False)
     raise ValueError(f"no workload {number}")
