@@ -20,7 +20,7 @@
 //   warp 0      TMA producer for X tiles (one thread);
 //   warp 1      TMEM allocator and MMA issuer (one thread);
 //   warps 2..5  epilogue: TMEM -> registers -> + b + sigma*nb -> Y (one per TMEM lane quarter);
-//   warps 6..13 hashing: W'_i = bf16(W + sigma*N_i), 16 bytes (8 k) per store.
+//   warps 6..21 hashing: W'_i = bf16(W + sigma*N_i), 16 bytes (8 k) per store.
 // A work unit is (group of G individuals, N tile, M tile of 128*MH output rows);
 // per k-chunk of 64 the unit's W elements are read once from L2 and perturbed
 // for each of the G individuals, whose accumulators sit side by side in TMEM
@@ -48,10 +48,10 @@ __device__ unsigned int g_device_status = 0;
 
 namespace {
 
-constexpr int kHashWarps = 8;
+constexpr int kHashWarps = 16;
 constexpr int kFirstHashWarp = 6;
-constexpr int kThreads = (kFirstHashWarp + kHashWarps) * 32;  // 448
-constexpr int kHashThreads = kHashWarps * 32;                 // 256
+constexpr int kThreads = (kFirstHashWarp + kHashWarps) * 32;  // 704
+constexpr int kHashThreads = kHashWarps * 32;                 // 512
 constexpr int kKC = 64;                                       // k per stage (128 bytes of bf16)
 constexpr uint32_t kHalfBytes = 128 * 128;                    // 128 rows x 128 bytes
 constexpr int kTmemCols = 512;
@@ -208,6 +208,20 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // W elements of one 16-byte output chunk (8 k): fp32 (two float4) or bf16 (one uint4).
 struct RawF32 { float4 a, b; };
 struct RawBf16 { uint4 a; };
+
+// The 8 weights of a chunk as fp32, minus 1.5*sigma: sigma*(1 + u) + (W - 1.5*sigma) = W + sigma*n.
+__device__ __forceinline__ void unpack_shift(const RawBf16& r, float shift, float (&w)[8]) {
+  const uint32_t wr[4] = {r.a.x, r.a.y, r.a.z, r.a.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    w[2 * e] = __uint_as_float(wr[e] << 16) + shift;
+    w[2 * e + 1] = __uint_as_float(wr[e] & 0xFFFF0000u) + shift;
+  }
+}
+__device__ __forceinline__ void unpack_shift(const RawF32& r, float shift, float (&w)[8]) {
+  w[0] = r.a.x + shift; w[1] = r.a.y + shift; w[2] = r.a.z + shift; w[3] = r.a.w + shift;
+  w[4] = r.b.x + shift; w[5] = r.b.y + shift; w[6] = r.b.z + shift; w[7] = r.b.w + shift;
+}
 
 struct Unit {
   int64_t i0;   // first individual of the group
@@ -406,20 +420,20 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
     }
   } else {
     // ----------------------------------------------------------------- hashing
-    // Thread t writes 16-byte chunk (t & 7) of rows (t >> 3) + 32q of each
-    // 128-row half, q < 4: one 128-byte row per 8 lanes, so each quarter-warp
-    // store covers all 32 banks once (the swizzle permutes chunks within a row).
-    constexpr int kCPT = MH * 4;  // chunks per thread per stage
+    // Thread t writes 16-byte chunk (t & 7) of rows (t >> 3) + 64q of the
+    // (128*MH)-row A tile, q < 2*MH: one 128-byte row per 8 lanes, so each
+    // quarter-warp store covers all 32 banks once (the swizzle permutes the
+    // chunks within a row). The two 128-row halves of an MH=2 tile are
+    // contiguous, so row r sits at (r >> 3)*1024 + (r & 7)*128 for any r < 256.
+    constexpr int kCPT = MH * 2;  // chunks per thread per stage
     using Raw = typename std::conditional<kWBf16, RawBf16, RawF32>::type;
     const int t = threadIdx.x - kFirstHashWarp * 32;
     const int cc = t & 7;
     const int r8 = (t >> 3) & 7;
-    // Chunk q: half h = q >> 2, row r = (t >> 3) + 32 * (q & 3) of that half;
-    // byte offset in the A tile = h*16K + (r >> 3)*1024 + (r & 7)*128 + ((cc ^ (r & 7)) << 4).
     const uint32_t soff0 = static_cast<uint32_t>(t >> 6) * 1024u + r8 * 128u + ((cc ^ r8) << 4);
     const int row0 = t >> 3;
-    auto soff = [&](int q) { return soff0 + (q >> 2) * kHalfBytes + (q & 3) * 4096u; };
-    auto rowq = [&](int q) { return row0 + (q >> 2) * 128 + (q & 3) * 32; };
+    auto soff = [&](int q) { return soff0 + q * 8192u; };
+    auto rowq = [&](int q) { return row0 + q * 64; };
     const float sigma = p.sigma;
     const float shift = -1.5f * sigma;
 
@@ -440,70 +454,91 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
       }
     };
 
-    // One register buffer per chunk: chunk q of the next stage group is loaded
-    // right after chunk q's last use in this one, so its latency is covered by
-    // the rest of the stage.
+    // raw holds the W chunks of the next stage group: at the start of a group
+    // they are turned into W - 1.5*sigma (fp32, shared by the group's G
+    // individuals) and the loads for the following group are issued at once,
+    // so a whole group of stages covers their latency. The seed of the next
+    // stage is likewise loaded one stage ahead.
     Raw raw[kCPT];
     uint32_t it = 0;
     bool ok = true;
     int64_t u = blockIdx.x;
+    uint64_t seed_next = 0;
     if (u < p.units) {
       const Unit first = decode(p, u, MH);
 #pragma unroll
       for (int q = 0; q < kCPT; ++q) load_chunk(first, 0, q, raw[q]);
+      seed_next = static_cast<uint64_t>(__ldg(p.seeds + first.i0));
     }
     for (; ok && u < p.units; u += gridDim.x) {
       const Unit un = decode(p, u, MH);
+      const bool has_next_unit = u + gridDim.x < p.units;
+      const Unit nun = has_next_unit ? decode(p, u + gridDim.x, MH) : un;
       for (int kc = 0; ok && kc < p.k_chunks; ++kc) {
-        const bool has_next = (kc + 1 < p.k_chunks) || (u + gridDim.x < p.units);
-        const Unit nun = (kc + 1 < p.k_chunks || !has_next) ? un : decode(p, u + gridDim.x, MH);
-        const int nkc = (kc + 1 < p.k_chunks) ? kc + 1 : 0;
         const int64_t k = static_cast<int64_t>(kc) * kKC + cc * 8;
+        // kHoist (G may exceed 1): W - 1.5*sigma is formed once per group in
+        // wm and the next group's loads go out at once. Otherwise (MH = 2,
+        // one individual per unit, tight registers) W is unpacked per use and
+        // chunk q of the next group is loaded right after chunk q's use.
+        constexpr bool kHoist = (MH == 1);
+        float wm[kHoist ? kCPT : 1][8];
         uint32_t blo[kCPT], bhi[kCPT];
         uint32_t live = 0;  // bit q: chunk q holds real weights (row < out, k < in)
 #pragma unroll
         for (int q = 0; q < kCPT; ++q) {
           const int64_t j = un.m0 + rowq(q);
           if ((j < p.out) && (k < p.in)) live |= 1u << q;
+          if constexpr (kHoist) unpack_shift(raw[q], shift, wm[q]);
           index_term(p.offset + static_cast<uint64_t>(j) * static_cast<uint64_t>(p.in) +
                          static_cast<uint64_t>(k),
                      blo[q], bhi[q]);
         }
+        const bool has_next = (kc + 1 < p.k_chunks) || has_next_unit;
+        const Unit& lun = (kc + 1 < p.k_chunks) ? un : nun;
+        const int lkc = (kc + 1 < p.k_chunks) ? kc + 1 : 0;
+        if constexpr (kHoist) {
+          if (has_next) {
+#pragma unroll
+            for (int q = 0; q < kCPT; ++q) load_chunk(lun, lkc, q, raw[q]);
+          }
+        }
         for (int ii = 0; ii < un.gcount; ++ii, ++it) {
           const int s = static_cast<int>(it % S);
           const uint32_t ph = (it / S) & 1u;
-          const bool last = (ii + 1 == un.gcount);
-          const uint64_t seed = static_cast<uint64_t>(__ldg(p.seeds + un.i0 + ii));
+          const uint64_t seed = seed_next;
+          // the individual of the next stage: next in the group, else the group's
+          // first (next k chunk), else the next unit's first
+          if (ii + 1 < un.gcount) {
+            seed_next = static_cast<uint64_t>(__ldg(p.seeds + un.i0 + ii + 1));
+          } else if (kc + 1 < p.k_chunks) {
+            seed_next = static_cast<uint64_t>(__ldg(p.seeds + un.i0));
+          } else if (has_next_unit) {
+            seed_next = static_cast<uint64_t>(__ldg(p.seeds + nun.i0));
+          }
           if (!(ok = mbar_wait(empty(s), ph ^ 1u, s_abort))) break;
           const uint32_t a0 = stage0 + s * p.stage_bytes;
+          const bool last = (ii + 1 == un.gcount);
 #pragma unroll
           for (int q = 0; q < kCPT; ++q) {
             uint32_t out4[4] = {0u, 0u, 0u, 0u};
             if (live & (1u << q)) {
-              float wv[8];
-              if constexpr (kWBf16) {
-                const uint32_t wr[4] = {raw[q].a.x, raw[q].a.y, raw[q].a.z, raw[q].a.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  wv[2 * e] = __uint_as_float(wr[e] << 16);
-                  wv[2 * e + 1] = __uint_as_float(wr[e] & 0xFFFF0000u);
-                }
-              } else {
-                wv[0] = raw[q].a.x; wv[1] = raw[q].a.y; wv[2] = raw[q].a.z; wv[3] = raw[q].a.w;
-                wv[4] = raw[q].b.x; wv[5] = raw[q].b.y; wv[6] = raw[q].b.z; wv[7] = raw[q].b.w;
-              }
+              float wl[8];
+              if constexpr (!kHoist) unpack_shift(raw[q], shift, wl);
+              const float* w8 = kHoist ? wm[kHoist ? q : 0] : wl;
               uint32_t lo = blo[q], hi = bhi[q];
               add64(lo, hi, static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
               float pv[8];
 #pragma unroll
               for (int e = 0; e < 8; ++e) {
-                pv[e] = fmaf(sigma, __uint_as_float(mix_to_one_plus_u(lo, hi)), wv[e] + shift);
+                pv[e] = fmaf(sigma, __uint_as_float(mix_to_one_plus_u(lo, hi)), w8[e]);
                 add64(lo, hi, kGammaLo, kGammaHi);
               }
 #pragma unroll
               for (int e = 0; e < 4; ++e) out4[e] = pack_bf16x2(pv[2 * e], pv[2 * e + 1]);
             }
-            if (last && has_next) load_chunk(nun, nkc, q, raw[q]);
+            if constexpr (!kHoist) {
+              if (last && has_next) load_chunk(lun, lkc, q, raw[q]);
+            }
             st_shared_v4(a0 + soff(q), out4[0], out4[1], out4[2], out4[3]);
           }
           fence_proxy_async_smem();

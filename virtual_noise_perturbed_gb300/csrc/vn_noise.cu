@@ -22,26 +22,37 @@ namespace {
 
 constexpr int kDumpThreads = 256;
 constexpr int kDumpGroups = 4;                                  // groups of 4 per thread
-constexpr int64_t kDumpChunk = kDumpThreads * 4 * kDumpGroups;  // elements per CTA step
+constexpr int64_t kDumpStride = kDumpThreads * 4;               // columns between a thread's groups
+constexpr int64_t kDumpChunk = kDumpStride * kDumpGroups;       // elements per CTA step
+// GAMMA * kDumpStride mod 2^64: the state difference between a thread's consecutive groups.
+constexpr uint64_t kDumpStep = kGamma * static_cast<uint64_t>(kDumpStride);
 
-// Grid-stride over (row i, chunk of kDumpChunk columns). vec4: every row starts
-// 16-byte aligned (out aligned and n % 4 == 0), so groups are stored as float4.
+// Grid-stride over (row i, chunk of kDumpChunk columns). Thread t makes the
+// 4-element groups at columns c + 4t + 1024g, g < 4: one 16-byte store per group,
+// consecutive lanes on consecutive 16-byte segments. The state of the next
+// element is the previous plus GAMMA and the state of the next group the
+// previous group's plus 1024*GAMMA, so no 64-bit multiply is needed per group.
+// vec4: every row starts 16-byte aligned (out aligned and n % 4 == 0).
 __global__ void __launch_bounds__(kDumpThreads)
 noise_dump_kernel(const int64_t* __restrict__ seeds, int64_t n, uint64_t offset,
                   float* __restrict__ out, int64_t chunks_per_row, int64_t total_chunks,
                   int vec4) {
   for (int64_t c = blockIdx.x; c < total_chunks; c += gridDim.x) {
     const int64_t i = c / chunks_per_row;
-    const int64_t t_base = (c - i * chunks_per_row) * kDumpChunk;
+    const int64_t t0 = (c - i * chunks_per_row) * kDumpChunk + threadIdx.x * 4;
     const uint64_t seed = static_cast<uint64_t>(__ldg(seeds + i));
     float* row = out + i * n;
+    uint32_t glo, ghi;  // state of the first element of the current group
+    index_term(offset + static_cast<uint64_t>(t0), glo, ghi);
+    add64(glo, ghi, static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
+    // number of this thread's groups that start inside the row
+    const int64_t left = n - t0;
+    const int full = left <= 0 ? 0 : static_cast<int>((left + kDumpStride - 1) / kDumpStride < kDumpGroups ? (left + kDumpStride - 1) / kDumpStride : kDumpGroups);
 #pragma unroll
     for (int g = 0; g < kDumpGroups; ++g) {
-      const int64_t t = t_base + g * (kDumpThreads * 4) + threadIdx.x * 4;
-      if (t < n) {
-        uint32_t lo, hi;
-        index_term(offset + static_cast<uint64_t>(t), lo, hi);
-        add64(lo, hi, static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
+      if (g < full) {
+        const int64_t t = t0 + g * kDumpStride;
+        uint32_t lo = glo, hi = ghi;
         float v[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -55,6 +66,7 @@ noise_dump_kernel(const int64_t* __restrict__ seeds, int64_t n, uint64_t offset,
           for (int q = 0; q < 4; ++q)
             if (t + q < n) row[t + q] = v[q];
         }
+        add64(glo, ghi, static_cast<uint32_t>(kDumpStep), static_cast<uint32_t>(kDumpStep >> 32));
       }
     }
   }
