@@ -6,8 +6,9 @@ with tanh, fp32, sigma 0.02, centered-rank fitness). One step is one pass of the
 whole hot path over one population:
   * forward: three perturbed linears (the tanh between layers fused into the
     epilogue of the first two),
-  * gradients: grad_W and grad_b of all three layers (six reductions over the
-    population),
+  * gradients: grad_W and grad_b of all three layers; the six blocks are laid
+    out by compute_offsets one after another, so they are one flat range of
+    element indices and one reduction over the population computes them all,
   * noise dump: the centered-uniform noise of the whole flat parameter vector
     (84,488 elements) for every individual,
 so each step regenerates the population's parameter noise three times.
@@ -77,15 +78,26 @@ def peaks():
 class Launch:
     """One C-ABI call with its arguments fixed; ``kernel`` names the kernel it runs."""
 
-    def __init__(self, kernel, fn, args, elements, flops=0.0, hbm_bytes=0.0):
+    def __init__(self, kernel, fn, args, elements, flops=0.0, hbm_bytes=0.0, grad_w_elems=0):
         self.kernel, self.fn, self.args = kernel, fn, args
         self.elements, self.flops, self.hbm_bytes = elements, flops, hbm_bytes
+        self.grad_w_elems = grad_w_elems
 
     def __call__(self):
         st = self.fn(*self.args)
         if st != 0:
             from virtual_noise_perturbed_gb300._lib import VNError
             raise VNError(st, self.kernel)
+
+
+def contiguous_blocks(wl) -> bool:
+    """True when the layers' blocks follow one another as compute_offsets lays them out."""
+    off = wl.layers[0].offset
+    for l in wl.layers:
+        if l.offset != off:
+            return False
+        off += l.out_f * l.in_f + l.out_f
+    return True
 
 
 def build_step(wl, dev, stream_ptr):
@@ -125,20 +137,34 @@ def build_step(wl, dev, stream_ptr):
             h = y
         outputs.append(h)
 
-    for li, l in enumerate(d.layers if wl.grads else []):
+    n_params = sum(l.out_f * l.in_f + l.out_f for l in wl.layers)
+    flat = wl.grads and len(wl.layers) > 1 and contiguous_blocks(wl)
+    if flat:
+        # The blocks (weights then bias, layer by layer) are laid out by
+        # compute_offsets, so the gradients of all of them are one flat range of
+        # element indices: one reduction over the population gives every block's
+        # gradient as a slice (grad_W of layer l = flat[off_l : off_l + out*in]).
+        g = torch.empty((n_params,), dtype=torch.float32, device=dev)
+        launches.append(Launch("grad", lib.vn_bias_gradient,
+                               (P(d.fitness.data_ptr()), P(d.seeds.data_ptr()), pop, n_params,
+                                float(wl.sigma), wl.layers[0].offset, P(g.data_ptr()), s),
+                               pop * n_params, hbm_bytes=g.numel() * 4, grad_w_elems=sum(
+                                   l.out_f * l.in_f for l in wl.layers)))
+        outputs.append(g)
+    for li, l in enumerate(d.layers if (wl.grads and not flat) else []):
         gw = torch.empty((l.out_f, l.in_f), dtype=torch.float32, device=dev)
         gb = torch.empty((l.out_f,), dtype=torch.float32, device=dev)
         launches.append(Launch("grad", lib.vn_weight_gradient,
                                (P(d.fitness.data_ptr()), P(d.seeds.data_ptr()), pop, l.out_f, l.in_f,
                                 float(wl.sigma), l.offset, P(gw.data_ptr()), s),
-                               pop * l.out_f * l.in_f, hbm_bytes=gw.numel() * 4))
+                               pop * l.out_f * l.in_f, hbm_bytes=gw.numel() * 4,
+                               grad_w_elems=l.out_f * l.in_f))
         launches.append(Launch("grad", lib.vn_bias_gradient,
                                (P(d.fitness.data_ptr()), P(d.seeds.data_ptr()), pop, l.out_f,
                                 float(wl.sigma), l.offset + l.out_f * l.in_f, P(gb.data_ptr()), s),
                                pop * l.out_f, hbm_bytes=gb.numel() * 4))
         outputs += [gw, gb]
 
-    n_params = sum(l.out_f * l.in_f + l.out_f for l in wl.layers)
     if wl.number in (1, 2):
         dump = torch.empty((pop, n_params), dtype=torch.float32, device=dev)
         launches.append(Launch("noise_dump", lib.vn_noise_dump,
@@ -443,7 +469,7 @@ def main(argv=None) -> int:
     # --- secondary metrics of the step (per phase)
     fwd = [x for x in launches if x.kernel.startswith("linear")]
     fwd_ms = sum(per_kernel[n]["ms"] for n in per_kernel if n.startswith("linear"))
-    grad_w_elems = sum(x.elements // wl.pop for x in launches if x.kernel == "grad" and x.fn.__name__ == "vn_weight_gradient")
+    grad_w_elems = sum(x.grad_w_elems for x in launches)
     extra = {
         "perturbed_linear_tflops": (sum(x.flops for x in fwd) * args.steps / (fwd_ms * 1e-3) / 1e12) if fwd else None,
         "grad_w_elem_per_s": (grad_w_elems * args.steps / (per_kernel["grad"]["ms"] * 1e-3)) if "grad" in per_kernel else None,

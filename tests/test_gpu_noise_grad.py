@@ -7,8 +7,9 @@ import torch
 
 from oracle import es
 from tests.parity import TOL_FP32, assert_close, to_np
-from virtual_noise_perturbed_gb300 import (VNError, noise_dump, virtual_bias_gradient,
-                                           virtual_reduce_metric, virtual_weight_gradient, workloads)
+from virtual_noise_perturbed_gb300 import (VNError, compute_offsets, noise_dump, virtual_bias_gradient,
+                                           virtual_flat_gradient, virtual_reduce_metric,
+                                           virtual_weight_gradient, workloads)
 from virtual_noise_perturbed_gb300.build import build
 
 pytestmark = pytest.mark.gpu
@@ -147,6 +148,26 @@ def test_workload2_all_gradients():
                      TOL_FP32, "w2 grad_W")
         assert_close(to_np(gb), es.bias_gradient(f, s, (l.out_f,), w.sigma, w.pop,
                                                  l.offset + l.out_f * l.in_f), TOL_FP32, "w2 grad_b")
+
+
+def test_flat_gradient_covers_every_block():
+    """One flat reduction over the ES MLP's parameter vector equals the per-block
+    oracle gradients, block by block (the layout of compute_offsets)."""
+    w = workloads.make(2)
+    shapes = []
+    for l in w.layers:
+        shapes += [(l.out_f, l.in_f), (l.out_f,)]
+    offs = compute_offsets(shapes)
+    n = offs[-1] + shapes[-1][0]
+    flat = to_np(virtual_flat_gradient(w.fitness.to(DEV), w.seeds.to(DEV), n, w.sigma, w.pop, 0))
+    f, s = w.fitness.numpy(), w.seeds.numpy()
+    for (shape, off) in zip(shapes, offs):
+        size = int(np.prod(shape))
+        if len(shape) == 2:
+            want = es.weight_gradient(f, s, shape, w.sigma, w.pop, off).ravel()
+        else:
+            want = es.bias_gradient(f, s, shape, w.sigma, w.pop, off)
+        assert_close(flat[off:off + size], want, TOL_FP32, f"flat block at {off}")
 
 
 def test_workload3_gradient_windows():

@@ -15,6 +15,7 @@ from .api import (  # noqa: F401
     noise_dump,
     perturbed_linear_path,
     virtual_bias_gradient,
+    virtual_flat_gradient,
     virtual_perturbed_linear,
     virtual_reduce_metric,
     virtual_weight_gradient,
@@ -22,6 +23,6 @@ from .api import (  # noqa: F401
 
 __all__ = [
     "VNError", "compute_offsets", "device_status", "noise_dump", "perturbed_linear_path",
-    "virtual_bias_gradient", "virtual_perturbed_linear", "virtual_reduce_metric",
+    "virtual_bias_gradient", "virtual_flat_gradient", "virtual_perturbed_linear", "virtual_reduce_metric",
     "virtual_weight_gradient",
 ]

@@ -141,6 +141,18 @@ def virtual_bias_gradient(fitness: torch.Tensor, seeds: torch.Tensor, bias_shape
     return g
 
 
+def virtual_flat_gradient(fitness: torch.Tensor, seeds: torch.Tensor, n_params: int, sigma: float,
+                          pop_size: int, offset: int = 0) -> torch.Tensor:
+    """grad[t] = sum_i fitness_i * PRNG(seed_i, offset + t) / (pop_size * sigma), t < n_params.
+
+    With parameter blocks laid out by ``compute_offsets`` (weights then bias, one
+    block after another), this is the gradient of every block in one launch:
+    block b's gradient is ``grad[offsets[b] : offsets[b] + numel_b]`` reshaped to the
+    block's shape, identical in value to ``virtual_weight_gradient`` /
+    ``virtual_bias_gradient`` on that block."""
+    return virtual_bias_gradient(fitness, seeds, (int(n_params),), sigma, pop_size, offset)
+
+
 def noise_dump(seeds: torch.Tensor, n_elements: int, offset: int) -> torch.Tensor:
     """(pop, n) fp32 centered-uniform noise, D[i, t] = PRNG(seed_i, offset + t)."""
     lib = load()
@@ -193,5 +205,6 @@ def device_status(device=None) -> None:
 
 
 __all__ = ["virtual_perturbed_linear", "virtual_weight_gradient", "virtual_bias_gradient",
+           "virtual_flat_gradient",
            "noise_dump", "virtual_reduce_metric", "compute_offsets", "perturbed_linear_path",
            "device_status", "VNError"]

@@ -8,18 +8,18 @@
 // registers" (module description): no noise tensor exists in memory.
 //
 // This path serves fp32 inputs and small per-individual batches (the ES
-// policy case, batch 1), where there is too little reuse of each perturbed
-// weight for tensor cores to matter: the work is one hash per (i, j, k) plus
-// `batch` FMAs.
+// policy case, batch 1), where each perturbed weight is used by only a few
+// rows of X and the work is one hash per (i, j, k) plus `batch` FMAs.
 //
-// Work decomposition: a CTA owns 32 output rows j (one per lane) for 8
-// individuals (one per warp), and walks k in tiles of 64. Each tile of W is
-// staged once in shared memory as W - 1.5*sigma (so that the perturbed weight
-// is one FMA from the hash bits: sigma*(1+u) + W - 1.5*sigma = W + sigma*n)
-// and serves all 8 individuals; each individual's X tile is staged next to it
-// and read back as 16-byte broadcasts. A thread walks its row's elements in
-// order, so each next state is the previous plus GAMMA. Batches larger than
-// the register budget (8 rows) are done 8 rows at a time, hashing again.
+// Work decomposition: a warp task is (individual i, block of up to 8 output
+// rows). The lanes split one row's k range in chunks of 8 consecutive
+// elements (L lanes per row, 32/L rows side by side), so each lane walks its
+// chunk with the state of the next element = previous + GAMMA, reads W and
+// X[i] as 16-byte vectors, and the row's partial sums meet in a warp-shuffle
+// reduction. Tasks are ordered row-block-major, so the 8 warps of a CTA share
+// W rows through L1, and handed out in a grid-stride loop of many small tasks,
+// which keeps the last wave short. Batches above 8 rows are done 8 rows at a
+// time, hashing again.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -31,121 +31,124 @@
 namespace vn {
 namespace {
 
-constexpr int kRows = 32;   // output rows per CTA (lanes)
-constexpr int kInds = 8;    // individuals per CTA (warps)
-constexpr int kThreads = kRows * kInds;
-constexpr int kKT = 64;     // k tile
-constexpr int kWStride = kKT + 4;  // conflict-free 16-byte row reads
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kRowsPerTask = 8;
 
 template <bool kBf16>
-__device__ __forceinline__ float load_elem(const void* p, int64_t idx) {
-  if constexpr (kBf16) {
-    return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[idx]);
+__device__ __forceinline__ void load8(const void* base, int64_t idx, int64_t valid, bool vec,
+                                      float (&v)[8]) {
+  if (vec && valid >= 8) {
+    if constexpr (kBf16) {
+      const uint4 r = __ldg(reinterpret_cast<const uint4*>(
+          reinterpret_cast<const __nv_bfloat16*>(base) + idx));
+      const uint32_t wr[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        v[2 * e] = __uint_as_float(wr[e] << 16);
+        v[2 * e + 1] = __uint_as_float(wr[e] & 0xFFFF0000u);
+      }
+    } else {
+      const float4* p = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(base) + idx);
+      const float4 a = __ldg(p), b = __ldg(p + 1);
+      v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+      v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
   } else {
-    return reinterpret_cast<const float*>(p)[idx];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      if (e < valid) {
+        v[e] = kBf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[idx + e])
+                     : reinterpret_cast<const float*>(base)[idx + e];
+      } else {
+        v[e] = 0.f;
+      }
+    }
   }
 }
 
+// lanes_log2: log2(L), L = lanes per output row (1..32).
 template <int NB, bool kXBf16, bool kWBf16>
 __global__ void __launch_bounds__(kThreads)
-linear_ffma_kernel(const LinearArgs a, int64_t row_tiles, int64_t tiles) {
-  extern __shared__ float4 smem4[];
-  float* s_w = reinterpret_cast<float*>(smem4);  // [kRows][kWStride]
-  float* s_x = s_w + kRows * kWStride;           // [slabs][NB][kKT]
-
-  const int warp = threadIdx.x >> 5;
+linear_rows_kernel(const LinearArgs a, int lanes_log2, int64_t row_blocks, int64_t tasks,
+                   int x_vec, int w_vec) {
   const int lane = threadIdx.x & 31;
-  const int slabs = a.x_shared ? 1 : kInds;
+  const int L = 1 << lanes_log2;
+  const int kl = lane & (L - 1);         // this lane's position along k
+  const int rsub = lane >> lanes_log2;   // which of the warp's rows
+  const int rows_per_iter = 32 >> lanes_log2;
+  const int64_t kstep = static_cast<int64_t>(L) * 8;
   const float sigma = a.sigma;
   const float shift = -1.5f * sigma;
+  const uint64_t bias_base = a.offset + static_cast<uint64_t>(a.out) * static_cast<uint64_t>(a.in);
+  const int64_t warps_total = static_cast<int64_t>(gridDim.x) * kWarps;
 
-  for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
-    const int64_t it = t / row_tiles;
-    const int64_t i0 = it * kInds;
-    const int64_t j0 = (t - it * row_tiles) * kRows;
-    const int64_t i = i0 + warp;
-    const int64_t j = j0 + lane;
-    const bool live = (i < a.pop) && (j < a.out);
-    const uint64_t seed = (i < a.pop) ? static_cast<uint64_t>(a.seeds[i]) : 0ull;
-
-    for (int64_t r0 = 0; r0 < a.batch; r0 += NB) {
-      float acc[NB];
+  for (int64_t task = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5); task < tasks;
+       task += warps_total) {
+    const int64_t rb = task / a.pop;
+    const int64_t i = task - rb * a.pop;
+    const uint64_t seed = static_cast<uint64_t>(__ldg(a.seeds + i));
+    const int64_t j_end = min(a.out, (rb + 1) * kRowsPerTask);
+    for (int64_t jr = rb * kRowsPerTask; jr < j_end; jr += rows_per_iter) {
+      const int64_t j = jr + rsub;
+      const bool jok = j < j_end;
+      for (int64_t r0 = 0; r0 < a.batch; r0 += NB) {
+        float acc[NB];
 #pragma unroll
-      for (int r = 0; r < NB; ++r) acc[r] = 0.f;
-      uint32_t slo, shi;
-      index_term(a.offset + static_cast<uint64_t>(j) * static_cast<uint64_t>(a.in), slo, shi);
-      add64(slo, shi, static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
-
-      for (int64_t k0 = 0; k0 < a.in; k0 += kKT) {
-        __syncthreads();  // previous tile fully consumed
-        for (int q = threadIdx.x; q < kRows * kKT; q += kThreads) {
-          const int rr = q / kKT, cc = q % kKT;
-          const int64_t jj = j0 + rr, kk = k0 + cc;
-          float v = 0.f;
-          if (jj < a.out && kk < a.in) v = load_elem<kWBf16>(a.w, jj * a.in + kk) + shift;
-          s_w[rr * kWStride + cc] = v;
-        }
-        for (int q = threadIdx.x; q < slabs * NB * kKT; q += kThreads) {
-          const int s = q / (NB * kKT);
-          const int rem = q % (NB * kKT);
-          const int r = rem / kKT, cc = rem % kKT;
-          const int64_t ii = i0 + s, rr = r0 + r, kk = k0 + cc;
-          float v = 0.f;
-          if ((a.x_shared || ii < a.pop) && rr < a.batch && kk < a.in) {
-            const int64_t base = a.x_shared ? 0 : ii * a.batch * a.in;
-            v = load_elem<kXBf16>(a.x, base + rr * a.in + kk);
-          }
-          s_x[q] = v;
-        }
-        __syncthreads();
-        if (live) {
-          const float* wrow = s_w + lane * kWStride;
-          const float* xs = s_x + (a.x_shared ? 0 : warp) * NB * kKT;
-#pragma unroll 2
-          for (int kk = 0; kk < kKT; kk += 4) {
-            const float4 wm = *reinterpret_cast<const float4*>(wrow + kk);
-            float wp[4];
-            wp[0] = fmaf(sigma, __uint_as_float(mix_to_one_plus_u(slo, shi)), wm.x);
-            add64(slo, shi, kGammaLo, kGammaHi);
-            wp[1] = fmaf(sigma, __uint_as_float(mix_to_one_plus_u(slo, shi)), wm.y);
-            add64(slo, shi, kGammaLo, kGammaHi);
-            wp[2] = fmaf(sigma, __uint_as_float(mix_to_one_plus_u(slo, shi)), wm.z);
-            add64(slo, shi, kGammaLo, kGammaHi);
-            wp[3] = fmaf(sigma, __uint_as_float(mix_to_one_plus_u(slo, shi)), wm.w);
-            add64(slo, shi, kGammaLo, kGammaHi);
+        for (int r = 0; r < NB; ++r) acc[r] = 0.f;
+        if (jok) {
+          for (int64_t k = static_cast<int64_t>(kl) * 8; k < a.in; k += kstep) {
+            const int64_t valid = a.in - k;
+            float w[8];
+            load8<kWBf16>(a.w, j * a.in + k, valid, w_vec != 0, w);
+            uint32_t lo, hi;
+            index_term(a.offset + static_cast<uint64_t>(j) * static_cast<uint64_t>(a.in) +
+                           static_cast<uint64_t>(k),
+                       lo, hi);
+            add64(lo, hi, static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
+            float wp[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              wp[e] = fmaf(sigma, __uint_as_float(mix_to_one_plus_u(lo, hi)), w[e] + shift);
+              add64(lo, hi, kGammaLo, kGammaHi);
+            }
 #pragma unroll
             for (int r = 0; r < NB; ++r) {
-              const float4 xv = *reinterpret_cast<const float4*>(xs + r * kKT + kk);
-              acc[r] = fmaf(xv.x, wp[0], acc[r]);
-              acc[r] = fmaf(xv.y, wp[1], acc[r]);
-              acc[r] = fmaf(xv.z, wp[2], acc[r]);
-              acc[r] = fmaf(xv.w, wp[3], acc[r]);
+              if (r0 + r < a.batch) {
+                const int64_t xrow = (a.x_shared ? 0 : i * a.batch) + r0 + r;
+                float x[8];
+                load8<kXBf16>(a.x, xrow * a.in + k, valid, x_vec != 0, x);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[r] = fmaf(x[e], wp[e], acc[r]);
+              }
             }
           }
         }
-      }
-
-      if (live) {
-        float bias = 0.f;
-        if (a.b != nullptr) {
-          const float bj = (a.b_dt == VN_BF16)
-                               ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(a.b)[j])
-                               : reinterpret_cast<const float*>(a.b)[j];
-          const uint64_t bidx = a.offset + static_cast<uint64_t>(a.out) * static_cast<uint64_t>(a.in) +
-                                static_cast<uint64_t>(j);
-          bias = fmaf(sigma, noise_at(seed, bidx), bj);
-        }
+        // Reduce over the L lanes of each row (lanes of a row are contiguous).
 #pragma unroll
         for (int r = 0; r < NB; ++r) {
-          const int64_t rr = r0 + r;
-          if (rr < a.batch) {
-            float v = acc[r] + bias;
-            if (a.act == VN_ACT_TANH) v = tanhf(v);
-            const int64_t o = (i * a.batch + rr) * a.out + j;
-            if (a.y_dt == VN_BF16)
-              reinterpret_cast<__nv_bfloat16*>(a.y)[o] = __float2bfloat16_rn(v);
-            else
-              reinterpret_cast<float*>(a.y)[o] = v;
+          for (int s = L >> 1; s > 0; s >>= 1) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], s);
+        }
+        if (jok && kl == 0) {
+          float bias = 0.f;
+          if (a.b != nullptr) {
+            const float bj = (a.b_dt == VN_BF16)
+                                 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(a.b)[j])
+                                 : reinterpret_cast<const float*>(a.b)[j];
+            bias = fmaf(sigma, noise_at(seed, bias_base + static_cast<uint64_t>(j)), bj);
+          }
+#pragma unroll
+          for (int r = 0; r < NB; ++r) {
+            const int64_t rr = r0 + r;
+            if (rr < a.batch) {
+              float v = acc[r] + bias;
+              if (a.act == VN_ACT_TANH) v = tanhf(v);
+              const int64_t o = (i * a.batch + rr) * a.out + j;
+              if (a.y_dt == VN_BF16)
+                reinterpret_cast<__nv_bfloat16*>(a.y)[o] = __float2bfloat16_rn(v);
+              else
+                reinterpret_cast<float*>(a.y)[o] = v;
+            }
           }
         }
       }
@@ -155,19 +158,23 @@ linear_ffma_kernel(const LinearArgs a, int64_t row_tiles, int64_t tiles) {
 
 template <int NB, bool kX, bool kW>
 cudaError_t launch_nb(const LinearArgs& a, cudaStream_t stream, int sm_count) {
-  const int64_t row_tiles = (a.out + kRows - 1) / kRows;
-  const int64_t ind_tiles = (a.pop + kInds - 1) / kInds;
-  const int64_t tiles = row_tiles * ind_tiles;
-  const int slabs = a.x_shared ? 1 : kInds;
-  const size_t smem = sizeof(float) * (kRows * kWStride + slabs * NB * kKT);
-  auto fn = linear_ffma_kernel<NB, kX, kW>;
+  // Lanes per row: enough 8-element chunks to cover `in` once, at most 32.
+  int lanes_log2 = 0;
+  while (lanes_log2 < 5 && (int64_t{8} << lanes_log2) < a.in) ++lanes_log2;
+  const int64_t row_blocks = (a.out + kRowsPerTask - 1) / kRowsPerTask;
+  const int64_t tasks = row_blocks * a.pop;
+  auto fn = linear_rows_kernel<NB, kX, kW>;
   static int occ = 0;
   if (occ == 0 &&
-      (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, kThreads, sizeof(float) * (kRows * kWStride + kInds * NB * kKT)) != cudaSuccess ||
-       occ < 1))
+      (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, kThreads, 0) != cudaSuccess || occ < 1))
     occ = 1;
-  const int64_t grid = std::min<int64_t>(tiles, static_cast<int64_t>(sm_count) * occ * 4);
-  fn<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(a, row_tiles, tiles);
+  const int64_t grid = std::max<int64_t>(
+      1, std::min<int64_t>((tasks + kWarps - 1) / kWarps, static_cast<int64_t>(sm_count) * occ));
+  const size_t xe = kX ? 2 : 4, we = kW ? 2 : 4;
+  const int x_vec = (a.in % (16 / xe) == 0) && (reinterpret_cast<uintptr_t>(a.x) % 16 == 0);
+  const int w_vec = (a.in % (16 / we) == 0) && (reinterpret_cast<uintptr_t>(a.w) % 16 == 0);
+  fn<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(a, lanes_log2, row_blocks, tasks, x_vec,
+                                                            w_vec);
   return cudaGetLastError();
 }
 

@@ -104,12 +104,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 // Bounded wait on the phase with the given parity. Returns false if the wait
 // ran out (the status word and the CTA's abort flag are then set) or if
-// another role of the CTA has already aborted.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
+// another role of the CTA has already aborted. Waiters that are not on the
+// critical path pass sleep_ns > 0 to back off between polls and leave the
+// issue slots to the hashing warps.
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
+                                            volatile int* abort_flag, uint32_t sleep_ns) {
   const uint64_t t0 = global_ns();
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (sleep_ns) __nanosleep(sleep_ns);
     if ((n & 15) == 0) {
       if (*abort_flag) return false;
       if (global_ns() - t0 > kTimeoutNs) {
@@ -120,6 +123,22 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
     }
   }
 }
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          uint32_t sleep_ns = 0) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort_flag, sleep_ns);
+}
+// Position in a ring of S slots: slot index and the parity of its current use.
+struct Ring {
+  int s = 0;
+  uint32_t ph = 0;
+  __device__ __forceinline__ void next(int n) {
+    if (++s == n) {
+      s = 0;
+      ph ^= 1u;
+    }
+  }
+};
 __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
@@ -294,15 +313,15 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t it = 0;
+      Ring rg;
       bool ok = true;
       const uint32_t x_bytes = static_cast<uint32_t>(p.nt) * 128u;
       for (int64_t u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
         const Unit un = decode(p, u, MH);
         for (int kc = 0; ok && kc < p.k_chunks; ++kc) {
-          for (int ii = 0; ii < un.gcount; ++ii, ++it) {
-            const int s = static_cast<int>(it % S);
-            const uint32_t ph = (it / S) & 1u;
-            if (!(ok = mbar_wait(empty(s), ph ^ 1u, s_abort))) break;
+          for (int ii = 0; ii < un.gcount; ++ii, ++it, rg.next(S)) {
+            const int s = rg.s;
+            if (!(ok = mbar_wait(empty(s), rg.ph ^ 1u, s_abort, 32))) break;
             mbar_expect_tx(full_x(s), x_bytes);
             const int ind = p.x_shared ? 0 : static_cast<int>(un.i0 + ii);
             tma_load_3d(stage0 + s * p.stage_bytes + p.a_bytes, &xmap, full_x(s), kc * kKC,
@@ -325,20 +344,19 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
   } else if (warp == 1) {
     // -------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      uint32_t it = 0, ut = 0;
+      Ring rg, tb;
       bool ok = true;
-      for (int64_t u = blockIdx.x; ok && u < p.units; u += gridDim.x, ++ut) {
+      for (int64_t u = blockIdx.x; ok && u < p.units; u += gridDim.x, tb.next(p.nbuf)) {
         const Unit un = decode(p, u, MH);
-        const int b = static_cast<int>(ut % p.nbuf);
-        if (!(ok = mbar_wait(tmem_empty(b), ((ut / p.nbuf) & 1u) ^ 1u, s_abort))) break;
+        const int b = tb.s;
+        if (!(ok = mbar_wait(tmem_empty(b), tb.ph ^ 1u, s_abort))) break;
         tc_fence_after();
         const uint32_t dcol = tmem + b * cols_per_buf;
         for (int kc = 0; ok && kc < p.k_chunks; ++kc) {
-          for (int ii = 0; ii < un.gcount; ++ii, ++it) {
-            const int s = static_cast<int>(it % S);
-            const uint32_t ph = (it / S) & 1u;
-            if (!(ok = mbar_wait(full_x(s), ph, s_abort))) break;
-            if (!(ok = mbar_wait(full_a(s), ph, s_abort))) break;
+          for (int ii = 0; ii < un.gcount; ++ii, rg.next(S)) {
+            const int s = rg.s;
+            if (!(ok = mbar_wait(full_x(s), rg.ph, s_abort))) break;
+            if (!(ok = mbar_wait(full_a(s), rg.ph, s_abort))) break;
             tc_fence_after();
             const uint32_t a0 = stage0 + s * p.stage_bytes;
             const uint32_t b0 = a0 + p.a_bytes;
@@ -366,11 +384,11 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
     // ---------------------------------------------------------------- epilogue
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
-    uint32_t ut = 0;
-    for (int64_t u = blockIdx.x; u < p.units; u += gridDim.x, ++ut) {
+    Ring tb;
+    for (int64_t u = blockIdx.x; u < p.units; u += gridDim.x, tb.next(p.nbuf)) {
       const Unit un = decode(p, u, MH);
-      const int b = static_cast<int>(ut % p.nbuf);
-      if (!mbar_wait(tmem_full(b), (ut / p.nbuf) & 1u, s_abort)) break;
+      const int b = tb.s;
+      if (!mbar_wait(tmem_full(b), tb.ph, s_abort, 256)) break;
       tc_fence_after();
       const uint32_t dcol = tmem + b * cols_per_buf + (static_cast<uint32_t>(quarter * 32) << 16);
       for (int ii = 0; ii < un.gcount; ++ii) {
@@ -460,7 +478,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
     // so a whole group of stages covers their latency. The seed of the next
     // stage is likewise loaded one stage ahead.
     Raw raw[kCPT];
-    uint32_t it = 0;
+    Ring rg;
     bool ok = true;
     int64_t u = blockIdx.x;
     uint64_t seed_next = 0;
@@ -502,9 +520,8 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
             for (int q = 0; q < kCPT; ++q) load_chunk(lun, lkc, q, raw[q]);
           }
         }
-        for (int ii = 0; ii < un.gcount; ++ii, ++it) {
-          const int s = static_cast<int>(it % S);
-          const uint32_t ph = (it / S) & 1u;
+        for (int ii = 0; ii < un.gcount; ++ii, rg.next(S)) {
+          const int s = rg.s;
           const uint64_t seed = seed_next;
           // the individual of the next stage: next in the group, else the group's
           // first (next k chunk), else the next unit's first
@@ -515,7 +532,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
           } else if (has_next_unit) {
             seed_next = static_cast<uint64_t>(__ldg(p.seeds + nun.i0));
           }
-          if (!(ok = mbar_wait(empty(s), ph ^ 1u, s_abort))) break;
+          if (!(ok = mbar_wait(empty(s), rg.ph ^ 1u, s_abort))) break;
           const uint32_t a0 = stage0 + s * p.stage_bytes;
           const bool last = (ii + 1 == un.gcount);
 #pragma unroll
