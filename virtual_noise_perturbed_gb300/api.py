@@ -148,8 +148,8 @@ def virtual_flat_gradient(fitness: torch.Tensor, seeds: torch.Tensor, n_params: 
     With parameter blocks laid out by ``compute_offsets`` (weights then bias, one
     block after another), this is the gradient of every block in one launch:
     block b's gradient is ``grad[offsets[b] : offsets[b] + numel_b]`` reshaped to the
-    block's shape, identical in value to ``virtual_weight_gradient`` /
-    ``virtual_bias_gradient`` on that block."""
+    block's shape, equal (up to the order of the fp32 sums) to
+    ``virtual_weight_gradient`` / ``virtual_bias_gradient`` on that block."""
     return virtual_bias_gradient(fitness, seeds, (int(n_params),), sigma, pop_size, offset)
 
 
