@@ -102,18 +102,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// try_wait with a suspend-time hint: a thread whose phase is not complete is
+// suspended until the phase completes or `ns` nanoseconds pass, so waiting
+// threads do not take issue slots from the hashing warps.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
 // Bounded wait on the phase with the given parity. Returns false if the wait
 // ran out (the status word and the CTA's abort flag are then set) or if
-// another role of the CTA has already aborted. Waiters that are not on the
-// critical path pass sleep_ns > 0 to back off between polls and leave the
-// issue slots to the hashing warps.
+// another role of the CTA has already aborted. Each poll suspends the thread
+// for up to kSuspendNs (it resumes as soon as the phase completes).
+constexpr uint32_t kSuspendNs = 200000;
 __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
                                             volatile int* abort_flag, uint32_t sleep_ns) {
   const uint64_t t0 = global_ns();
   for (uint32_t n = 1;; ++n) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_suspend(bar, parity, kSuspendNs)) return true;
     if (sleep_ns) __nanosleep(sleep_ns);
-    if ((n & 15) == 0) {
+    if ((n & 3) == 0) {
       if (*abort_flag) return false;
       if (global_ns() - t0 > kTimeoutNs) {
         atomicOr(&g_device_status, 1u);
