@@ -21,24 +21,29 @@ namespace vn {
 namespace {
 
 constexpr int kDumpThreads = 256;
-constexpr int kDumpGroups = 4;                                  // groups of 4 per thread
+constexpr int kDumpGroups = 8;                                  // groups of 4 per thread
 constexpr int64_t kDumpStride = kDumpThreads * 4;               // columns between a thread's groups
 constexpr int64_t kDumpChunk = kDumpStride * kDumpGroups;       // elements per CTA step
 // GAMMA * kDumpStride mod 2^64: the state difference between a thread's consecutive groups.
 constexpr uint64_t kDumpStep = kGamma * static_cast<uint64_t>(kDumpStride);
 
 // Grid-stride over (row i, chunk of kDumpChunk columns). Thread t makes the
-// 4-element groups at columns c + 4t + 1024g, g < 4: one 16-byte store per group,
+// 4-element groups at columns c + 4t + 1024g, g < 8: one 16-byte store per group,
 // consecutive lanes on consecutive 16-byte segments. The state of the next
 // element is the previous plus GAMMA and the state of the next group the
 // previous group's plus 1024*GAMMA, so no 64-bit multiply is needed per group.
 // vec4: every row starts 16-byte aligned (out aligned and n % 4 == 0).
+// kIdx32: the chunk count fits in 32 bits, so the row of a chunk is a 32-bit
+// division (a 64-bit one costs several instructions per element).
+template <bool kIdx32>
 __global__ void __launch_bounds__(kDumpThreads)
 noise_dump_kernel(const int64_t* __restrict__ seeds, int64_t n, uint64_t offset,
                   float* __restrict__ out, int64_t chunks_per_row, int64_t total_chunks,
                   int vec4) {
   for (int64_t c = blockIdx.x; c < total_chunks; c += gridDim.x) {
-    const int64_t i = c / chunks_per_row;
+    const int64_t i = kIdx32 ? static_cast<int64_t>(static_cast<uint32_t>(c) /
+                                                    static_cast<uint32_t>(chunks_per_row))
+                             : c / chunks_per_row;
     const int64_t t0 = (c - i * chunks_per_row) * kDumpChunk + threadIdx.x * 4;
     const uint64_t seed = static_cast<uint64_t>(__ldg(seeds + i));
     float* row = out + i * n;
@@ -129,8 +134,12 @@ cudaError_t launch_noise_dump(const int64_t* seeds, int64_t pop, int64_t n, uint
   const int64_t total = pop * chunks_per_row;
   const int vec4 = (n % 4 == 0) && (reinterpret_cast<uintptr_t>(out) % 16 == 0);
   const int64_t grid = std::min<int64_t>(total, static_cast<int64_t>(dev.sm_count) * 8);
-  noise_dump_kernel<<<static_cast<unsigned>(grid), kDumpThreads, 0, stream>>>(
-      seeds, n, offset, out, chunks_per_row, total, vec4);
+  if (total <= 0xFFFFFFFFll)
+    noise_dump_kernel<true><<<static_cast<unsigned>(grid), kDumpThreads, 0, stream>>>(
+        seeds, n, offset, out, chunks_per_row, total, vec4);
+  else
+    noise_dump_kernel<false><<<static_cast<unsigned>(grid), kDumpThreads, 0, stream>>>(
+        seeds, n, offset, out, chunks_per_row, total, vec4);
   return cudaGetLastError();
 }
 
