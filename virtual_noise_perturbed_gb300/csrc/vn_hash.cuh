@@ -66,10 +66,19 @@ __device__ __forceinline__ uint32_t mix_to_one_plus_u(uint32_t lo, uint32_t hi) 
   return ((l4 >> 9) ^ (h4 >> 8)) | kOneBits;
 }
 
+// The same on a 64-bit state (plain 64-bit adds on the state compile to a
+// carry pair that the compiler schedules better than hand-written ones).
+__device__ __forceinline__ uint32_t mix_to_one_plus_u(uint64_t state) {
+  return mix_to_one_plus_u(static_cast<uint32_t>(state), static_cast<uint32_t>(state >> 32));
+}
+
 // Bits from mix_to_one_plus_u -> the noise value (1 + u) - 1.5, exact.
 __device__ __forceinline__ float noise_from_bits(uint32_t bits) {
   return __uint_as_float(bits) - 1.5f;
 }
+
+// (idx + 1) * GAMMA mod 2^64: the per-element part of the state.
+__device__ __forceinline__ uint64_t index_term(uint64_t idx) { return (idx + 1ull) * kGamma; }
 
 // (idx + 1) * GAMMA mod 2^64 as halves: the per-element part of the state.
 __device__ __forceinline__ void index_term(uint64_t idx, uint32_t& lo, uint32_t& hi) {

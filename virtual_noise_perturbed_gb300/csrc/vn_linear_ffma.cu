@@ -144,7 +144,7 @@ linear_pop_kernel(const LinearArgs a, const PopParams q) {
 
         // This thread's chunks of W for the pass, and their state terms.
         float wm[CPT][8];
-        uint32_t blo[CPT], bhi[CPT];
+        uint64_t bst[CPT];
         uint32_t live = 0;
 #pragma unroll
         for (int cq = 0; cq < CPT; ++cq) {
@@ -156,18 +156,18 @@ linear_pop_kernel(const LinearArgs a, const PopParams q) {
             load8<kWBf16>(a.w, j * a.in + k, a.in - k, q.w_vec != 0, w);
 #pragma unroll
             for (int e = 0; e < 8; ++e) wm[cq][e] = w[e] + shift;
-            index_term(a.offset + static_cast<uint64_t>(j) * static_cast<uint64_t>(a.in) +
-                           static_cast<uint64_t>(k),
-                       blo[cq], bhi[cq]);
+            bst[cq] = index_term(a.offset + static_cast<uint64_t>(j) * static_cast<uint64_t>(a.in) +
+                                 static_cast<uint64_t>(k));
           } else {
 #pragma unroll
             for (int e = 0; e < 8; ++e) wm[cq][e] = 0.f;
-            blo[cq] = bhi[cq] = 0u;
+            bst[cq] = 0ull;
           }
         }
 
         for (int ii = 0; ii < np; ++ii) {
           const uint2 sd = s_seed[ii];
+          const uint64_t seed = (static_cast<uint64_t>(sd.y) << 32) | sd.x;
           float part[NB];
 #pragma unroll
           for (int r = 0; r < NB; ++r) part[r] = 0.f;
@@ -175,13 +175,12 @@ linear_pop_kernel(const LinearArgs a, const PopParams q) {
           for (int cq = 0; cq < CPT; ++cq) {
             if (live & (1u << cq)) {
               const int kk = 8 * (slot + slots * cq);
-              uint32_t lo = blo[cq], hi = bhi[cq];
-              add64(lo, hi, sd.x, sd.y);
+              uint64_t st = bst[cq] + seed;
               float wp[8];
 #pragma unroll
               for (int e = 0; e < 8; ++e) {
-                wp[e] = fmaf(sigma, __uint_as_float(mix_to_one_plus_u(lo, hi)), wm[cq][e]);
-                add64(lo, hi, kGammaLo, kGammaHi);
+                wp[e] = fmaf(sigma, __uint_as_float(mix_to_one_plus_u(st)), wm[cq][e]);
+                st += kGamma;
               }
 #pragma unroll
               for (int r = 0; r < NB; ++r) {

@@ -402,7 +402,8 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
     for (int64_t u = blockIdx.x; u < p.units; u += gridDim.x, tb.next(p.nbuf)) {
       const Unit un = decode(p, u, MH);
       const int b = tb.s;
-      if (!mbar_wait(tmem_full(b), tb.ph, s_abort, 256)) break;
+      // Off the critical path when TMEM is double-buffered: back off longer.
+      if (!mbar_wait(tmem_full(b), tb.ph, s_abort, p.nbuf == 2 ? 2000 : 300)) break;
       tc_fence_after();
       const uint32_t dcol = tmem + b * cols_per_buf + (static_cast<uint32_t>(quarter * 32) << 16);
       for (int ii = 0; ii < un.gcount; ++ii) {
@@ -514,16 +515,15 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
         // chunk q of the next group is loaded right after chunk q's use.
         constexpr bool kHoist = (MH == 1);
         float wm[kHoist ? kCPT : 1][8];
-        uint32_t blo[kCPT], bhi[kCPT];
-        uint32_t live = 0;  // bit q: chunk q holds real weights (row < out, k < in)
+        uint64_t bst[kCPT];  // (offset + j*in + k + 1) * GAMMA of each chunk's first element
+        uint32_t live = 0;   // bit q: chunk q holds real weights (row < out, k < in)
 #pragma unroll
         for (int q = 0; q < kCPT; ++q) {
           const int64_t j = un.m0 + rowq(q);
           if ((j < p.out) && (k < p.in)) live |= 1u << q;
           if constexpr (kHoist) unpack_shift(raw[q], shift, wm[q]);
-          index_term(p.offset + static_cast<uint64_t>(j) * static_cast<uint64_t>(p.in) +
-                         static_cast<uint64_t>(k),
-                     blo[q], bhi[q]);
+          bst[q] = index_term(p.offset + static_cast<uint64_t>(j) * static_cast<uint64_t>(p.in) +
+                              static_cast<uint64_t>(k));
         }
         const bool has_next = (kc + 1 < p.k_chunks) || has_next_unit;
         const Unit& lun = (kc + 1 < p.k_chunks) ? un : nun;
@@ -556,13 +556,12 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
               float wl[8];
               if constexpr (!kHoist) unpack_shift(raw[q], shift, wl);
               const float* w8 = kHoist ? wm[kHoist ? q : 0] : wl;
-              uint32_t lo = blo[q], hi = bhi[q];
-              add64(lo, hi, static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
+              uint64_t st = bst[q] + seed;
               float pv[8];
 #pragma unroll
               for (int e = 0; e < 8; ++e) {
-                pv[e] = fmaf(sigma, __uint_as_float(mix_to_one_plus_u(lo, hi)), w8[e]);
-                add64(lo, hi, kGammaLo, kGammaHi);
+                pv[e] = fmaf(sigma, __uint_as_float(mix_to_one_plus_u(st)), w8[e]);
+                st += kGamma;
               }
 #pragma unroll
               for (int e = 0; e < 4; ++e) out4[e] = pack_bf16x2(pv[2 * e], pv[2 * e + 1]);

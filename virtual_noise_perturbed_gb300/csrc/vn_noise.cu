@@ -47,9 +47,7 @@ noise_dump_kernel(const int64_t* __restrict__ seeds, int64_t n, uint64_t offset,
     const int64_t t0 = (c - i * chunks_per_row) * kDumpChunk + threadIdx.x * 4;
     const uint64_t seed = static_cast<uint64_t>(__ldg(seeds + i));
     float* row = out + i * n;
-    uint32_t glo, ghi;  // state of the first element of the current group
-    index_term(offset + static_cast<uint64_t>(t0), glo, ghi);
-    add64(glo, ghi, static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
+    uint64_t gst = index_term(offset + static_cast<uint64_t>(t0)) + seed;  // first element of the group
     // number of this thread's groups that start inside the row
     const int64_t left = n - t0;
     const int full = left <= 0 ? 0 : static_cast<int>((left + kDumpStride - 1) / kDumpStride < kDumpGroups ? (left + kDumpStride - 1) / kDumpStride : kDumpGroups);
@@ -57,12 +55,12 @@ noise_dump_kernel(const int64_t* __restrict__ seeds, int64_t n, uint64_t offset,
     for (int g = 0; g < kDumpGroups; ++g) {
       if (g < full) {
         const int64_t t = t0 + g * kDumpStride;
-        uint32_t lo = glo, hi = ghi;
+        uint64_t st = gst;
         float v[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          v[q] = noise_from_bits(mix_to_one_plus_u(lo, hi));
-          add64(lo, hi, kGammaLo, kGammaHi);
+          v[q] = noise_from_bits(mix_to_one_plus_u(st));
+          st += kGamma;
         }
         if (vec4 && t + 4 <= n) {
           __stcs(reinterpret_cast<float4*>(row + t), make_float4(v[0], v[1], v[2], v[3]));
@@ -71,7 +69,7 @@ noise_dump_kernel(const int64_t* __restrict__ seeds, int64_t n, uint64_t offset,
           for (int q = 0; q < 4; ++q)
             if (t + q < n) row[t + q] = v[q];
         }
-        add64(glo, ghi, static_cast<uint32_t>(kDumpStep), static_cast<uint32_t>(kDumpStep >> 32));
+        gst += kDumpStep;
       }
     }
   }
@@ -91,9 +89,7 @@ reduce_metric_kernel(const float* __restrict__ center, const int64_t* __restrict
     const uint64_t seed = static_cast<uint64_t>(__ldg(seeds + i));
     float acc = 0.f;
     for (int64_t k = static_cast<int64_t>(threadIdx.x) * 4; k < n; k += kMetricThreads * 4) {
-      uint32_t lo, hi;
-      index_term(offset + static_cast<uint64_t>(k), lo, hi);
-      add64(lo, hi, static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
+      uint64_t st = index_term(offset + static_cast<uint64_t>(k)) + seed;
       float c[4];
       if (vec4 && k + 4 <= n) {
         const float4 c4 = __ldg(reinterpret_cast<const float4*>(center + k));
@@ -104,9 +100,9 @@ reduce_metric_kernel(const float* __restrict__ center, const int64_t* __restrict
       }
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const float v = fabsf(fmaf(sigma, noise_from_bits(mix_to_one_plus_u(lo, hi)), c[q]));
+        const float v = fabsf(fmaf(sigma, noise_from_bits(mix_to_one_plus_u(st)), c[q]));
         if (k + q < n) acc += v;
-        add64(lo, hi, kGammaLo, kGammaHi);
+        st += kGamma;
       }
     }
 #pragma unroll
