@@ -57,10 +57,14 @@ grad_kernel(const float* __restrict__ fitness, const int64_t* __restrict__ seeds
 
   for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
     const int64_t e0 = tile * kTile + lane * kE;
-    uint64_t bst[kE];  // (offset + e + 1) * GAMMA for this lane's elements
-    bst[0] = index_term(offset + static_cast<uint64_t>(e0));
+    uint32_t blo[kE], bhi[kE];  // (offset + e + 1) * GAMMA for this lane's elements
+    index_term(offset + static_cast<uint64_t>(e0), blo[0], bhi[0]);
 #pragma unroll
-    for (int e = 1; e < kE; ++e) bst[e] = bst[e - 1] + kGamma;
+    for (int e = 1; e < kE; ++e) {
+      blo[e] = blo[e - 1];
+      bhi[e] = bhi[e - 1];
+      add64(blo[e], bhi[e], kGammaLo, kGammaHi);
+    }
     float acc[kE];
 #pragma unroll
     for (int e = 0; e < kE; ++e) acc[e] = 0.f;
@@ -77,10 +81,12 @@ grad_kernel(const float* __restrict__ fitness, const int64_t* __restrict__ seeds
       for (int q = warp; q < cn; q += kWarps) {
         const uint4 v = s_ind[q];
         const float f = __uint_as_float(v.z);
-        const uint64_t seed = (static_cast<uint64_t>(v.y) << 32) | v.x;
 #pragma unroll
-        for (int e = 0; e < kE; ++e)
-          acc[e] = fmaf(f, noise_from_bits(mix_to_one_plus_u(bst[e] + seed)), acc[e]);
+        for (int e = 0; e < kE; ++e) {
+          uint32_t lo = blo[e], hi = bhi[e];
+          add64(lo, hi, v.x, v.y);
+          acc[e] = fmaf(f, noise_from_bits(mix_to_one_plus_u(lo, hi)), acc[e]);
+        }
       }
     }
 
