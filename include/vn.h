@@ -70,7 +70,7 @@ typedef enum vn_path {
   VN_PATH_AUTO = 0,  /* VN_PATH_TC when it applies and batch >= 16, else FFMA      */
   VN_PATH_FFMA = 1,  /* CUDA-core path: any dtypes, any batch                       */
   VN_PATH_TC = 2     /* tcgen05/TMEM path: x bf16, in % 8 == 0, x and w 16-byte     */
-                     /* aligned, pop, batch and in below 2^31                       */
+                     /* aligned, pop, batch, in and out below 2^31                 */
 } vn_path;
 
 /* Element-wise activation applied to Y after the bias (vn_perturbed_linear_ex). */
