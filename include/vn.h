@@ -158,6 +158,26 @@ vn_status vn_reduce_metric(const float* center, const int64_t* seeds, int64_t po
  * since the last call, VN_ERR_CUDA if synchronisation failed, else VN_OK. */
 vn_status vn_device_status(void* stream);
 
+/* Test hook for the bounded-wait machinery of the tensor-core kernel; not part
+ * of the method. Runs the tensor-core forward with the arguments of
+ * vn_perturbed_linear (validated the same way, VN_PATH_TC) but with every
+ * barrier wait limited to `timeout_ms` (0 < timeout_ms <= 60000) and one
+ * hashing thread of the first CTA skipping its arrive at stage
+ * `withhold_stage` (>= 0), so that the MMA thread's wait on that stage can
+ * never complete. The kernel must record VN_ERR_TIMEOUT in the status word,
+ * stop every role, wait (bounded) for its copies and MMAs in flight, free its
+ * tensor memory and return; vn_device_status() then reports VN_ERR_TIMEOUT and
+ * the context stays usable. y is left partly unwritten. No GPU fault, trap or
+ * hang is involved. If the CTA has fewer stages than withhold_stage, nothing is
+ * withheld and the call completes normally. */
+vn_status vn_testhook_linear_tc_withhold(const void* x, vn_dtype x_dt, int x_shared,
+                                         const void* w, vn_dtype w_dt,
+                                         const void* b, vn_dtype b_dt,
+                                         const int64_t* seeds, int64_t pop, int64_t batch,
+                                         int64_t in, int64_t out, double sigma, uint64_t offset,
+                                         void* y, vn_dtype y_dt, int64_t withhold_stage,
+                                         double timeout_ms, void* stream);
+
 /* A static, human-readable name for a status code. */
 const char* vn_status_string(vn_status status);
 

@@ -221,6 +221,37 @@ vn_status vn_perturbed_linear(const void* x, vn_dtype x_dt, int x_shared, const 
                                 sigma, offset, y, y_dt, VN_PATH_AUTO, VN_ACT_NONE, stream);
 }
 
+vn_status vn_testhook_linear_tc_withhold(const void* x, vn_dtype x_dt, int x_shared, const void* w,
+                                         vn_dtype w_dt, const void* b, vn_dtype b_dt,
+                                         const int64_t* seeds, int64_t pop, int64_t batch,
+                                         int64_t in, int64_t out, double sigma, uint64_t offset,
+                                         void* y, vn_dtype y_dt, int64_t withhold_stage,
+                                         double timeout_ms, void* stream) {
+  if (!(timeout_ms > 0.0) || !(timeout_ms <= 60000.0) || withhold_stage < 0) return VN_ERR_VALUE;
+  // Validate exactly as a forced tensor-core call would (this launches nothing:
+  // pop = 0 makes the output empty).
+  vn_status st = vn_perturbed_linear_ex(x, x_dt, x_shared, w, w_dt, b, b_dt, seeds, 0, batch, in,
+                                        out, sigma, offset, y, y_dt, VN_PATH_TC, VN_ACT_NONE,
+                                        stream);
+  if (st != VN_OK) return st;
+  if (pop < 1 || batch < 1 || out < 1) return VN_ERR_SHAPE;
+  if (seeds == nullptr || y == nullptr || x == nullptr || w == nullptr) return VN_ERR_NULL;
+  vn::DeviceInfo dev;
+  cudaError_t err = vn::device_info(&dev);
+  if (err != cudaSuccess) return cuda_failure(err);
+  if (!device_is_cc10(dev)) return VN_ERR_DEVICE;
+  if (!vn::linear_tc_applies(x, x_dt, w, w_dt, batch, in, out) || pop > (int64_t{1} << 31) - 1)
+    return VN_ERR_PATH;
+  vn::LinearArgs a;
+  a.x = x; a.x_dt = x_dt; a.x_shared = x_shared ? 1 : 0;
+  a.w = w; a.w_dt = w_dt; a.b = b; a.b_dt = b_dt;
+  a.seeds = seeds; a.pop = pop; a.batch = batch; a.in = in; a.out = out;
+  a.sigma = static_cast<float>(sigma); a.offset = offset; a.y = y; a.y_dt = y_dt;
+  a.act = VN_ACT_NONE;
+  return launched(vn::launch_linear_tc_hook(a, static_cast<cudaStream_t>(stream), withhold_stage,
+                                            static_cast<unsigned long long>(timeout_ms * 1e6)));
+}
+
 vn_status vn_device_status(void* stream) {
   cudaError_t err = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (err != cudaSuccess) return cuda_failure(err);

@@ -59,6 +59,11 @@ bool linear_tc_applies(const void* x, vn_dtype x_dt, const void* w, vn_dtype w_d
                        int64_t batch, int64_t in, int64_t out);
 // tcgen05/TMEM forward (x bf16).
 cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream);
+// The same with every barrier wait bounded by timeout_ns and, when
+// withhold_stage >= 0, one hashing thread of CTA 0 skipping its arrive at that
+// stage (test hook for the bounded-wait path).
+cudaError_t launch_linear_tc_hook(const LinearArgs& a, cudaStream_t stream, long long withhold_stage,
+                                  unsigned long long timeout_ns);
 
 // Reads and clears the device status word of the bounded-wait kernels (0 = fine).
 cudaError_t take_device_status(unsigned int* status, cudaStream_t stream);

@@ -55,7 +55,7 @@ constexpr int kHashThreads = kHashWarps * 32;                 // 512
 constexpr int kKC = 64;                                       // k per stage (128 bytes of bf16)
 constexpr uint32_t kHalfBytes = 128 * 128;                    // 128 rows x 128 bytes
 constexpr int kTmemCols = 512;
-constexpr unsigned long long kTimeoutNs = 4000000000ull;      // 4 s per wait
+constexpr unsigned long long kTimeoutNs = 4000000000ull;      // default limit of one wait: 4 s
 
 struct TcParams {
   const void* w;
@@ -69,6 +69,16 @@ struct TcParams {
   int b_bf16, act;
   int nt, g, nbuf, stages, k_chunks, x_shared;
   uint32_t stage_bytes, a_bytes, idesc;
+  unsigned long long timeout_ns;  // limit of every barrier wait
+  long long withhold_stage;       // test hook: >= 0 makes one thread skip that stage's arrive
+};
+
+// Shared by a CTA's roles: the abort flag (set by the first wait that runs out)
+// and the limit of every wait.
+struct WaitCtl {
+  int abort;
+  int pad;
+  unsigned long long timeout_ns;
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -121,26 +131,27 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t par
 // another role of the CTA has already aborted. Each poll suspends the thread
 // for up to kSuspendNs (it resumes as soon as the phase completes).
 constexpr uint32_t kSuspendNs = 200000;
-__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
-                                            volatile int* abort_flag, uint32_t sleep_ns) {
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile WaitCtl* ctl,
+                                            uint32_t sleep_ns) {
   const uint64_t t0 = global_ns();
+  const unsigned long long limit = ctl->timeout_ns;
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait_suspend(bar, parity, kSuspendNs)) return true;
     if (sleep_ns) __nanosleep(sleep_ns);
     if ((n & 3) == 0) {
-      if (*abort_flag) return false;
-      if (global_ns() - t0 > kTimeoutNs) {
+      if (ctl->abort) return false;
+      if (global_ns() - t0 > limit) {
         atomicOr(&g_device_status, 1u);
-        *abort_flag = 1;
+        ctl->abort = 1;
         return false;
       }
     }
   }
 }
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile WaitCtl* ctl,
                                           uint32_t sleep_ns = 0) {
   if (mbar_try_wait(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity, abort_flag, sleep_ns);
+  return mbar_wait_slow(bar, parity, ctl, sleep_ns);
 }
 // Position in a ring of S slots: slot index and the parity of its current use.
 struct Ring {
@@ -278,7 +289,7 @@ __device__ __forceinline__ Unit decode(const TcParams& p, int64_t u, int mh) {
 }
 
 // ---------------------------------------------------------------- the kernel
-template <int MH, int KA, bool kWBf16, bool kYBf16>
+template <int MH, bool kWBf16, bool kYBf16>
 __global__ void __launch_bounds__(kThreads, 1)
 linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -295,7 +306,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
   auto tmem_empty = [&](int b) { return bar0 + 8u * (3 * S + 2 + b); };
   const uint32_t drain = bar0 + 8u * (3 * S + 4);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 3 * S + 5);
-  volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+  volatile WaitCtl* s_abort = reinterpret_cast<volatile WaitCtl*>(bars + 3 * S + 6);
   const uint32_t stage0 = smem_u32(smem);
 
   const int warp = threadIdx.x >> 5;
@@ -312,7 +323,8 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
       mbar_init(tmem_empty(b), 128);
     }
     mbar_init(drain, 1);
-    *s_abort = 0;
+    s_abort->abort = 0;
+    s_abort->timeout_ns = p.timeout_ns;
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -331,19 +343,17 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
       uint32_t it = 0;
       Ring rg;
       bool ok = true;
-      const uint32_t x_box = static_cast<uint32_t>(p.nt) * 128u;
+      const uint32_t x_bytes = static_cast<uint32_t>(p.nt) * 128u;
       for (int64_t u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
         const Unit un = decode(p, u, MH);
         for (int kc = 0; ok && kc < p.k_chunks; ++kc) {
           for (int ii = 0; ii < un.gcount; ++ii, ++it, rg.next(S)) {
             const int s = rg.s;
             if (!(ok = mbar_wait(empty(s), rg.ph ^ 1u, s_abort, 32))) break;
-            mbar_expect_tx(full_x(s), KA * x_box);
+            mbar_expect_tx(full_x(s), x_bytes);
             const int ind = p.x_shared ? 0 : static_cast<int>(un.i0 + ii);
-#pragma unroll
-            for (int a = 0; a < KA; ++a)
-              tma_load_3d(stage0 + s * p.stage_bytes + p.a_bytes + a * x_box, &xmap, full_x(s),
-                          (kc * KA + a) * kKC, static_cast<int>(un.n0), ind);
+            tma_load_3d(stage0 + s * p.stage_bytes + p.a_bytes, &xmap, full_x(s), kc * kKC,
+                        static_cast<int>(un.n0), ind);
           }
         }
       }
@@ -354,7 +364,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
           const uint32_t j = it - 1 - k;
           const uint64_t t0 = global_ns();
           while (!mbar_try_wait(full_x(static_cast<int>(j % S)), (j / S) & 1u) &&
-                 global_ns() - t0 < kTimeoutNs) {
+                 global_ns() - t0 < p.timeout_ns) {
           }
         }
       }
@@ -378,16 +388,13 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
             tc_fence_after();
             const uint32_t a0 = stage0 + s * p.stage_bytes;
             const uint32_t b0 = a0 + p.a_bytes;
-            // K steps of 16 over the KA atoms of the stage: atom a, 32-byte step within it.
 #pragma unroll
-            for (int ks = 0; ks < KA * (kKC / 16); ++ks) {
-              const int a = ks >> 2, sub = ks & 3;
-              const uint64_t bdesc = sdesc_sw128(b0 + a * p.nt * 128u + sub * 32);
+            for (int ks = 0; ks < kKC / 16; ++ks) {
+              const uint64_t bdesc = sdesc_sw128(b0 + ks * 32);
 #pragma unroll
               for (int h = 0; h < MH; ++h) {
-                umma_bf16(dcol + (ii * MH + h) * p.nt,
-                          sdesc_sw128(a0 + (a * MH + h) * kHalfBytes + sub * 32), bdesc, p.idesc,
-                          (kc | ks) != 0);
+                umma_bf16(dcol + (ii * MH + h) * p.nt, sdesc_sw128(a0 + h * kHalfBytes + ks * 32),
+                          bdesc, p.idesc, (kc | ks) != 0);
               }
             }
             umma_commit(empty(s));
@@ -398,7 +405,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
       // All issued MMAs have completed once this commit arrives.
       umma_commit(drain);
       const uint64_t t0 = global_ns();
-      while (!mbar_try_wait(drain, 0) && global_ns() - t0 < kTimeoutNs) {
+      while (!mbar_try_wait(drain, 0) && global_ns() - t0 < p.timeout_ns) {
       }
     }
   } else if (warp < kFirstHashWarp) {
@@ -430,20 +437,15 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
                 static_cast<uint64_t>(j);
             bias = fmaf(p.sigma, noise_at(seed, bidx), bj);
           }
-          // Two 16-column loads in flight per wait.
-          for (int c0 = 0; c0 < p.nt; c0 += 32) {
-            uint32_t v[32];
-            tmem_ld16(dcol + (ii * MH + h) * p.nt + c0, *reinterpret_cast<uint32_t(*)[16]>(v));
-            const bool two = c0 + 16 < p.nt;
-            if (two)
-              tmem_ld16(dcol + (ii * MH + h) * p.nt + c0 + 16,
-                        *reinterpret_cast<uint32_t(*)[16]>(v + 16));
+          for (int c0 = 0; c0 < p.nt; c0 += 16) {
+            uint32_t v[16];
+            tmem_ld16(dcol + (ii * MH + h) * p.nt + c0, v);
             tmem_wait_ld();
             if (jok) {
 #pragma unroll
-              for (int q = 0; q < 32; ++q) {
+              for (int q = 0; q < 16; ++q) {
                 const int64_t n = un.n0 + c0 + q;
-                if ((q < 16 || two) && n < p.batch) {
+                if (n < p.batch) {
                   float val = __uint_as_float(v[q]) + bias;
                   if (p.act == VN_ACT_TANH) val = tanhf(val);
                   const int64_t o = (i * p.batch + n) * p.out + j;
@@ -465,32 +467,27 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
     }
   } else {
     // ----------------------------------------------------------------- hashing
-    // A stage's A tile is KA swizzle atoms along k (64 k each), each atom
-    // 128*MH rows x 128 bytes; row r of an atom sits at (r >> 3)*1024 + (r & 7)*128
-    // (the two 128-row halves of an MH = 2 atom are contiguous). Thread t writes
-    // 16-byte chunk (t & 7) of rows (t >> 3) + 64*rb of every atom, so one
-    // 128-byte row is written by 8 lanes and each quarter-warp store covers all
-    // 32 banks once (the swizzle permutes the chunks within a row). Chunk q of a
-    // thread is (atom q % KA, row block q / KA).
-    constexpr int kCPT = 2 * MH * KA;  // 16-byte chunks per thread per stage
+    // Thread t writes 16-byte chunk (t & 7) of rows (t >> 3) + 64q of the
+    // (128*MH)-row A tile, q < 2*MH: one 128-byte row per 8 lanes, so each
+    // quarter-warp store covers all 32 banks once (the swizzle permutes the
+    // chunks within a row). The two 128-row halves of an MH=2 tile are
+    // contiguous, so row r sits at (r >> 3)*1024 + (r & 7)*128 for any r < 256.
+    constexpr int kCPT = MH * 2;  // chunks per thread per stage
     using Raw = typename std::conditional<kWBf16, RawBf16, RawF32>::type;
     const int t = threadIdx.x - kFirstHashWarp * 32;
     const int cc = t & 7;
     const int r8 = (t >> 3) & 7;
     const uint32_t soff0 = static_cast<uint32_t>(t >> 6) * 1024u + r8 * 128u + ((cc ^ r8) << 4);
     const int row0 = t >> 3;
-    auto soff = [&](int q) { return (q % KA) * MH * kHalfBytes + soff0 + (q / KA) * 8192u; };
-    auto rowq = [&](int q) { return row0 + (q / KA) * 64; };
-    auto kq = [&](int kc, int q) {
-      return (static_cast<int64_t>(kc) * KA + q % KA) * kKC + cc * 8;
-    };
+    auto soff = [&](int q) { return soff0 + q * 8192u; };
+    auto rowq = [&](int q) { return row0 + q * 64; };
     const float sigma = p.sigma;
     const float shift = -1.5f * sigma;
 
     // W for chunk q of the stage group (u, kc): 8 consecutive k of one row.
     auto load_chunk = [&](const Unit& un, int kc, int q, Raw& r) {
       const int64_t j = un.m0 + rowq(q);
-      const int64_t k = kq(kc, q);
+      const int64_t k = static_cast<int64_t>(kc) * kKC + cc * 8;
       if (j < p.out && k < p.in) {
         if constexpr (kWBf16) {
           r.a = __ldg(reinterpret_cast<const uint4*>(
@@ -504,12 +501,16 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
       }
     };
 
-    // raw[q] holds chunk q's weights for the current stage group; the next
-    // group's chunk q is loaded right after chunk q's last use (the group's last
-    // individual), so its latency is covered by the rest of that stage. The seed
-    // of the next stage is likewise loaded one stage ahead.
+    // raw holds the W chunks of the next stage group: at the start of a group
+    // they are turned into W - 1.5*sigma (fp32, shared by the group's G
+    // individuals) and the loads for the following group are issued at once,
+    // so a whole group of stages covers their latency. The seed of the next
+    // stage is likewise loaded one stage ahead.
     Raw raw[kCPT];
     Ring rg;
+    // Test hook: the stage at which this thread skips its arrive (-1: never).
+    int withhold_at = (p.withhold_stage >= 0 && p.withhold_stage < 0x7FFFFFFF && blockIdx.x == 0 &&
+                       t == 0) ? static_cast<int>(p.withhold_stage) : -1;
     bool ok = true;
     int64_t u = blockIdx.x;
     uint64_t seed_next = 0;
@@ -522,21 +523,34 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
     for (; ok && u < p.units; u += gridDim.x) {
       const Unit un = decode(p, u, MH);
       const bool has_next_unit = u + gridDim.x < p.units;
+      const Unit nun = has_next_unit ? decode(p, u + gridDim.x, MH) : un;
       for (int kc = 0; ok && kc < p.k_chunks; ++kc) {
+        const int64_t k = static_cast<int64_t>(kc) * kKC + cc * 8;
+        // kHoist (G may exceed 1): W - 1.5*sigma is formed once per group in
+        // wm and the next group's loads go out at once. Otherwise (MH = 2,
+        // one individual per unit, tight registers) W is unpacked per use and
+        // chunk q of the next group is loaded right after chunk q's use.
+        constexpr bool kHoist = (MH == 1);
+        float wm[kHoist ? kCPT : 1][8];
         uint64_t bst[kCPT];  // (offset + j*in + k + 1) * GAMMA of each chunk's first element
         uint32_t live = 0;   // bit q: chunk q holds real weights (row < out, k < in)
 #pragma unroll
         for (int q = 0; q < kCPT; ++q) {
           const int64_t j = un.m0 + rowq(q);
-          const int64_t k = kq(kc, q);
           if ((j < p.out) && (k < p.in)) live |= 1u << q;
+          if constexpr (kHoist) unpack_shift(raw[q], shift, wm[q]);
           bst[q] = index_term(p.offset + static_cast<uint64_t>(j) * static_cast<uint64_t>(p.in) +
                               static_cast<uint64_t>(k));
         }
-        // where the next stage group is: this unit's next k chunk, or the next unit's first
         const bool has_next = (kc + 1 < p.k_chunks) || has_next_unit;
-        const Unit lun = (kc + 1 < p.k_chunks || !has_next) ? un : decode(p, u + gridDim.x, MH);
+        const Unit& lun = (kc + 1 < p.k_chunks) ? un : nun;
         const int lkc = (kc + 1 < p.k_chunks) ? kc + 1 : 0;
+        if constexpr (kHoist) {
+          if (has_next) {
+#pragma unroll
+            for (int q = 0; q < kCPT; ++q) load_chunk(lun, lkc, q, raw[q]);
+          }
+        }
         for (int ii = 0; ii < un.gcount; ++ii, rg.next(S)) {
           const int s = rg.s;
           const uint64_t seed = seed_next;
@@ -547,7 +561,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
           } else if (kc + 1 < p.k_chunks) {
             seed_next = static_cast<uint64_t>(__ldg(p.seeds + un.i0));
           } else if (has_next_unit) {
-            seed_next = static_cast<uint64_t>(__ldg(p.seeds + lun.i0));
+            seed_next = static_cast<uint64_t>(__ldg(p.seeds + nun.i0));
           }
           if (!(ok = mbar_wait(empty(s), rg.ph ^ 1u, s_abort))) break;
           const uint32_t a0 = stage0 + s * p.stage_bytes;
@@ -556,8 +570,9 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
           for (int q = 0; q < kCPT; ++q) {
             uint32_t out4[4] = {0u, 0u, 0u, 0u};
             if (live & (1u << q)) {
-              float w8[8];
-              unpack_shift(raw[q], shift, w8);
+              float wl[8];
+              if constexpr (!kHoist) unpack_shift(raw[q], shift, wl);
+              const float* w8 = kHoist ? wm[kHoist ? q : 0] : wl;
               uint64_t st = bst[q] + seed;
               float pv[8];
 #pragma unroll
@@ -568,11 +583,14 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
 #pragma unroll
               for (int e = 0; e < 4; ++e) out4[e] = pack_bf16x2(pv[2 * e], pv[2 * e + 1]);
             }
-            if (last && has_next) load_chunk(lun, lkc, q, raw[q]);
+            if constexpr (!kHoist) {
+              if (last && has_next) load_chunk(lun, lkc, q, raw[q]);
+            }
             st_shared_v4(a0 + soff(q), out4[0], out4[1], out4[2], out4[3]);
           }
           fence_proxy_async_smem();
-          mbar_arrive(full_a(s));
+          if (withhold_at != 0) mbar_arrive(full_a(s));
+          if (withhold_at >= 0) --withhold_at;
         }
       }
     }
@@ -601,10 +619,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-template <int MH, int KA, bool kW, bool kY>
+template <int MH, bool kW, bool kY>
 cudaError_t launch_typed(const CUtensorMap& xmap, const TcParams& p, int grid, size_t smem,
                          cudaStream_t stream) {
-  auto fn = linear_tc_kernel<MH, KA, kW, kY>;
+  auto fn = linear_tc_kernel<MH, kW, kY>;
   static size_t configured = 0;
   if (configured < smem) {
     cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -628,6 +646,11 @@ bool linear_tc_applies(const void* x, vn_dtype x_dt, const void* w, vn_dtype w_d
 }
 
 cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
+  return launch_linear_tc_hook(a, stream, -1, kTimeoutNs);
+}
+
+cudaError_t launch_linear_tc_hook(const LinearArgs& a, cudaStream_t stream, long long withhold_stage,
+                                  unsigned long long timeout_ns) {
   DeviceInfo dev;
   cudaError_t err = device_info(&dev);
   if (err != cudaSuccess) return err;
@@ -650,22 +673,21 @@ cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
   p.nt = static_cast<int>(nt);
   p.g = g;
   p.nbuf = (static_cast<int64_t>(g) * mh * nt <= kTmemCols / 2) ? 2 : 1;
-  // Stage depth along k: two swizzle atoms (128 k) for 128-row tiles, one for
-  // 256-row tiles, so that every hashing thread writes 4 chunks per stage.
-  const int ka = (mh == 1) ? 2 : 1;
-  p.a_bytes = static_cast<uint32_t>(mh * ka) * kHalfBytes;
-  p.stage_bytes = p.a_bytes + static_cast<uint32_t>(ka * nt) * 128u;
-  const size_t fixed = 1024 + 8 * (3 * 16 + 5) + 16;
+  p.a_bytes = static_cast<uint32_t>(mh) * kHalfBytes;
+  p.stage_bytes = p.a_bytes + static_cast<uint32_t>(nt) * 128u;
+  const size_t fixed = 1024 + 8 * (3 * 16 + 6) + 16;
   const int stages = static_cast<int>(std::min<int64_t>(
       8, (static_cast<int64_t>(dev.smem_optin) - static_cast<int64_t>(fixed)) / p.stage_bytes));
   if (stages < 2) return cudaErrorInvalidConfiguration;
   p.stages = stages;
-  p.k_chunks = static_cast<int>((a.in + kKC * ka - 1) / (kKC * ka));
+  p.k_chunks = static_cast<int>((a.in + kKC - 1) / kKC);
   p.m_tiles = (a.out + 128 * mh - 1) / (128 * mh);
   p.n_tiles = (a.batch + nt - 1) / nt;
   const int64_t groups = (a.pop + g - 1) / g;
   p.units = groups * p.n_tiles * p.m_tiles;
   p.x_shared = a.x_shared;
+  p.timeout_ns = timeout_ns;
+  p.withhold_stage = withhold_stage;
   // Instruction descriptor: fp32 accumulator, bf16 A and B, both K-major,
   // N = nt (bits 17-22, N >> 3), M = 128 (bits 24-28, M >> 4).
   p.idesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(nt >> 3) << 17) |
@@ -690,14 +712,14 @@ cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream) {
   const int grid = static_cast<int>(std::min<int64_t>(p.units, dev.sm_count));
   const bool ybf = a.y_dt == VN_BF16;
   if (mh == 2) {
-    return ybf ? launch_typed<2, 1, true, true>(xmap, p, grid, smem, stream)
-               : launch_typed<2, 1, true, false>(xmap, p, grid, smem, stream);
+    return ybf ? launch_typed<2, true, true>(xmap, p, grid, smem, stream)
+               : launch_typed<2, true, false>(xmap, p, grid, smem, stream);
   }
   if (wbf) {
-    return ybf ? launch_typed<1, 2, true, true>(xmap, p, grid, smem, stream)
-               : launch_typed<1, 2, true, false>(xmap, p, grid, smem, stream);
+    return ybf ? launch_typed<1, true, true>(xmap, p, grid, smem, stream)
+               : launch_typed<1, true, false>(xmap, p, grid, smem, stream);
   }
-  return launch_typed<1, 2, false, false>(xmap, p, grid, smem, stream);
+  return launch_typed<1, false, false>(xmap, p, grid, smem, stream);
 }
 
 cudaError_t take_device_status(unsigned int* status, cudaStream_t stream) {
