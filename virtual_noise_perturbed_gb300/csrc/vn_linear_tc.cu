@@ -56,6 +56,12 @@ constexpr int kKC = 64;                                       // k per stage (12
 constexpr uint32_t kHalfBytes = 128 * 128;                    // 128 rows x 128 bytes
 constexpr int kTmemCols = 512;
 constexpr unsigned long long kTimeoutNs = 4000000000ull;      // default limit of one wait: 4 s
+// Back-off between polls of roles that run stages ahead of their consumers.
+constexpr uint32_t kProducerSleepNs = 256;
+constexpr uint32_t kMmaSleepNs = 64;
+constexpr int kEpilogueFirstThread = 2 * 32;  // warps 2..5
+constexpr int kEpilogueThreads = 4 * 32;
+constexpr int kEpilogueBarrier = 1;           // named barrier id (0 is __syncthreads)
 
 struct TcParams {
   const void* w;
@@ -164,6 +170,10 @@ struct Ring {
     }
   }
 };
+// Named CTA barrier among `count` threads; may be reached by a divergent warp.
+__device__ __forceinline__ void named_barrier_sync(int id, int count) {
+  asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
@@ -349,7 +359,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
         for (int kc = 0; ok && kc < p.k_chunks; ++kc) {
           for (int ii = 0; ii < un.gcount; ++ii, ++it, rg.next(S)) {
             const int s = rg.s;
-            if (!(ok = mbar_wait(empty(s), rg.ph ^ 1u, s_abort, 32))) break;
+            if (!(ok = mbar_wait(empty(s), rg.ph ^ 1u, s_abort, kProducerSleepNs))) break;
             mbar_expect_tx(full_x(s), x_bytes);
             const int ind = p.x_shared ? 0 : static_cast<int>(un.i0 + ii);
             tma_load_3d(stage0 + s * p.stage_bytes + p.a_bytes, &xmap, full_x(s), kc * kKC,
@@ -377,14 +387,14 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
       for (int64_t u = blockIdx.x; ok && u < p.units; u += gridDim.x, tb.next(p.nbuf)) {
         const Unit un = decode(p, u, MH);
         const int b = tb.s;
-        if (!(ok = mbar_wait(tmem_empty(b), tb.ph ^ 1u, s_abort))) break;
+        if (!(ok = mbar_wait(tmem_empty(b), tb.ph ^ 1u, s_abort, kMmaSleepNs))) break;
         tc_fence_after();
         const uint32_t dcol = tmem + b * cols_per_buf;
         for (int kc = 0; ok && kc < p.k_chunks; ++kc) {
           for (int ii = 0; ii < un.gcount; ++ii, rg.next(S)) {
             const int s = rg.s;
-            if (!(ok = mbar_wait(full_x(s), rg.ph, s_abort))) break;
-            if (!(ok = mbar_wait(full_a(s), rg.ph, s_abort))) break;
+            if (!(ok = mbar_wait(full_x(s), rg.ph, s_abort, kMmaSleepNs))) break;
+            if (!(ok = mbar_wait(full_a(s), rg.ph, s_abort, kMmaSleepNs))) break;
             tc_fence_after();
             const uint32_t a0 = stage0 + s * p.stage_bytes;
             const uint32_t b0 = a0 + p.a_bytes;
@@ -416,8 +426,14 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
     for (int64_t u = blockIdx.x; u < p.units; u += gridDim.x, tb.next(p.nbuf)) {
       const Unit un = decode(p, u, MH);
       const int b = tb.s;
-      // Off the critical path when TMEM is double-buffered: back off longer.
-      if (!mbar_wait(tmem_full(b), tb.ph, s_abort, p.nbuf == 2 ? 2000 : 300)) break;
+      // One thread polls (backing off longer when TMEM is double-buffered and the
+      // epilogue is off the critical path); the other 127 epilogue threads block
+      // on a named barrier, which takes no issue slots.
+      if (threadIdx.x == kEpilogueFirstThread)
+        mbar_wait(tmem_full(b), tb.ph, s_abort, p.nbuf == 2 ? 2000 : 300);
+      named_barrier_sync(kEpilogueBarrier, kEpilogueThreads);
+      __syncwarp();
+      if (s_abort->abort) break;
       tc_fence_after();
       const uint32_t dcol = tmem + b * cols_per_buf + (static_cast<uint32_t>(quarter * 32) << 16);
       for (int ii = 0; ii < un.gcount; ++ii) {
