@@ -483,20 +483,21 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
     }
   } else {
     // ----------------------------------------------------------------- hashing
-    // Thread t writes 16-byte chunk (t & 7) of rows (t >> 3) + 64q of the
-    // (128*MH)-row A tile, q < 2*MH: one 128-byte row per 8 lanes, so each
+    // Thread t writes 16-byte chunk (t & 7) of rows (t >> 3) + kRowsPerPass*q of
+    // the (128*MH)-row A tile, q < kCPT: one 128-byte row per 8 lanes, so each
     // quarter-warp store covers all 32 banks once (the swizzle permutes the
     // chunks within a row). The two 128-row halves of an MH=2 tile are
     // contiguous, so row r sits at (r >> 3)*1024 + (r & 7)*128 for any r < 256.
-    constexpr int kCPT = MH * 2;  // chunks per thread per stage
+    constexpr int kRowsPerPass = kHashThreads / 8;          // rows covered by one chunk round
+    constexpr int kCPT = MH * 128 / kRowsPerPass;           // chunks per thread per stage
     using Raw = typename std::conditional<kWBf16, RawBf16, RawF32>::type;
     const int t = threadIdx.x - kFirstHashWarp * 32;
     const int cc = t & 7;
     const int r8 = (t >> 3) & 7;
     const uint32_t soff0 = static_cast<uint32_t>(t >> 6) * 1024u + r8 * 128u + ((cc ^ r8) << 4);
     const int row0 = t >> 3;
-    auto soff = [&](int q) { return soff0 + q * 8192u; };
-    auto rowq = [&](int q) { return row0 + q * 64; };
+    auto soff = [&](int q) { return soff0 + q * (kRowsPerPass * 128u); };
+    auto rowq = [&](int q) { return row0 + q * kRowsPerPass; };
     const float sigma = p.sigma;
     const float shift = -1.5f * sigma;
 
@@ -522,7 +523,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
     // individuals) and the loads for the following group are issued at once,
     // so a whole group of stages covers their latency. The seed of the next
     // stage is likewise loaded one stage ahead.
-    Raw raw[kCPT];
+    Raw raw[kCPT] = {};  // chunks outside the matrix keep zeros (hashed, then discarded)
     Ring rg;
     // Test hook: the stage at which this thread skips its arrive (-1: never).
     int withhold_at = (p.withhold_stage >= 0 && p.withhold_stage < 0x7FFFFFFF && blockIdx.x == 0 &&
@@ -571,34 +572,33 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
           const int s = rg.s;
           const uint64_t seed = seed_next;
           // the individual of the next stage: next in the group, else the group's
-          // first (next k chunk), else the next unit's first
-          if (ii + 1 < un.gcount) {
-            seed_next = static_cast<uint64_t>(__ldg(p.seeds + un.i0 + ii + 1));
-          } else if (kc + 1 < p.k_chunks) {
-            seed_next = static_cast<uint64_t>(__ldg(p.seeds + un.i0));
-          } else if (has_next_unit) {
-            seed_next = static_cast<uint64_t>(__ldg(p.seeds + nun.i0));
-          }
+          // first (next k chunk), else the next unit's first (selected, not branched)
+          const int nidx = (ii + 1 < un.gcount) ? un.i0 + ii + 1
+                           : (kc + 1 < p.k_chunks) ? un.i0
+                           : (has_next_unit ? nun.i0 : un.i0);
+          seed_next = static_cast<uint64_t>(__ldg(p.seeds + nidx));
           if (!(ok = mbar_wait(empty(s), rg.ph ^ 1u, s_abort))) break;
           const uint32_t a0 = stage0 + s * p.stage_bytes;
           const bool last = (ii + 1 == un.gcount);
+          // Every chunk is hashed; chunks outside the matrix (rows >= out or
+          // k >= in, only at ragged edges) are replaced by zeros with selects, so
+          // the loop has no branches.
 #pragma unroll
           for (int q = 0; q < kCPT; ++q) {
-            uint32_t out4[4] = {0u, 0u, 0u, 0u};
-            if (live & (1u << q)) {
-              float wl[8];
-              if constexpr (!kHoist) unpack_shift(raw[q], shift, wl);
-              const float* w8 = kHoist ? wm[kHoist ? q : 0] : wl;
-              uint64_t st = bst[q] + seed;
-              float pv[8];
+            float wl[8];
+            if constexpr (!kHoist) unpack_shift(raw[q], shift, wl);
+            const float* w8 = kHoist ? wm[kHoist ? q : 0] : wl;
+            uint64_t st = bst[q] + seed;
+            float pv[8];
 #pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                pv[e] = fmaf(sigma, __uint_as_float(mix_to_one_plus_u(st)), w8[e]);
-                st += kGamma;
-              }
-#pragma unroll
-              for (int e = 0; e < 4; ++e) out4[e] = pack_bf16x2(pv[2 * e], pv[2 * e + 1]);
+            for (int e = 0; e < 8; ++e) {
+              pv[e] = fmaf(sigma, __uint_as_float(mix_to_one_plus_u(st)), w8[e]);
+              st += kGamma;
             }
+            const bool lv = (live >> q) & 1u;
+            uint32_t out4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) out4[e] = lv ? pack_bf16x2(pv[2 * e], pv[2 * e + 1]) : 0u;
             if constexpr (!kHoist) {
               if (last && has_next) load_chunk(lun, lkc, q, raw[q]);
             }
