@@ -145,13 +145,13 @@ linear_pop_kernel(const LinearArgs a, const PopParams q) {
         // This thread's chunks of W for the pass, and their state terms.
         float wm[CPT][8];
         uint64_t bst[CPT];
-        uint32_t live = 0;
+        float sg[CPT];  // sigma for a chunk inside the pass, 0 for one past it
 #pragma unroll
         for (int cq = 0; cq < CPT; ++cq) {
           const int kk = 8 * (slot + slots * cq);
           const int64_t k = kp0 + kk;
+          sg[cq] = (kk < kpw) ? sigma : 0.f;
           if (row_ok && kk < kpw && k < a.in) {
-            live |= 1u << cq;
             float w[8];
             load8<kWBf16>(a.w, j * a.in + k, a.in - k, q.w_vec != 0, w);
 #pragma unroll
@@ -171,21 +171,24 @@ linear_pop_kernel(const LinearArgs a, const PopParams q) {
           float part[NB];
 #pragma unroll
           for (int r = 0; r < NB; ++r) part[r] = 0.f;
+          // All CPT chunks are hashed, without branches: past the end of the row
+          // (k >= in) X is zero in shared memory, and a chunk past the end of the
+          // pass has W' = 0 (sigma and W both 0) and reads in-bounds X.
+          const float* xi = s_x + ii * NB * kpw;
 #pragma unroll
           for (int cq = 0; cq < CPT; ++cq) {
-            if (live & (1u << cq)) {
-              const int kk = 8 * (slot + slots * cq);
+            {
+              const int kk = min(8 * (slot + slots * cq), kpw - 8);
               uint64_t st = bst[cq] + seed;
               float wp[8];
 #pragma unroll
               for (int e = 0; e < 8; ++e) {
-                wp[e] = fmaf(sigma, __uint_as_float(mix_to_one_plus_u(st)), wm[cq][e]);
+                wp[e] = fmaf(sg[cq], __uint_as_float(mix_to_one_plus_u(st)), wm[cq][e]);
                 st += kGamma;
               }
 #pragma unroll
               for (int r = 0; r < NB; ++r) {
-                const float4* xs =
-                    reinterpret_cast<const float4*>(s_x + (ii * NB + r) * kpw + kk);
+                const float4* xs = reinterpret_cast<const float4*>(xi + r * kpw + kk);
                 const float4 xa = xs[0], xb = xs[1];
                 part[r] = fmaf(xa.x, wp[0], part[r]);
                 part[r] = fmaf(xa.y, wp[1], part[r]);
