@@ -21,10 +21,11 @@
 //   warp 1      TMEM allocator and MMA issuer (one thread);
 //   warps 2..5  epilogue: TMEM -> registers -> + b + sigma*nb -> Y (one per TMEM lane quarter);
 //   warps 6..21 hashing: W'_i = bf16(W + sigma*N_i), 16 bytes (8 k) per store.
-// A work unit is (group of G individuals, N tile, M tile of 128*MH output rows);
-// per k-chunk of 64 the unit's W elements are read once from L2 and perturbed
-// for each of the G individuals, whose accumulators sit side by side in TMEM
-// (G*MH*NT <= 256 columns, so two units can be in flight: double-buffered TMEM).
+// A work unit is (group of G individuals, N tile, M tile of 128*MH output rows;
+// the host uses MH = 1); per k-chunk of 64 the unit's W elements are read once
+// from L2 and perturbed for each of the G individuals, whose accumulators sit
+// side by side in TMEM (G*MH*NT <= 256 columns, so two units can be in flight:
+// double-buffered TMEM).
 // Every barrier wait is bounded; a wait that runs out records a status word,
 // makes the other roles stop, drains what was issued, frees TMEM and returns.
 #include <cuda.h>
@@ -678,7 +679,11 @@ cudaError_t launch_linear_tc_hook(const LinearArgs& a, cudaStream_t stream, long
   std::memset(&p, 0, sizeof(p));
   const int64_t nt = std::min<int64_t>(256, (a.batch + 15) / 16 * 16);
   const bool wbf = a.w_dt == VN_BF16;
-  const int mh = (nt >= 128 && a.out > 128 && wbf) ? 2 : 1;
+  // 128-row units: each unit's accumulators fit in 256 TMEM columns, so TMEM is
+  // double-buffered and the epilogue of one unit overlaps the next unit's MMAs.
+  // (256-row units halve the X traffic per element but then fill all 512
+  // columns; measured slower on the 256-batch workload.)
+  const int mh = 1;
   int g = static_cast<int>(std::max<int64_t>(1, 256 / (mh * nt)));
   g = static_cast<int>(std::min<int64_t>(g, a.pop));
   p.w = a.w; p.b = a.b; p.seeds = a.seeds; p.y = a.y;
@@ -727,10 +732,6 @@ cudaError_t launch_linear_tc_hook(const LinearArgs& a, cudaStream_t stream, long
   const size_t smem = fixed + static_cast<size_t>(stages) * p.stage_bytes;
   const int grid = static_cast<int>(std::min<int64_t>(p.units, dev.sm_count));
   const bool ybf = a.y_dt == VN_BF16;
-  if (mh == 2) {
-    return ybf ? launch_typed<2, true, true>(xmap, p, grid, smem, stream)
-               : launch_typed<2, true, false>(xmap, p, grid, smem, stream);
-  }
   if (wbf) {
     return ybf ? launch_typed<1, true, true>(xmap, p, grid, smem, stream)
                : launch_typed<1, true, false>(xmap, p, grid, smem, stream);
