@@ -48,6 +48,23 @@ noise_dump_kernel(const int64_t* __restrict__ seeds, int64_t n, uint64_t offset,
     const uint64_t seed = static_cast<uint64_t>(__ldg(seeds + i));
     float* row = out + i * n;
     uint64_t gst = index_term(offset + static_cast<uint64_t>(t0)) + seed;  // first element of the group
+    if (vec4 && t0 - threadIdx.x * 4 + kDumpChunk <= n) {
+      // The whole chunk lies inside the row: no per-group checks.
+#pragma unroll
+      for (int g = 0; g < kDumpGroups; ++g) {
+        uint64_t st = gst;
+        float v[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          v[q] = noise_from_bits(mix_to_one_plus_u(st));
+          st += kGamma;
+        }
+        __stcs(reinterpret_cast<float4*>(row + t0 + g * kDumpStride),
+               make_float4(v[0], v[1], v[2], v[3]));
+        gst += kDumpStep;
+      }
+      continue;
+    }
     // number of this thread's groups that start inside the row
     const int64_t left = n - t0;
     const int full = left <= 0 ? 0 : static_cast<int>((left + kDumpStride - 1) / kDumpStride < kDumpGroups ? (left + kDumpStride - 1) / kDumpStride : kDumpGroups);
