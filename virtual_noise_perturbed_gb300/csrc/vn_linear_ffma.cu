@@ -43,7 +43,7 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr int kMaxCPT = 4;
+constexpr int kMaxCPT = 2;  // more chunks per thread cost more registers than they save
 constexpr size_t kSmemBudget = 48 * 1024;
 
 template <bool kBf16>
@@ -299,7 +299,6 @@ cudaError_t launch_nb(const LinearArgs& a, cudaStream_t stream, int sm_count) {
   const int64_t chunks = (a.in + 7) / 8;
   const int64_t cpt = std::max<int64_t>(1, (chunks + slots - 1) / slots);
   if (cpt <= 1) return launch_cfg<NB, 1, kX, kW>(a, stream, sm_count, r_log2);
-  if (cpt <= 2) return launch_cfg<NB, 2, kX, kW>(a, stream, sm_count, r_log2);
   return launch_cfg<NB, kMaxCPT, kX, kW>(a, stream, sm_count, r_log2);
 }
 
