@@ -202,7 +202,8 @@ def test_workload4_full_size_windows():
     assert torch.allclose(part, gw[r0:r1], rtol=0, atol=1e-5 * float(gw.abs().max()))
 
 
-@pytest.mark.parametrize("pop,n", [(1, 1), (5, 1000), (300, 4099), (16, 1 << 16)])
+@pytest.mark.parametrize("pop,n", [(1, 1), (5, 1000), (300, 4099), (16, 1 << 16), (2, 300001),
+                                   (8, 1 << 20)])
 def test_reduce_metric_matches_oracle(pop, n):
     g = torch.Generator().manual_seed(n)
     c = torch.randn(n, generator=g)

@@ -10,12 +10,15 @@
 // works on groups of 4 consecutive elements so that the state of the next
 // element is the previous one plus GAMMA (a two-operation 64-bit add) and the
 // dump writes one 16-byte store per group.
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
 
 #include "vn_hash.cuh"
 #include "vn_internal.h"
+
+namespace cg = cooperative_groups;
 
 namespace vn {
 namespace {
@@ -94,32 +97,44 @@ noise_dump_kernel(const int64_t* __restrict__ seeds, int64_t n, uint64_t offset,
 
 constexpr int kMetricThreads = 256;
 
-// One CTA per individual (grid-stride over individuals). Each thread sums
-// |center[k] + sigma*n| over k = 4*tid + 1024*g + q; the block then adds the
-// partial sums in a fixed order.
+// Individual i is handled by the S CTAs of a cluster (S = gridDim.y, 1 when the
+// population alone fills the GPU); CTA rank s sums |center[k] + sigma*n| over its
+// slice of k, thread t over k = k0 + 4t + 1024g + q. Partial sums are added in a
+// fixed order: lanes by shuffle, warps in order, then the S CTAs' sums in rank
+// order through distributed shared memory. Grid-stride over individuals.
+template <bool kCluster>
 __global__ void __launch_bounds__(kMetricThreads)
 reduce_metric_kernel(const float* __restrict__ center, const int64_t* __restrict__ seeds,
                      int64_t pop, int64_t n, float sigma, float inv_n, uint64_t offset,
                      float* __restrict__ fitness, int vec4) {
   __shared__ float s_warp[kMetricThreads / 32];
+  __shared__ float s_cta;
+  const int slices = gridDim.y;
+  // slice bounds, multiples of 4 so that 16-byte loads stay aligned
+  const int64_t per = ((n + slices - 1) / slices + 3) / 4 * 4;
+  const int64_t k_begin = min(n, static_cast<int64_t>(blockIdx.y) * per);
+  const int64_t k_end = min(n, k_begin + per);
   for (int64_t i = blockIdx.x; i < pop; i += gridDim.x) {
     const uint64_t seed = static_cast<uint64_t>(__ldg(seeds + i));
     float acc = 0.f;
-    for (int64_t k = static_cast<int64_t>(threadIdx.x) * 4; k < n; k += kMetricThreads * 4) {
+    for (int64_t k = k_begin + static_cast<int64_t>(threadIdx.x) * 4; k < k_end;
+         k += kMetricThreads * 4) {
       uint64_t st = index_term(offset + static_cast<uint64_t>(k)) + seed;
-      float c[4];
-      if (vec4 && k + 4 <= n) {
+      if (vec4 && k + 4 <= k_end) {  // the common case: four in-range elements, no checks
         const float4 c4 = __ldg(reinterpret_cast<const float4*>(center + k));
-        c[0] = c4.x; c[1] = c4.y; c[2] = c4.z; c[3] = c4.w;
+        const float c[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          acc += fabsf(fmaf(sigma, noise_from_bits(mix_to_one_plus_u(st)), c[q]));
+          st += kGamma;
+        }
       } else {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) c[q] = (k + q < n) ? __ldg(center + k + q) : 0.f;
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float v = fabsf(fmaf(sigma, noise_from_bits(mix_to_one_plus_u(st)), c[q]));
-        if (k + q < n) acc += v;
-        st += kGamma;
+        for (int q = 0; q < 4; ++q) {
+          if (k + q < k_end)
+            acc += fabsf(fmaf(sigma, noise_from_bits(mix_to_one_plus_u(st)), __ldg(center + k + q)));
+          st += kGamma;
+        }
       }
     }
 #pragma unroll
@@ -130,9 +145,21 @@ reduce_metric_kernel(const float* __restrict__ center, const int64_t* __restrict
       float total = 0.f;
 #pragma unroll
       for (int w = 0; w < kMetricThreads / 32; ++w) total += s_warp[w];
-      fitness[i] = total * inv_n;
+      s_cta = total;
     }
-    __syncthreads();
+    if constexpr (!kCluster) {
+      if (threadIdx.x == 0) fitness[i] = s_cta * inv_n;
+      __syncthreads();
+    } else {
+      cg::cluster_group cluster = cg::this_cluster();
+      cluster.sync();
+      if (cluster.block_rank() == 0 && threadIdx.x == 0) {
+        float total = 0.f;
+        for (int q = 0; q < slices; ++q) total += *cluster.map_shared_rank(&s_cta, q);
+        fitness[i] = total * inv_n;
+      }
+      cluster.sync();  // no CTA may leave (or reuse s_cta) while rank 0 reads it
+    }
   }
 }
 
@@ -163,10 +190,32 @@ cudaError_t launch_reduce_metric(const float* center, const int64_t* seeds, int6
   cudaError_t err = device_info(&dev);
   if (err != cudaSuccess) return err;
   const int vec4 = (reinterpret_cast<uintptr_t>(center) % 16 == 0);
-  const int64_t grid = std::min<int64_t>(pop, static_cast<int64_t>(dev.sm_count) * 8);
-  reduce_metric_kernel<<<static_cast<unsigned>(grid), kMetricThreads, 0, stream>>>(
-      center, seeds, pop, n, sigma, inv_n, offset, fitness, vec4);
-  return cudaGetLastError();
+  const int64_t resident = static_cast<int64_t>(dev.sm_count) * 8;
+  // Split each individual over a cluster while the population alone leaves the
+  // GPU mostly idle and each slice keeps at least 16 Ki elements.
+  int slices = 1;
+  while (slices < 8 && pop * slices < resident && n >= static_cast<int64_t>(slices) * 2 * 16384)
+    slices *= 2;
+  if (slices == 1) {
+    const int64_t grid = std::min<int64_t>(pop, resident);
+    reduce_metric_kernel<false><<<static_cast<unsigned>(grid), kMetricThreads, 0, stream>>>(
+        center, seeds, pop, n, sigma, inv_n, offset, fitness, vec4);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(std::min<int64_t>(pop, std::max<int64_t>(1, resident / slices))),
+                     static_cast<unsigned>(slices), 1);
+  cfg.blockDim = dim3(kMetricThreads, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = static_cast<unsigned>(slices);
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, reduce_metric_kernel<true>, center, seeds, pop, n, sigma, inv_n,
+                            offset, fitness, vec4);
 }
 
 }  // namespace vn
