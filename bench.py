@@ -47,13 +47,17 @@ sys.path.insert(0, ROOT)
 METRIC = "virtual-noise elem/s"
 UNIT = "noise elements/s"
 
-# 32-bit operations per noise element in the definition, on 32-bit halves:
-# state add 2, xor-shift 30: 4, multiply by GAMMA: 3, xor-shift 27: 4,
-# multiply by GAMMA: 3, final xor-shift 31 + top-23-bit extraction: 3  (19 integer)
-# + the float conversion (1 FADD) and the one FMA that consumes the noise (2 fp).
+# Cost of one noise element in the definition, on 32-bit halves (the GPU has no
+# 64-bit integer unit). Integer ALU pipe (LOP3 / SHF / IADD): right shifts 6 (two
+# funnel shifts and two plain shifts for the xor-shifts 30 and 27, two for the
+# final xor-shift 31 with the top-23-bit extraction), three-input logic ops 5,
+# state add 2  -> 13. IMAD pipe: the two products by GAMMA, 3 each -> 6. Plus the
+# float conversion and the FMA that consumes the noise -> 21 operations in all.
+ALU_OPS_PER_ELEMENT = 13
 OPS_PER_ELEMENT = 21
 SMS_NOMINAL = 152
 SM_CLOCK_MAX_HZ = 2.07e9
+ALU_LANES_PER_SM = 64             # integer ALU pipe: 16 lanes per scheduler, 4 schedulers
 ISSUE_LANES_PER_SM = 128          # 4 schedulers x 32 lanes, one instruction per clock each
 L2_FLUSH_BYTES = 256 << 20
 
@@ -67,7 +71,8 @@ def peaks():
         p = {"hbm_gbs": float(m["hbm_gbs"]), "bf16_tflops": float(m["bf16_tflops"]),
              "bf16_tflops_sustained": float(m.get("bf16_tflops_sustained", m["bf16_tflops"])),
              "source": "measured"}
-    p["alu_ops"] = SMS_NOMINAL * ISSUE_LANES_PER_SM * SM_CLOCK_MAX_HZ
+    p["alu_ops"] = SMS_NOMINAL * ALU_LANES_PER_SM * SM_CLOCK_MAX_HZ
+    p["issue_ops"] = SMS_NOMINAL * ISSUE_LANES_PER_SM * SM_CLOCK_MAX_HZ
     return p
 
 
@@ -449,7 +454,7 @@ def main(argv=None) -> int:
     dom = max(per_kernel, key=lambda n: per_kernel[n]["ms"])
     r = per_kernel[dom]
     secs = r["ms"] * 1e-3
-    cands = {"alu": (r["elements"] * OPS_PER_ELEMENT / secs / 1e12, pk["alu_ops"] / 1e12, "Tops/s")}
+    cands = {"alu": (r["elements"] * ALU_OPS_PER_ELEMENT / secs / 1e12, pk["alu_ops"] / 1e12, "Tops/s")}
     if r["hbm_bytes"]:
         cands["hbm"] = (r["hbm_bytes"] / secs / 1e9, pk["hbm_gbs"], "GB/s")
     if r["flops"]:
@@ -458,9 +463,12 @@ def main(argv=None) -> int:
     ach, peak, unit = cands[bound]
     roofline = {"bound": bound, "kernel": dom, "achieved": ach, "peak": peak, "unit": unit,
                 "frac": ach / peak, "traffic": traffic_for(dom),
-                "peak_source": ("derived: 152 SMs x 128 issue lanes x 2.07 GHz, 32-bit ops"
+                "peak_source": ("derived: 152 SMs x 64 integer-ALU lanes x 2.07 GHz"
                                 if bound == "alu" else pk["source"]),
-                "ops_per_element": OPS_PER_ELEMENT if bound == "alu" else None,
+                "ops_per_element": ALU_OPS_PER_ELEMENT if bound == "alu" else None,
+                # the stricter bound: every one of the 21 operations through the issue
+                # port (152 SMs x 128 lanes x 2.07 GHz)
+                "issue_frac": r["elements"] * OPS_PER_ELEMENT / secs / pk["issue_ops"],
                 "launches": r["launches"], "avg_launch_us": 1e3 * r["ms"] / r["launches"]}
     kernels = {n: {"launches": v["launches"], "share": v["ms"] / sum(x["ms"] for x in per_kernel.values()),
                    "avg_us": 1e3 * v["ms"] / v["launches"],
