@@ -516,6 +516,8 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
           r.a = __ldg(src);
           r.b = __ldg(src + 1);
         }
+      } else {
+        r = Raw{};
       }
     };
 
@@ -524,7 +526,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
     // individuals) and the loads for the following group are issued at once,
     // so a whole group of stages covers their latency. The seed of the next
     // stage is likewise loaded one stage ahead.
-    Raw raw[kCPT] = {};  // chunks outside the matrix keep zeros (hashed, then discarded)
+    Raw raw[kCPT] = {};
     Ring rg;
     // Test hook: the stage at which this thread skips its arrive (-1: never).
     int withhold_at = (p.withhold_stage >= 0 && p.withhold_stage < 0x7FFFFFFF && blockIdx.x == 0 &&
@@ -544,30 +546,28 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
       const Unit nun = has_next_unit ? decode(p, u + gridDim.x, MH) : un;
       for (int kc = 0; ok && kc < p.k_chunks; ++kc) {
         const int64_t k = static_cast<int64_t>(kc) * kKC + cc * 8;
-        // kHoist (G may exceed 1): W - 1.5*sigma is formed once per group in
-        // wm and the next group's loads go out at once. Otherwise (MH = 2,
-        // one individual per unit, tight registers) W is unpacked per use and
-        // chunk q of the next group is loaded right after chunk q's use.
-        constexpr bool kHoist = (MH == 1);
-        float wm[kHoist ? kCPT : 1][8];
+        // W - 1.5*sigma of this stage group's chunks, shared by its G individuals,
+        // and each chunk's state term. A chunk outside the matrix (row >= out or
+        // k >= in, only at ragged edges) holds W = 0, so its values are finite:
+        // its X columns are TMA's zero fill (k >= in) or its output rows are
+        // never stored (row >= out), and no masking is needed below.
+        float wm[kCPT][8];
         uint64_t bst[kCPT];  // (offset + j*in + k + 1) * GAMMA of each chunk's first element
-        uint32_t live = 0;   // bit q: chunk q holds real weights (row < out, k < in)
 #pragma unroll
         for (int q = 0; q < kCPT; ++q) {
           const int64_t j = un.m0 + rowq(q);
-          if ((j < p.out) && (k < p.in)) live |= 1u << q;
-          if constexpr (kHoist) unpack_shift(raw[q], shift, wm[q]);
+          unpack_shift(raw[q], shift, wm[q]);
           bst[q] = index_term(p.offset + static_cast<uint64_t>(j) * static_cast<uint64_t>(p.in) +
                               static_cast<uint64_t>(k));
         }
-        const bool has_next = (kc + 1 < p.k_chunks) || has_next_unit;
-        const Unit& lun = (kc + 1 < p.k_chunks) ? un : nun;
-        const int lkc = (kc + 1 < p.k_chunks) ? kc + 1 : 0;
-        if constexpr (kHoist) {
-          if (has_next) {
+        // Prefetch the next stage group's W chunks (this unit's next k chunk, or
+        // the next unit's first).
+        if (kc + 1 < p.k_chunks) {
 #pragma unroll
-            for (int q = 0; q < kCPT; ++q) load_chunk(lun, lkc, q, raw[q]);
-          }
+          for (int q = 0; q < kCPT; ++q) load_chunk(un, kc + 1, q, raw[q]);
+        } else if (has_next_unit) {
+#pragma unroll
+          for (int q = 0; q < kCPT; ++q) load_chunk(nun, 0, q, raw[q]);
         }
         for (int ii = 0; ii < un.gcount; ++ii, rg.next(S)) {
           const int s = rg.s;
@@ -580,30 +580,17 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
           seed_next = static_cast<uint64_t>(__ldg(p.seeds + nidx));
           if (!(ok = mbar_wait(empty(s), rg.ph ^ 1u, s_abort))) break;
           const uint32_t a0 = stage0 + s * p.stage_bytes;
-          const bool last = (ii + 1 == un.gcount);
-          // Every chunk is hashed; chunks outside the matrix (rows >= out or
-          // k >= in, only at ragged edges) are replaced by zeros with selects, so
-          // the loop has no branches.
 #pragma unroll
           for (int q = 0; q < kCPT; ++q) {
-            float wl[8];
-            if constexpr (!kHoist) unpack_shift(raw[q], shift, wl);
-            const float* w8 = kHoist ? wm[kHoist ? q : 0] : wl;
             uint64_t st = bst[q] + seed;
             float pv[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-              pv[e] = fmaf(sigma, __uint_as_float(mix_to_one_plus_u(st)), w8[e]);
+              pv[e] = fmaf(sigma, __uint_as_float(mix_to_one_plus_u(st)), wm[q][e]);
               st += kGamma;
             }
-            const bool lv = (live >> q) & 1u;
-            uint32_t out4[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) out4[e] = lv ? pack_bf16x2(pv[2 * e], pv[2 * e + 1]) : 0u;
-            if constexpr (!kHoist) {
-              if (last && has_next) load_chunk(lun, lkc, q, raw[q]);
-            }
-            st_shared_v4(a0 + soff(q), out4[0], out4[1], out4[2], out4[3]);
+            st_shared_v4(a0 + soff(q), pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]),
+                         pack_bf16x2(pv[4], pv[5]), pack_bf16x2(pv[6], pv[7]));
           }
           fence_proxy_async_smem();
           if (withhold_at != 0) mbar_arrive(full_a(s));
