@@ -169,7 +169,8 @@ vn_status vn_device_status(void* stream);
  * tensor memory and return; vn_device_status() then reports VN_ERR_TIMEOUT and
  * the context stays usable. y is left partly unwritten. No GPU fault, trap or
  * hang is involved. If the CTA has fewer stages than withhold_stage, nothing is
- * withheld and the call completes normally. */
+ * withheld and the call completes normally. The hook exists for bf16 W and Y
+ * only (VN_ERR_DTYPE otherwise). */
 vn_status vn_testhook_linear_tc_withhold(const void* x, vn_dtype x_dt, int x_shared,
                                          const void* w, vn_dtype w_dt,
                                          const void* b, vn_dtype b_dt,

@@ -228,6 +228,7 @@ vn_status vn_testhook_linear_tc_withhold(const void* x, vn_dtype x_dt, int x_sha
                                          void* y, vn_dtype y_dt, int64_t withhold_stage,
                                          double timeout_ms, void* stream) {
   if (!(timeout_ms > 0.0) || !(timeout_ms <= 60000.0) || withhold_stage < 0) return VN_ERR_VALUE;
+  if (w_dt != VN_BF16 || y_dt != VN_BF16) return VN_ERR_DTYPE;  // the hook's one instance
   // Validate exactly as a forced tensor-core call would (this launches nothing:
   // pop = 0 makes the output empty).
   vn_status st = vn_perturbed_linear_ex(x, x_dt, x_shared, w, w_dt, b, b_dt, seeds, 0, batch, in,

@@ -10,20 +10,22 @@
 //
 // Per individual the product is D = W'_i X_i^T with D[j, n] = Y_i[n, j]:
 //   A = W'_i tile, 128 output rows x 64 k (bf16, K-major), written into shared
-//       memory by "hashing" warps in the 128-byte-swizzled canonical layout;
+//       memory by "hashing" warps in the 128-byte-swizzled canonical layout
+//       from the W tile (fp32 or bf16, 128 rows x 64 k), which TMA stages once
+//       per (unit, k chunk) into a two-slot ring shared by all hashing warps;
 //   B = X_i tile, NT batch rows x 64 k (bf16, K-major), loaded by TMA with the
 //       same 128-byte swizzle;
 //   D = fp32 accumulator in TMEM, 128 lanes (output rows) x NT columns (batch).
 // The contraction is tiny next to the hash work (one 64-bit splitmix64 hash per
 // weight element per individual, about 20 integer operations), so the kernel is
 // built around keeping the integer pipes busy:
-//   warp 0      TMA producer for X tiles (one thread);
+//   warp 0      TMA producer for W and X tiles (one thread);
 //   warp 1      TMEM allocator and MMA issuer (one thread);
 //   warps 2..5  epilogue: TMEM -> registers -> + b + sigma*nb -> Y (one per TMEM lane quarter);
 //   warps 6..21 hashing: W'_i = bf16(W + sigma*N_i), 16 bytes (8 k) per store.
 // A work unit is (group of G individuals, N tile, M tile of 128*MH output rows;
-// the host uses MH = 1); per k-chunk of 64 the unit's W elements are read once
-// from L2 and perturbed for each of the G individuals, whose accumulators sit
+// the host uses MH = 1); per k-chunk of 64 the unit's W tile is staged once and
+// perturbed for each of the G individuals, whose accumulators sit
 // side by side in TMEM (G*MH*NT <= 256 columns, so two units can be in flight:
 // double-buffered TMEM).
 // Every barrier wait is bounded; a wait that runs out records a status word,
@@ -58,14 +60,13 @@ constexpr uint32_t kHalfBytes = 128 * 128;                    // 128 rows x 128 
 constexpr int kTmemCols = 512;
 constexpr unsigned long long kTimeoutNs = 4000000000ull;      // default limit of one wait: 4 s
 // Back-off between polls of roles that run stages ahead of their consumers.
-constexpr uint32_t kProducerSleepNs = 256;
-constexpr uint32_t kMmaSleepNs = 64;
+constexpr uint32_t kProducerSleepNs = 1024;
+constexpr uint32_t kMmaSleepNs = 256;
 constexpr int kEpilogueFirstThread = 2 * 32;  // warps 2..5
 constexpr int kEpilogueThreads = 4 * 32;
 constexpr int kEpilogueBarrier = 1;           // named barrier id (0 is __syncthreads)
 
 struct TcParams {
-  const void* w;
   const void* b;
   const int64_t* seeds;
   void* y;
@@ -76,6 +77,7 @@ struct TcParams {
   int b_bf16, act;
   int nt, g, nbuf, stages, k_chunks, x_shared;
   uint32_t stage_bytes, a_bytes, idesc;
+  uint32_t w_bytes;  // one W tile in shared memory: 128 rows x 64 k of W's dtype
   unsigned long long timeout_ns;  // limit of every barrier wait
   long long withhold_stage;       // test hook: >= 0 makes one thread skip that stage's arrive
 };
@@ -181,6 +183,14 @@ __device__ __forceinline__ void fence_barrier_init() {
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int c0, int c1, int c2) {
   asm volatile(
@@ -244,6 +254,15 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row
 // groups 1024 bytes apart (stride byte offset), descriptor version 1.
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
@@ -300,15 +319,21 @@ __device__ __forceinline__ Unit decode(const TcParams& p, int64_t u, int mh) {
 }
 
 // ---------------------------------------------------------------- the kernel
-template <int MH, bool kWBf16, bool kYBf16>
+// kHook: the test-hook instance (one hashing thread may withhold an arrive);
+// the ordinary instances carry no trace of it.
+template <int MH, bool kWBf16, bool kYBf16, bool kHook>
 __global__ void __launch_bounds__(kThreads, 1)
-linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
+linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
+                 const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const int S = p.stages;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(S) * p.stage_bytes);
-  // barriers: full_a[S], full_x[S], empty[S], tmem_full[2], tmem_empty[2], drain
+  // layout: S stages (A tile, X tile), 2 W slots, barriers
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(S) * p.stage_bytes +
+                                               2 * static_cast<size_t>(p.w_bytes));
+  // barriers: full_a[S], full_x[S], empty[S], tmem_full[2], tmem_empty[2], drain,
+  // full_w[2], empty_w[2]
   const uint32_t bar0 = smem_u32(bars);
   auto full_a = [&](int s) { return bar0 + 8u * s; };
   auto full_x = [&](int s) { return bar0 + 8u * (S + s); };
@@ -316,9 +341,12 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
   auto tmem_full = [&](int b) { return bar0 + 8u * (3 * S + b); };
   auto tmem_empty = [&](int b) { return bar0 + 8u * (3 * S + 2 + b); };
   const uint32_t drain = bar0 + 8u * (3 * S + 4);
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 3 * S + 5);
-  volatile WaitCtl* s_abort = reinterpret_cast<volatile WaitCtl*>(bars + 3 * S + 6);
+  auto full_w = [&](int b) { return bar0 + 8u * (3 * S + 5 + b); };
+  auto empty_w = [&](int b) { return bar0 + 8u * (3 * S + 7 + b); };
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + 3 * S + 9);
+  volatile WaitCtl* s_abort = reinterpret_cast<volatile WaitCtl*>(bars + 3 * S + 10);
   const uint32_t stage0 = smem_u32(smem);
+  const uint32_t wslot0 = stage0 + S * p.stage_bytes;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -334,6 +362,10 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
       mbar_init(tmem_empty(b), 128);
     }
     mbar_init(drain, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(full_w(b), 1);
+      mbar_init(empty_w(b), kHashThreads);
+    }
     s_abort->abort = 0;
     s_abort->timeout_ns = p.timeout_ns;
     fence_barrier_init();
@@ -351,13 +383,19 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      uint32_t it = 0;
-      Ring rg;
+      uint32_t it = 0, wit = 0;
+      Ring rg, wr;
       bool ok = true;
       const uint32_t x_bytes = static_cast<uint32_t>(p.nt) * 128u;
       for (int64_t u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
         const Unit un = decode(p, u, MH);
         for (int kc = 0; ok && kc < p.k_chunks; ++kc) {
+          // The group's W tile (rows >= out and k >= in arrive as zeros).
+          if (!(ok = mbar_wait(empty_w(wr.s), wr.ph ^ 1u, s_abort, kProducerSleepNs))) break;
+          mbar_expect_tx(full_w(wr.s), p.w_bytes);
+          tma_load_2d(wslot0 + wr.s * p.w_bytes, &wmap, full_w(wr.s), kc * kKC, un.m0);
+          ++wit;
+          wr.next(2);
           for (int ii = 0; ii < un.gcount; ++ii, ++it, rg.next(S)) {
             const int s = rg.s;
             if (!(ok = mbar_wait(empty(s), rg.ph ^ 1u, s_abort, kProducerSleepNs))) break;
@@ -375,6 +413,13 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
           const uint32_t j = it - 1 - k;
           const uint64_t t0 = global_ns();
           while (!mbar_try_wait(full_x(static_cast<int>(j % S)), (j / S) & 1u) &&
+                 global_ns() - t0 < p.timeout_ns) {
+          }
+        }
+        for (uint32_t k = 0; k < 2u && k < wit; ++k) {
+          const uint32_t j = wit - 1 - k;
+          const uint64_t t0 = global_ns();
+          while (!mbar_try_wait(full_w(static_cast<int>(j & 1u)), (j >> 1) & 1u) &&
                  global_ns() - t0 < p.timeout_ns) {
           }
         }
@@ -502,100 +547,107 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const TcParams p) {
     const float sigma = p.sigma;
     const float shift = -1.5f * sigma;
 
-    // W for chunk q of the stage group (u, kc): 8 consecutive k of one row.
-    auto load_chunk = [&](const Unit& un, int kc, int q, Raw& r) {
-      const int64_t j = un.m0 + rowq(q);
-      const int64_t k = static_cast<int64_t>(kc) * kKC + cc * 8;
-      if (j < p.out && k < p.in) {
-        if constexpr (kWBf16) {
-          r.a = __ldg(reinterpret_cast<const uint4*>(
-              reinterpret_cast<const __nv_bfloat16*>(p.w) + j * p.in + k));
-        } else {
-          const float4* src =
-              reinterpret_cast<const float4*>(reinterpret_cast<const float*>(p.w) + j * p.in + k);
-          r.a = __ldg(src);
-          r.b = __ldg(src + 1);
-        }
+    // This thread's chunk q inside a staged W tile (rows of 64 k, 256 bytes in
+    // fp32, 128 in bf16). In fp32 the two 16-byte halves are read in an order
+    // that depends on cc, so the 8 threads of a row hit distinct banks.
+    constexpr uint32_t kWRow = kWBf16 ? 128u : 256u;
+    const uint32_t wfirst = kWBf16 ? 0u : ((cc >> 2) & 1u) * 16u;
+    auto woff = [&](int q) { return static_cast<uint32_t>(rowq(q)) * kWRow + cc * (kWRow / 8); };
+    auto load_w = [&](uint32_t addr, Raw& r) {
+      if constexpr (kWBf16) {
+        r.a = ld_shared_v4(addr);
       } else {
-        r = Raw{};
+        const uint4 h0 = ld_shared_v4(addr + wfirst);
+        const uint4 h1 = ld_shared_v4(addr + (wfirst ^ 16u));
+        const uint4 lo = wfirst ? h1 : h0;
+        const uint4 hi = wfirst ? h0 : h1;
+        r.a = make_float4(__uint_as_float(lo.x), __uint_as_float(lo.y), __uint_as_float(lo.z),
+                          __uint_as_float(lo.w));
+        r.b = make_float4(__uint_as_float(hi.x), __uint_as_float(hi.y), __uint_as_float(hi.z),
+                          __uint_as_float(hi.w));
       }
     };
+    // State term step from one k chunk to the next: 64 * GAMMA mod 2^64.
+    constexpr uint64_t kChunkStep = static_cast<uint64_t>(kKC) * kGamma;
 
-    // raw holds the W chunks of the next stage group: at the start of a group
-    // they are turned into W - 1.5*sigma (fp32, shared by the group's G
-    // individuals) and the loads for the following group are issued at once,
-    // so a whole group of stages covers their latency. The seed of the next
-    // stage is likewise loaded one stage ahead.
-    Raw raw[kCPT] = {};
-    Ring rg;
+    Ring rg, wr;
     // Test hook: the stage at which this thread skips its arrive (-1: never).
-    int withhold_at = (p.withhold_stage >= 0 && p.withhold_stage < 0x7FFFFFFF && blockIdx.x == 0 &&
-                       t == 0) ? static_cast<int>(p.withhold_stage) : -1;
+    int withhold_at = (kHook && p.withhold_stage >= 0 && p.withhold_stage < 0x7FFFFFFF &&
+                       blockIdx.x == 0 && t == 0) ? static_cast<int>(p.withhold_stage) : -1;
     bool ok = true;
     int64_t u = blockIdx.x;
-    uint64_t seed_next = 0;
-    if (u < p.units) {
-      const Unit first = decode(p, u, MH);
-#pragma unroll
-      for (int q = 0; q < kCPT; ++q) load_chunk(first, 0, q, raw[q]);
-      seed_next = static_cast<uint64_t>(__ldg(p.seeds + first.i0));
-    }
+    // The seed of the next stage is loaded one stage ahead.
+    uint64_t seed_next = (u < p.units) ? static_cast<uint64_t>(__ldg(p.seeds + decode(p, u, MH).i0))
+                                       : 0ull;
     for (; ok && u < p.units; u += gridDim.x) {
       const Unit un = decode(p, u, MH);
       const bool has_next_unit = u + gridDim.x < p.units;
-      const Unit nun = has_next_unit ? decode(p, u + gridDim.x, MH) : un;
+      const int next_i0 = has_next_unit ? decode(p, u + gridDim.x, MH).i0 : un.i0;
+      // (offset + j*in + k + 1) * GAMMA of each chunk's first element, k chunk 0;
+      // advanced by kChunkStep per k chunk.
+      uint64_t bst[kCPT];
+#pragma unroll
+      for (int q = 0; q < kCPT; ++q) {
+        bst[q] = index_term(p.offset +
+                            static_cast<uint64_t>(un.m0 + rowq(q)) * static_cast<uint64_t>(p.in) +
+                            static_cast<uint64_t>(cc * 8));
+      }
       for (int kc = 0; ok && kc < p.k_chunks; ++kc) {
-        const int64_t k = static_cast<int64_t>(kc) * kKC + cc * 8;
-        // W - 1.5*sigma of this stage group's chunks, shared by its G individuals,
-        // and each chunk's state term. A chunk outside the matrix (row >= out or
-        // k >= in, only at ragged edges) holds W = 0, so its values are finite:
-        // its X columns are TMA's zero fill (k >= in) or its output rows are
+        // W - 1.5*sigma of this stage group's chunks, shared by its G
+        // individuals. Chunks outside the matrix (row >= out or k >= in, only
+        // at ragged edges) are TMA's zero fill, so their values are finite:
+        // their X columns are zero fill too (k >= in) or their output rows are
         // never stored (row >= out), and no masking is needed below.
+        if (!(ok = mbar_wait(full_w(wr.s), wr.ph, s_abort))) break;
         float wm[kCPT][8];
-        uint64_t bst[kCPT];  // (offset + j*in + k + 1) * GAMMA of each chunk's first element
+        {
+          const uint32_t wb = wslot0 + wr.s * p.w_bytes;
 #pragma unroll
-        for (int q = 0; q < kCPT; ++q) {
-          const int64_t j = un.m0 + rowq(q);
-          unpack_shift(raw[q], shift, wm[q]);
-          bst[q] = index_term(p.offset + static_cast<uint64_t>(j) * static_cast<uint64_t>(p.in) +
-                              static_cast<uint64_t>(k));
+          for (int q = 0; q < kCPT; ++q) {
+            Raw r;
+            load_w(wb + woff(q), r);
+            unpack_shift(r, shift, wm[q]);
+          }
         }
-        // Prefetch the next stage group's W chunks (this unit's next k chunk, or
-        // the next unit's first).
-        if (kc + 1 < p.k_chunks) {
-#pragma unroll
-          for (int q = 0; q < kCPT; ++q) load_chunk(un, kc + 1, q, raw[q]);
-        } else if (has_next_unit) {
-#pragma unroll
-          for (int q = 0; q < kCPT; ++q) load_chunk(nun, 0, q, raw[q]);
-        }
+        // The slot's next tile is written by TMA (the async proxy): order this
+        // thread's generic-proxy reads of it before that write. Without the
+        // fence a late warp's reads could return the next tile's values.
+        fence_proxy_async_smem();
+        mbar_arrive(empty_w(wr.s));
+        wr.next(2);
         for (int ii = 0; ii < un.gcount; ++ii, rg.next(S)) {
           const int s = rg.s;
           const uint64_t seed = seed_next;
           // the individual of the next stage: next in the group, else the group's
           // first (next k chunk), else the next unit's first (selected, not branched)
           const int nidx = (ii + 1 < un.gcount) ? un.i0 + ii + 1
-                           : (kc + 1 < p.k_chunks) ? un.i0
-                           : (has_next_unit ? nun.i0 : un.i0);
+                           : (kc + 1 < p.k_chunks) ? un.i0 : next_i0;
           seed_next = static_cast<uint64_t>(__ldg(p.seeds + nidx));
           if (!(ok = mbar_wait(empty(s), rg.ph ^ 1u, s_abort))) break;
           const uint32_t a0 = stage0 + s * p.stage_bytes;
 #pragma unroll
           for (int q = 0; q < kCPT; ++q) {
-            uint64_t st = bst[q] + seed;
+            const uint64_t st0 = bst[q] + seed;
+            uint32_t slo = static_cast<uint32_t>(st0), shi = static_cast<uint32_t>(st0 >> 32);
             float pv[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-              pv[e] = fmaf(sigma, __uint_as_float(mix_to_one_plus_u(st)), wm[q][e]);
-              st += kGamma;
+              pv[e] = fmaf(sigma, __uint_as_float(mix_to_one_plus_u(slo, shi)), wm[q][e]);
+              add64(slo, shi, kGammaLo, kGammaHi);
             }
             st_shared_v4(a0 + soff(q), pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]),
                          pack_bf16x2(pv[4], pv[5]), pack_bf16x2(pv[6], pv[7]));
           }
           fence_proxy_async_smem();
-          if (withhold_at != 0) mbar_arrive(full_a(s));
-          if (withhold_at >= 0) --withhold_at;
+          if constexpr (kHook) {
+            if (withhold_at != 0) mbar_arrive(full_a(s));
+            if (withhold_at >= 0) --withhold_at;
+          } else {
+            mbar_arrive(full_a(s));
+          }
         }
+#pragma unroll
+        for (int q = 0; q < kCPT; ++q) bst[q] += kChunkStep;
       }
     }
   }
@@ -623,10 +675,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-template <int MH, bool kW, bool kY>
-cudaError_t launch_typed(const CUtensorMap& xmap, const TcParams& p, int grid, size_t smem,
-                         cudaStream_t stream) {
-  auto fn = linear_tc_kernel<MH, kW, kY>;
+template <int MH, bool kW, bool kY, bool kHook>
+cudaError_t launch_typed(const CUtensorMap& xmap, const CUtensorMap& wmap, const TcParams& p,
+                         int grid, size_t smem, cudaStream_t stream) {
+  auto fn = linear_tc_kernel<MH, kW, kY, kHook>;
   static size_t configured = 0;
   if (configured < smem) {
     cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -634,7 +686,7 @@ cudaError_t launch_typed(const CUtensorMap& xmap, const TcParams& p, int grid, s
     if (err != cudaSuccess) return err;
     configured = smem;
   }
-  fn<<<grid, kThreads, smem, stream>>>(xmap, p);
+  fn<<<grid, kThreads, smem, stream>>>(xmap, wmap, p);
   return cudaGetLastError();
 }
 
@@ -673,7 +725,7 @@ cudaError_t launch_linear_tc_hook(const LinearArgs& a, cudaStream_t stream, long
   const int mh = 1;
   int g = static_cast<int>(std::max<int64_t>(1, 256 / (mh * nt)));
   g = static_cast<int>(std::min<int64_t>(g, a.pop));
-  p.w = a.w; p.b = a.b; p.seeds = a.seeds; p.y = a.y;
+  p.b = a.b; p.seeds = a.seeds; p.y = a.y;
   p.pop = a.pop; p.batch = a.batch; p.in = a.in; p.out = a.out;
   p.offset = a.offset; p.sigma = a.sigma;
   p.b_bf16 = (a.b != nullptr && a.b_dt == VN_BF16) ? 1 : 0;
@@ -683,9 +735,12 @@ cudaError_t launch_linear_tc_hook(const LinearArgs& a, cudaStream_t stream, long
   p.nbuf = (static_cast<int64_t>(g) * mh * nt <= kTmemCols / 2) ? 2 : 1;
   p.a_bytes = static_cast<uint32_t>(mh) * kHalfBytes;
   p.stage_bytes = p.a_bytes + static_cast<uint32_t>(nt) * 128u;
-  const size_t fixed = 1024 + 8 * (3 * 16 + 6) + 16;
+  p.w_bytes = 128u * static_cast<uint32_t>(kKC) * (wbf ? 2u : 4u);
+  // alignment slack + barriers (at most 8 stages) + TMEM address + wait control
+  const size_t fixed = 1024 + 8 * (3 * 8 + 9) + 8 + 16;
   const int stages = static_cast<int>(std::min<int64_t>(
-      8, (static_cast<int64_t>(dev.smem_optin) - static_cast<int64_t>(fixed)) / p.stage_bytes));
+      8, (static_cast<int64_t>(dev.smem_optin) - static_cast<int64_t>(fixed) -
+          2 * static_cast<int64_t>(p.w_bytes)) / p.stage_bytes));
   if (stages < 2) return cudaErrorInvalidConfiguration;
   p.stages = stages;
   p.k_chunks = static_cast<int>((a.in + kKC - 1) / kKC);
@@ -716,14 +771,35 @@ cudaError_t launch_linear_tc_hook(const LinearArgs& a, cudaStream_t stream, long
                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
 
-  const size_t smem = fixed + static_cast<size_t>(stages) * p.stage_bytes;
+  // W as a 2-D tensor [out][in] of its dtype; box = 64 k x 128 rows, no
+  // swizzle (the hashing warps read it with plain shared loads). Rows >= out
+  // and k >= in arrive as zeros.
+  CUtensorMap wmap;
+  std::memset(&wmap, 0, sizeof(wmap));
+  const cuuint64_t wdims[2] = {static_cast<cuuint64_t>(a.in), static_cast<cuuint64_t>(a.out)};
+  const cuuint64_t wstrides[1] = {static_cast<cuuint64_t>(a.in) * (wbf ? 2 : 4)};
+  const cuuint32_t wbox[2] = {static_cast<cuuint32_t>(kKC), 128};
+  const cuuint32_t westr[2] = {1, 1};
+  const CUresult wr = encode(&wmap,
+                             wbf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                             2, const_cast<void*>(a.w), wdims, wstrides, wbox, westr,
+                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (wr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+
+  const size_t smem = fixed + static_cast<size_t>(stages) * p.stage_bytes + 2 * p.w_bytes;
   const int grid = static_cast<int>(std::min<int64_t>(p.units, dev.sm_count));
   const bool ybf = a.y_dt == VN_BF16;
-  if (wbf) {
-    return ybf ? launch_typed<1, true, true>(xmap, p, grid, smem, stream)
-               : launch_typed<1, true, false>(xmap, p, grid, smem, stream);
+  if (withhold_stage >= 0) {
+    // The test hook has one instance: bf16 W and Y.
+    if (!(wbf && ybf)) return cudaErrorInvalidValue;
+    return launch_typed<1, true, true, true>(xmap, wmap, p, grid, smem, stream);
   }
-  return launch_typed<1, false, false>(xmap, p, grid, smem, stream);
+  if (wbf) {
+    return ybf ? launch_typed<1, true, true, false>(xmap, wmap, p, grid, smem, stream)
+               : launch_typed<1, true, false, false>(xmap, wmap, p, grid, smem, stream);
+  }
+  return launch_typed<1, false, false, false>(xmap, wmap, p, grid, smem, stream);
 }
 
 cudaError_t take_device_status(unsigned int* status, cudaStream_t stream) {
