@@ -4,8 +4,8 @@
 Default workload: the ES MLP policy step (pop 1024, batch 1, 64 -> 256 -> 256 -> 8
 with tanh, fp32, sigma 0.02, centered-rank fitness). One step is one pass of the
 whole hot path over one population:
-  * forward: three perturbed linears (the tanh between layers fused into the
-    epilogue of the first two),
+  * forward: the three perturbed linears in one launch (vn_perturbed_mlp: the
+    activations stay on chip, tanh between layers),
   * gradients: grad_W and grad_b of all three layers; the six blocks are laid
     out by compute_offsets one after another, so they are one flat range of
     element indices and one reduction over the population computes them all,
@@ -120,7 +120,31 @@ def build_step(wl, dev, stream_ptr):
     pop, batch = wl.pop, wl.batch
     dt = {torch.float32: _lib.VN_F32, torch.bfloat16: _lib.VN_BF16}
 
-    if wl.forward:
+    fused = (wl.forward and len(d.layers) > 1 and batch <= 8 and d.x.dtype in (torch.float32, torch.bfloat16)
+             and all(l.weight.dtype == torch.float32 and l.bias.dtype == torch.float32 for l in d.layers))
+    if fused:
+        # A policy (several fp32 layers, small batch): every layer in one launch,
+        # the activations kept on chip (vn_perturbed_mlp).
+        bufs["x"] = d.x
+        n = len(d.layers)
+        dims = [d.layers[0].in_f] + [l.out_f for l in d.layers]
+        for li, l in enumerate(d.layers):
+            bufs[f"w{li}"], bufs[f"b{li}"] = l.weight, l.bias
+        y = torch.empty((pop, batch, dims[-1]), dtype=torch.float32, device=dev)
+        c_dims = (ctypes.c_int64 * (n + 1))(*dims)
+        c_w = (ctypes.c_void_p * n)(*[l.weight.data_ptr() for l in d.layers])
+        c_b = (ctypes.c_void_p * n)(*[l.bias.data_ptr() for l in d.layers])
+        c_off = (ctypes.c_uint64 * n)(*[l.offset for l in d.layers])
+        act = _lib.VN_ACT_TANH if wl.activation == "tanh" else _lib.VN_ACT_NONE
+        args = (P(d.x.data_ptr()), dt[d.x.dtype], 0, n, c_dims, c_w, c_b, c_off, P(d.seeds.data_ptr()),
+                pop, batch, float(wl.sigma), act, P(y.data_ptr()), s)
+        el = pop * sum(l.out_f * l.in_f for l in d.layers)
+        hbm = (d.x.numel() * d.x.element_size() + y.numel() * 4
+               + sum(l.weight.numel() * 4 + l.bias.numel() * 4 for l in d.layers))
+        launches.append(Launch("linear_mlp", lib.vn_perturbed_mlp, args, el, flops=2.0 * el * batch,
+                               hbm_bytes=hbm))
+        outputs.append(y)
+    elif wl.forward:
         h = d.x
         bufs["x"] = d.x
         for li, l in enumerate(d.layers):

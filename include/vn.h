@@ -153,6 +153,39 @@ vn_status vn_reduce_metric(const float* center, const int64_t* seeds, int64_t po
                            int64_t n_params, double sigma, uint64_t offset,
                            float* fitness, void* stream);
 
+/*
+ * vn_perturbed_mlp -- a chain of "virtual_perturbed_linear" layers (API entry
+ * of the page) evaluated in one launch, for ES policies:
+ *     h_0 = X[i];  h_{l+1} = act_l( h_l @ (W_l + sigma*N_{i,l})^T + (b_l + sigma*nb_{i,l}) )
+ *     Y[i] = h_{n_layers}
+ * act_l = `act` for every layer but the last, which has none. Layer l reads its
+ * weight noise at offsets[l] + j*in_l + k and its bias noise at
+ * offsets[l] + out_l*in_l + j, exactly as vn_perturbed_linear with offset =
+ * offsets[l] would (with "compute_offsets" over (W_0, b_0, W_1, b_1, ...) the
+ * weight offsets are entries 0, 2, 4, ...).
+ * n_layers  1 .. 8.
+ * dims      HOST array of n_layers + 1 sizes: in_0, out_0 (= in_1), ..., out_{n-1}.
+ * w         HOST array of n_layers DEVICE pointers, w[l] fp32 [dims[l+1], dims[l]].
+ * b         HOST array of n_layers DEVICE pointers, b[l] fp32 [dims[l+1]] or NULL
+ *           (no bias and no bias noise for that layer); b itself may be NULL
+ *           (no layer has a bias).
+ * offsets   HOST array of n_layers weight-block offsets.
+ * x         [pop, batch, dims[0]] of x_dt (VN_F32 or VN_BF16), or [batch, dims[0]]
+ *           when x_shared != 0.      y  [pop, batch, dims[n_layers]] fp32.
+ * batch     0 .. 8 (the per-individual batch of a policy rollout); larger
+ *           batches return VN_ERR_SHAPE (use vn_perturbed_linear per layer).
+ * Arithmetic is fp32 throughout (as the FFMA path of vn_perturbed_linear); the
+ * activations between layers stay on chip. Layers wider than the device's
+ * shared memory allows for one individual (about 3,600 units at batch 8, far
+ * more at batch 1) return VN_ERR_SHAPE.
+ */
+vn_status vn_perturbed_mlp(const void* x, vn_dtype x_dt, int x_shared,
+                           int64_t n_layers, const int64_t* dims,
+                           const float* const* w, const float* const* b,
+                           const uint64_t* offsets,
+                           const int64_t* seeds, int64_t pop, int64_t batch,
+                           double sigma, vn_act act, float* y, void* stream);
+
 /* Synchronises `stream`, then reads and clears the current device's status
  * word: VN_ERR_TIMEOUT if a kernel of this library recorded an expired wait
  * since the last call, VN_ERR_CUDA if synchronisation failed, else VN_OK. */

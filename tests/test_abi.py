@@ -98,3 +98,33 @@ def test_empty_outputs_are_valid_and_launch_nothing(lib):
     assert lib.vn_reduce_metric(P(0), P(0), 0, 5, 0.1, 0, P(0), P(0)) == 0
     assert lib.vn_perturbed_linear(P(0), 0, 0, P(0), 0, P(0), 0, P(0), 0, 4, 4, 4, 0.1, 0,
                                    P(0), 0, P(0)) == 0
+
+
+def test_mlp_validation_refuses_before_launch(lib):
+    fake = 0x1000
+    I64, U64, VP = ctypes.c_int64, ctypes.c_uint64, ctypes.c_void_p
+
+    def call(n=2, dims=(4, 8, 2), w=(fake, fake), b=None, offs=(0, 40), x=fake, xd=0, s=fake,
+             pop=3, batch=1, sig=0.1, act=1, y=fake):
+        cd = (I64 * len(dims))(*dims)
+        cw = (VP * len(w))(*w)
+        cb = None if b is None else (VP * len(b))(*b)
+        co = (U64 * len(offs))(*offs)
+        return lib.vn_perturbed_mlp(P(x), xd, 0, n, cd, cw, cb, co, P(s), pop, batch, sig, act,
+                                    P(y), P(0))
+    assert call(xd=5) == 3                        # unknown x dtype
+    assert call(act=9) == 4                       # unknown activation
+    assert call(n=0) == 2                         # no layers
+    assert call(n=9, dims=(4,) * 10, w=(fake,) * 9, offs=(0,) * 9) == 2   # more than 8 layers
+    assert call(batch=9) == 2                     # batch above 8
+    assert call(dims=(4, -8, 2)) == 2
+    assert call(sig=float("inf")) == 4
+    assert call(w=(fake, 0)) == 1                 # a layer with weights needs a pointer
+    assert call(w=(fake + 2, fake)) == 5          # fp32 weights 4-byte aligned
+    assert call(b=(fake, fake + 1)) == 5
+    assert call(s=0) == 1
+    assert call(y=fake + 2) == 5
+    assert call(x=0) == 1
+    assert call(pop=1 << 40, batch=8, dims=(4, 8, 1 << 30)) == 6
+    assert call(pop=0, s=0, y=0, x=0) == 0        # empty output: valid, nothing launched
+    assert call(dims=(4, 8, 0), y=0) == 0

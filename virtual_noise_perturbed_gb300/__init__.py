@@ -17,12 +17,14 @@ from .api import (  # noqa: F401
     virtual_bias_gradient,
     virtual_flat_gradient,
     virtual_perturbed_linear,
+    virtual_perturbed_mlp,
     virtual_reduce_metric,
     virtual_weight_gradient,
 )
 
 __all__ = [
     "VNError", "compute_offsets", "device_status", "noise_dump", "perturbed_linear_path",
-    "virtual_bias_gradient", "virtual_flat_gradient", "virtual_perturbed_linear", "virtual_reduce_metric",
+    "virtual_bias_gradient", "virtual_flat_gradient", "virtual_perturbed_linear", "virtual_perturbed_mlp",
+    "virtual_reduce_metric",
     "virtual_weight_gradient",
 ]

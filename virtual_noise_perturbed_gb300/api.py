@@ -105,6 +105,73 @@ def virtual_perturbed_linear(x: torch.Tensor, weight: torch.Tensor, bias: Option
     return out
 
 
+def virtual_perturbed_mlp(x: torch.Tensor, weights: Sequence[torch.Tensor],
+                          biases: Optional[Sequence[Optional[torch.Tensor]]], seeds: torch.Tensor,
+                          sigma: float, offsets: Optional[Sequence[int]] = None, *,
+                          activation: Optional[str] = "tanh",
+                          out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """A chain of perturbed linear layers in one launch (fp32 weights, batch <= 8).
+
+    Layer l computes ``act(h @ (W_l + sigma*N_{i,l})^T + b_l + sigma*nb_{i,l})``
+    with the activation on every layer but the last. ``offsets`` are the weight
+    blocks' offsets; by default those of ``compute_offsets`` over
+    (W_0, b_0, W_1, b_1, ...) -- so layer l's bias noise sits right after its
+    weights, as in ``virtual_perturbed_linear``. x is (batch, in) or
+    (pop, batch, in); the result is fp32 (pop, batch, out_last)."""
+    lib = load()
+    x = _cuda(x, "x")
+    seeds = _seeds(seeds)
+    weights = [_cuda(w, f"weights[{l}]") for l, w in enumerate(weights)]
+    n = len(weights)
+    if n == 0:
+        raise ValueError("at least one layer is needed")
+    if biases is None:
+        biases = [None] * n
+    if len(biases) != n:
+        raise ValueError("one bias (or None) per layer")
+    dims = [weights[0].shape[1]] + [w.shape[0] for w in weights]
+    for l, w in enumerate(weights):
+        if w.dim() != 2 or w.shape[1] != dims[l] or w.dtype != torch.float32:
+            raise ValueError(f"weights[{l}] must be float32 ({dims[l + 1]}, {dims[l]})")
+    biases = [None if b is None else _cuda(b, f"biases[{l}]") for l, b in enumerate(biases)]
+    for l, b in enumerate(biases):
+        if b is not None and (b.shape != (dims[l + 1],) or b.dtype != torch.float32):
+            raise ValueError(f"biases[{l}] must be float32 ({dims[l + 1]},)")
+    if offsets is None:
+        shapes = []
+        for l in range(n):
+            shapes += [(dims[l + 1], dims[l]), (dims[l + 1],)]
+        offsets = compute_offsets(shapes)[0::2]
+    if len(offsets) != n:
+        raise ValueError("one offset per layer")
+    pop = seeds.numel()
+    if x.dim() == 2:
+        shared, batch = 1, x.shape[0]
+    elif x.dim() == 3:
+        if x.shape[0] != pop:
+            raise ValueError(f"x has {x.shape[0]} individuals but there are {pop} seeds")
+        shared, batch = 0, x.shape[1]
+    else:
+        raise ValueError("x must be (batch, in) or (pop, batch, in)")
+    if x.shape[-1] != dims[0]:
+        raise ValueError(f"x has {x.shape[-1]} features, the first layer expects {dims[0]}")
+    if activation not in _ACTS:
+        raise ValueError("activation must be None or 'tanh'")
+    if out is None:
+        out = torch.empty((pop, batch, dims[-1]), dtype=torch.float32, device=x.device)
+    elif out.shape != (pop, batch, dims[-1]) or out.dtype != torch.float32 or not out.is_contiguous():
+        raise ValueError("out has the wrong shape, dtype or layout")
+    c_dims = (ctypes.c_int64 * (n + 1))(*dims)
+    c_w = (ctypes.c_void_p * n)(*[_ptr(w).value for w in weights])
+    c_b = (ctypes.c_void_p * n)(*[_ptr(b).value for b in biases])
+    c_off = (ctypes.c_uint64 * n)(*[int(o) & _M64 for o in offsets])
+    st = lib.vn_perturbed_mlp(_ptr(x), _dt(x, "x"), shared, n, c_dims, c_w, c_b, c_off,
+                              _ptr(seeds), pop, batch, float(sigma), _ACTS[activation],
+                              _ptr(out), _stream(x))
+    check(st, "vn_perturbed_mlp")
+    return out
+
+
 def _fitness(fitness: torch.Tensor, pop_size: int, seeds: torch.Tensor) -> torch.Tensor:
     fitness = _cuda(fitness, "fitness").reshape(-1).to(torch.float32)
     if fitness.numel() != pop_size or seeds.numel() != pop_size:

@@ -253,6 +253,51 @@ vn_status vn_testhook_linear_tc_withhold(const void* x, vn_dtype x_dt, int x_sha
                                             static_cast<unsigned long long>(timeout_ms * 1e6)));
 }
 
+vn_status vn_perturbed_mlp(const void* x, vn_dtype x_dt, int x_shared, int64_t n_layers,
+                           const int64_t* dims, const float* const* w, const float* const* b,
+                           const uint64_t* offsets, const int64_t* seeds, int64_t pop,
+                           int64_t batch, double sigma, vn_act act, float* y, void* stream) {
+  if (!dtype_ok(x_dt)) return VN_ERR_DTYPE;
+  if (act != VN_ACT_NONE && act != VN_ACT_TANH) return VN_ERR_VALUE;
+  if (n_layers < 1 || n_layers > vn::kMlpMaxLayers) return VN_ERR_SHAPE;
+  if (dims == nullptr || w == nullptr || offsets == nullptr) return VN_ERR_NULL;
+  if (pop < 0 || batch < 0 || batch > vn::kMlpMaxBatch) return VN_ERR_SHAPE;
+  constexpr int64_t kMaxDim = (int64_t{1} << 31) - 1;
+  for (int64_t l = 0; l <= n_layers; ++l)
+    if (dims[l] < 0 || dims[l] > kMaxDim) return VN_ERR_SHAPE;
+  float sig;
+  if (!float_sigma(sigma, &sig)) return VN_ERR_VALUE;
+  int64_t x_elems, y_elems, t;
+  if (!mul(batch, dims[0], &x_elems) || (!x_shared && !mul(x_elems, pop, &x_elems)) ||
+      !mul(pop, batch, &t) || !mul(t, dims[n_layers], &y_elems))
+    return VN_ERR_OVERFLOW;
+  for (int64_t l = 0; l < n_layers; ++l) {
+    int64_t we;
+    if (!mul(dims[l], dims[l + 1], &we)) return VN_ERR_OVERFLOW;
+    if (we > 0 && w[l] == nullptr) return VN_ERR_NULL;
+    if (!aligned(w[l], 4) || (b != nullptr && !aligned(b[l], 4))) return VN_ERR_ALIGN;
+  }
+  if (y_elems == 0) return VN_OK;
+  if (seeds == nullptr || y == nullptr || (x_elems > 0 && x == nullptr)) return VN_ERR_NULL;
+  if (!aligned(seeds, 8) || !aligned(y, 4) || !aligned(x, dtype_size(x_dt))) return VN_ERR_ALIGN;
+  // The one device-dependent check: both activation buffers of one individual
+  // must fit in the device's shared memory.
+  const size_t buf = vn::mlp_buffer_floats(static_cast<int>(n_layers), dims);
+  vn::DeviceInfo dev;
+  cudaError_t err = vn::device_info(&dev);
+  if (err != cudaSuccess) return cuda_failure(err);
+  if (vn::mlp_bytes_per_individual(batch, buf) > static_cast<size_t>(dev.smem_optin))
+    return VN_ERR_SHAPE;
+
+  static const float* const kNoBias[vn::kMlpMaxLayers] = {};
+  vn::MlpArgs m;
+  m.x = x; m.x_dt = x_dt; m.x_shared = x_shared ? 1 : 0;
+  m.n_layers = static_cast<int>(n_layers);
+  m.dims = dims; m.w = w; m.b = b != nullptr ? b : kNoBias; m.offsets = offsets;
+  m.seeds = seeds; m.pop = pop; m.batch = batch; m.sigma = sig; m.act = act; m.y = y;
+  return launched(vn::launch_mlp(m, static_cast<cudaStream_t>(stream)));
+}
+
 vn_status vn_device_status(void* stream) {
   cudaError_t err = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (err != cudaSuccess) return cuda_failure(err);

@@ -65,6 +65,33 @@ cudaError_t launch_linear_tc(const LinearArgs& a, cudaStream_t stream);
 cudaError_t launch_linear_tc_hook(const LinearArgs& a, cudaStream_t stream, long long withhold_stage,
                                   unsigned long long timeout_ns);
 
+// A chain of perturbed linear layers in one launch (fp32 weights, batch <= 8).
+constexpr int kMlpMaxLayers = 8;
+constexpr int64_t kMlpMaxBatch = 8;
+struct MlpArgs {
+  const void* x;
+  vn_dtype x_dt;
+  int x_shared;
+  int n_layers;
+  const int64_t* dims;       // host, n_layers + 1
+  const float* const* w;     // host array of device pointers
+  const float* const* b;     // host array of device pointers (entries may be null)
+  const uint64_t* offsets;   // host, n_layers
+  const int64_t* seeds;
+  int64_t pop, batch;
+  float sigma;
+  vn_act act;
+  float* y;
+};
+// Floats per (individual, batch row) of one activation buffer for these dims.
+size_t mlp_buffer_floats(int n_layers, const int64_t* dims);
+// Shared memory the kernel needs for one individual at this batch (both buffers).
+inline size_t mlp_bytes_per_individual(int64_t batch, size_t buf_floats) {
+  const int64_t nb = batch <= 1 ? 1 : batch <= 2 ? 2 : batch <= 4 ? 4 : 8;
+  return 2 * static_cast<size_t>(nb) * buf_floats * sizeof(float) + 64;
+}
+cudaError_t launch_mlp(const MlpArgs& m, cudaStream_t stream);
+
 // Reads and clears the device status word of the bounded-wait kernels (0 = fine).
 cudaError_t take_device_status(unsigned int* status, cudaStream_t stream);
 

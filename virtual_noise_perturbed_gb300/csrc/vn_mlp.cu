@@ -1,0 +1,373 @@
+// vn_mlp.cu -- a chain of perturbed linear layers (an ES policy) in one launch.
+//
+// EvoX API page "evox.triton_kernels.kernels.virtual_noise": each layer is the
+// "virtual_perturbed_linear" entry,
+//   h_{l+1}[i] = act_l( h_l[i] @ (W_l + sigma*N_{i,l})^T + (b_l + sigma*nb_{i,l}) ),
+// with N_{i,l}[j,k] at offset_l + j*in_l + k and nb_{i,l}[j] at
+// offset_l + out_l*in_l + j ("Noise indexing scheme"), and the layers' offsets
+// laid out by "compute_offsets". The activation between layers (tanh) is not
+// part of the method; the last layer has none.
+//
+// Why one launch: at the policy sizes (batch 1 per individual, layers of a few
+// hundred units) a layer is a few microseconds of hashing, so separate
+// launches pay a launch gap and a full-device drain per layer, and the small
+// last layer cannot fill the GPU. Here an individual's activations never leave
+// shared memory: a CTA takes a contiguous slice of the population, P
+// individuals at a time, and runs them through every layer.
+//
+// Work of one layer inside a CTA (16 warps):
+//   * A row of W_l is split into 8-element chunks; LR lanes (a power of two,
+//     at most 32) share a row, each taking every LR-th chunk, so a warp covers
+//     32/LR rows at a time and the warps take row groups round-robin. LR is
+//     the smallest power of two that gives every thread a row slot (2 for 256
+//     rows on 512 threads, 32 for 8 rows), so wide layers need only a short
+//     butterfly per row and the lanes of a warp read the same activation chunk
+//     (a shared-memory broadcast).
+//   * Per chunk a lane loads the 8 weights once (from L2: W is shared by the
+//     whole population) as W - 1.5*sigma with the chunk's state term
+//     (offset + j*in + k + 1)*GAMMA, then for each of the P individuals hashes
+//     the 8 elements, forms W' = fma(sigma, 1 + u, W - 1.5*sigma) = W +
+//     sigma*n and adds W' . h[i][k..k+7] to that individual's partial sum. The
+//     next chunk's weights are loaded while this one is hashed.
+//   * The LR partials of a row are summed with an xor butterfly (fixed order,
+//     deterministic); lane q of the group then finishes the (individual, batch
+//     row) pairs congruent to q: bias, bias noise, activation, and the value
+//     goes to the other activation buffer in shared memory.
+//   * Chunks past the end of a row read zero activations (each buffer is
+//     zero-padded to the length the next layer reads) and rows past `out`
+//     are computed on zero weights and discarded, so no lane branches on
+//     ragged edges.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "vn_hash.cuh"
+#include "vn_internal.h"
+
+namespace vn {
+namespace {
+
+constexpr int kWarps = 16;
+constexpr int kThreads = kWarps * 32;
+constexpr int kAcc = 8;              // accumulators per lane: individuals x batch rows per group
+constexpr int kSeedFloats = 16;      // shared-memory words reserved for the group's seeds
+
+struct MlpLayerDev {
+  const float* w;
+  const float* b;   // may be null
+  uint64_t offset;  // weight block offset; bias noise at offset + out*in
+  int in, out;
+  int lr_log2;      // LR = 1 << lr_log2 lanes per row
+  int cpl;          // chunks per lane: ceil(ceil(in / 8) / LR)
+  int in_pad;       // length this layer reads from its input buffer: LR * cpl * 8
+  int w_vec;        // W rows are 16-byte aligned and in % 8 == 0: two float4 loads per chunk
+};
+
+struct MlpDev {
+  MlpLayerDev layer[kMlpMaxLayers];
+  const void* x;
+  const int64_t* seeds;
+  float* y;
+  int64_t pop;
+  int batch;
+  int n_layers;
+  int x_shared;
+  int act;
+  int p;        // individuals per group (<= kAcc / NB)
+  int buf_len;  // floats per (individual, batch row) in an activation buffer, a multiple of 8
+  float sigma;
+};
+
+// Eight weights of row j from column k (zeros outside the matrix).
+__device__ __forceinline__ void load_w8(const MlpLayerDev& L, int j, int k, float (&w)[8]) {
+  if (j < L.out && k < L.in) {
+    const float* src = L.w + static_cast<int64_t>(j) * L.in + k;
+    if (L.w_vec) {
+      const float4 a = __ldg(reinterpret_cast<const float4*>(src));
+      const float4 b = __ldg(reinterpret_cast<const float4*>(src) + 1);
+      w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+      w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) w[e] = (k + e < L.in) ? __ldg(src + e) : 0.f;
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) w[e] = 0.f;
+  }
+}
+
+template <int NB, bool kXBf16>
+__global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant__ MlpDev a) {
+  constexpr int kP = kAcc / NB;  // individuals per group, compile-time bound
+  extern __shared__ float4 smem4[];
+  float* smem = reinterpret_cast<float*>(smem4);
+  uint2* s_seed = reinterpret_cast<uint2*>(smem);                 // [P]
+  const int P = a.p;
+  const int blen = a.buf_len;
+  // Two activation buffers [P][NB][blen], `bstride` floats apart.
+  float* const s_buf0 = smem + kSeedFloats;
+  const int bstride = P * NB * blen;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const float sigma = a.sigma;
+  const float shift = -1.5f * sigma;
+  const int64_t i_begin = a.pop * blockIdx.x / gridDim.x;
+  const int64_t i_end = a.pop * (blockIdx.x + 1) / gridDim.x;
+
+  for (int64_t ib = i_begin; ib < i_end; ib += P) {
+    const int np = static_cast<int>(min(static_cast<int64_t>(P), i_end - ib));
+    __syncthreads();  // the previous group is done with the seeds and buffers
+    for (int t = threadIdx.x; t < np; t += kThreads) {
+      const uint64_t s = static_cast<uint64_t>(a.seeds[ib + t]);
+      s_seed[t] = make_uint2(static_cast<uint32_t>(s), static_cast<uint32_t>(s >> 32));
+    }
+    // Stage x: zero past `in`, for batch rows >= batch and for missing individuals.
+    {
+      const int in0 = a.layer[0].in;
+      const int per = NB * blen;
+      for (int t = threadIdx.x; t < P * per; t += kThreads) {
+        const int ii = t / per;
+        const int rem = t - ii * per;
+        const int r = rem / blen;
+        const int k = rem - r * blen;
+        float v = 0.f;
+        if (ii < np && r < a.batch && k < in0) {
+          const int64_t row = (a.x_shared ? 0 : (ib + ii) * a.batch) + r;
+          if constexpr (kXBf16)
+            v = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(a.x)[row * in0 + k]);
+          else
+            v = reinterpret_cast<const float*>(a.x)[row * in0 + k];
+        }
+        s_buf0[t] = v;
+      }
+    }
+    __syncthreads();
+
+    for (int l = 0; l < a.n_layers; ++l) {
+      const MlpLayerDev& L = a.layer[l];
+      const float* src = s_buf0 + (l & 1) * bstride;
+      float* dst = s_buf0 + ((l & 1) ^ 1) * bstride;
+      const bool last = l + 1 == a.n_layers;
+      const int LR = 1 << L.lr_log2;
+      const int q = lane & (LR - 1);         // lane within its row group
+      const int rsub = lane >> L.lr_log2;    // row of this lane within the warp's group
+      const int rows_per_group = 32 >> L.lr_log2;
+      const int n_rg = (L.out + rows_per_group - 1) / rows_per_group;
+      const int my_rg = n_rg > warp ? (n_rg - warp + kWarps - 1) / kWarps : 0;
+      const int cpl = L.cpl;
+      const int steps = my_rg * cpl;
+      const uint64_t bias_base =
+          L.offset + static_cast<uint64_t>(L.out) * static_cast<uint64_t>(L.in);
+
+      float part[kP][NB];
+      float wn[8];
+      if (steps > 0) load_w8(L, warp * rows_per_group + rsub, q * 8, wn);
+      for (int s = 0, rgi = 0, m = 0; s < steps; ++s) {
+        const int j = (warp + rgi * kWarps) * rows_per_group + rsub;
+        const int k = (q + (m << L.lr_log2)) * 8;
+        if (m == 0) {
+#pragma unroll
+          for (int ii = 0; ii < kP; ++ii)
+#pragma unroll
+            for (int r = 0; r < NB; ++r) part[ii][r] = 0.f;
+        }
+        float wm[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) wm[e] = wn[e] + shift;
+        // The next step's chunk: the same row's next one, or the next row group's first.
+        const int m1 = (m + 1 < cpl) ? m + 1 : 0;
+        const int rgi1 = (m + 1 < cpl) ? rgi : rgi + 1;
+        if (s + 1 < steps)
+          load_w8(L, (warp + rgi1 * kWarps) * rows_per_group + rsub, (q + (m1 << L.lr_log2)) * 8, wn);
+        const uint64_t bst = index_term(L.offset +
+                                        static_cast<uint64_t>(j) * static_cast<uint64_t>(L.in) +
+                                        static_cast<uint64_t>(k));
+#pragma unroll
+        for (int ii = 0; ii < kP; ++ii) {
+          if (ii < np) {
+            const uint2 sd = s_seed[ii];
+            uint64_t st = bst + ((static_cast<uint64_t>(sd.y) << 32) | sd.x);
+            float wp[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              wp[e] = fmaf(sigma, __uint_as_float(mix_to_one_plus_u(st)), wm[e]);
+              st += kGamma;
+            }
+#pragma unroll
+            for (int r = 0; r < NB; ++r) {
+              const float4* h = reinterpret_cast<const float4*>(src + (ii * NB + r) * blen + k);
+              const float4 xa = h[0], xb = h[1];
+              float acc = part[ii][r];
+              acc = fmaf(xa.x, wp[0], acc);
+              acc = fmaf(xa.y, wp[1], acc);
+              acc = fmaf(xa.z, wp[2], acc);
+              acc = fmaf(xa.w, wp[3], acc);
+              acc = fmaf(xb.x, wp[4], acc);
+              acc = fmaf(xb.y, wp[5], acc);
+              acc = fmaf(xb.z, wp[6], acc);
+              acc = fmaf(xb.w, wp[7], acc);
+              part[ii][r] = acc;
+            }
+          }
+        }
+        if (m + 1 == cpl) {
+          // Sum the row's LR partials (every lane of the group ends with the total).
+          for (int o = LR >> 1; o > 0; o >>= 1) {
+#pragma unroll
+            for (int ii = 0; ii < kP; ++ii)
+#pragma unroll
+              for (int r = 0; r < NB; ++r)
+                part[ii][r] += __shfl_xor_sync(0xffffffffu, part[ii][r], o);
+          }
+          if (j < L.out) {
+            const float bj = L.b != nullptr ? __ldg(L.b + j) : 0.f;
+#pragma unroll
+            for (int ii = 0; ii < kP; ++ii) {
+#pragma unroll
+              for (int r = 0; r < NB; ++r) {
+                if (ii < np && ((ii * NB + r) & (LR - 1)) == q) {
+                  float v = part[ii][r];
+                  if (L.b != nullptr) {
+                    const uint2 sd = s_seed[ii];
+                    const uint64_t seed = (static_cast<uint64_t>(sd.y) << 32) | sd.x;
+                    v += fmaf(sigma, noise_at(seed, bias_base + static_cast<uint64_t>(j)), bj);
+                  }
+                  if (!last && a.act == VN_ACT_TANH) v = tanhf(v);
+                  dst[(ii * NB + r) * blen + j] = v;
+                }
+              }
+            }
+          }
+        }
+        if (++m == cpl) { m = 0; ++rgi; }
+      }
+      // dst must read as zeros on [out, next layer's in_pad).
+      if (!last) {
+        const int pad = a.layer[l + 1].in_pad - L.out;
+        if (pad > 0) {
+          for (int t = threadIdx.x; t < P * NB * pad; t += kThreads) {
+            const int row = t / pad;
+            dst[row * blen + L.out + (t - row * pad)] = 0.f;
+          }
+        }
+      }
+      __syncthreads();
+    }
+
+    // y[i, r, j] from the last layer's buffer.
+    const float* fin = s_buf0 + (a.n_layers & 1) * bstride;
+    const int outl = a.layer[a.n_layers - 1].out;
+    const int per = a.batch * outl;
+    for (int t = threadIdx.x; t < np * per; t += kThreads) {
+      const int ii = t / per;
+      const int rem = t - ii * per;
+      const int r = rem / outl;
+      const int j = rem - r * outl;
+      a.y[(ib + ii) * per + rem] = fin[(ii * NB + r) * blen + j];
+    }
+  }
+}
+
+// Lanes per row (as log2), chunks per lane and the padded input length of a
+// layer. Enough lanes share a row to give every thread of the CTA a row slot
+// (fewer rows -> more lanes per row), but never more lanes than the row has
+// chunks: the butterfly that sums a row's lanes is then short for wide layers.
+struct LayerShape {
+  int lr_log2, cpl, in_pad;
+};
+LayerShape layer_shape(int64_t in, int64_t out) {
+  const int64_t chunks = std::max<int64_t>(1, (in + 7) / 8);  // in == 0: one all-zero chunk
+  int lg = 0;
+  while (lg < 5 && (int64_t{2} << lg) * std::max<int64_t>(out, 1) <= kThreads &&
+         (int64_t{1} << lg) < chunks)
+    ++lg;
+  LayerShape sh;
+  sh.lr_log2 = lg;
+  sh.cpl = static_cast<int>((chunks + (int64_t{1} << lg) - 1) >> lg);
+  sh.in_pad = sh.cpl * (8 << lg);
+  return sh;
+}
+
+template <int NB, bool kX>
+cudaError_t launch_typed(MlpDev& d, cudaStream_t stream, const DeviceInfo& dev) {
+  auto fn = mlp_kernel<NB, kX>;
+  constexpr int kP = kAcc / NB;
+  const size_t per_ind = 2ull * NB * static_cast<size_t>(d.buf_len) * sizeof(float);
+  const size_t base = kSeedFloats * sizeof(float);
+  const size_t budget = static_cast<size_t>(dev.smem_optin);
+  if (base + per_ind > budget) return cudaErrorInvalidValue;  // checked by the caller
+  d.p = static_cast<int>(std::min<size_t>(kP, (budget - base) / per_ind));
+  const size_t smem = base + static_cast<size_t>(d.p) * per_ind;
+  if (smem > 48 * 1024) {
+    static size_t configured = 0;
+    if (configured < smem) {
+      cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+      if (err != cudaSuccess) return err;
+      configured = smem;
+    }
+  }
+  int occ = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, kThreads, smem) != cudaSuccess ||
+      occ < 1)
+    occ = 1;
+  const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(d.pop, int64_t{dev.sm_count} * occ));
+  fn<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(d);
+  return cudaGetLastError();
+}
+
+template <int NB>
+cudaError_t launch_nb(MlpDev& d, bool xb, cudaStream_t stream, const DeviceInfo& dev) {
+  return xb ? launch_typed<NB, true>(d, stream, dev) : launch_typed<NB, false>(d, stream, dev);
+}
+
+}  // namespace
+
+size_t mlp_buffer_floats(int n_layers, const int64_t* dims) {
+  int64_t len = 8;
+  for (int l = 0; l < n_layers; ++l) {
+    len = std::max<int64_t>(len, layer_shape(dims[l], dims[l + 1]).in_pad);
+    len = std::max<int64_t>(len, dims[l + 1]);
+  }
+  return static_cast<size_t>((len + 7) / 8 * 8);
+}
+
+cudaError_t launch_mlp(const MlpArgs& m, cudaStream_t stream) {
+  DeviceInfo dev;
+  cudaError_t err = device_info(&dev);
+  if (err != cudaSuccess) return err;
+  MlpDev d{};
+  for (int l = 0; l < m.n_layers; ++l) {
+    MlpLayerDev& L = d.layer[l];
+    L.w = m.w[l];
+    L.b = m.b[l];
+    L.offset = m.offsets[l];
+    L.in = static_cast<int>(m.dims[l]);
+    L.out = static_cast<int>(m.dims[l + 1]);
+    const LayerShape sh = layer_shape(L.in, L.out);
+    L.lr_log2 = sh.lr_log2;
+    L.cpl = sh.cpl;
+    L.in_pad = sh.in_pad;
+    L.w_vec = (L.in % 8 == 0) && (reinterpret_cast<uintptr_t>(L.w) % 16 == 0);
+  }
+  d.x = m.x;
+  d.seeds = m.seeds;
+  d.y = m.y;
+  d.pop = m.pop;
+  d.batch = static_cast<int>(m.batch);
+  d.n_layers = m.n_layers;
+  d.x_shared = m.x_shared;
+  d.act = m.act;
+  d.buf_len = static_cast<int>(mlp_buffer_floats(m.n_layers, m.dims));
+  d.sigma = m.sigma;
+  const bool xb = m.x_dt == VN_BF16;
+  if (m.batch <= 1) return launch_nb<1>(d, xb, stream, dev);
+  if (m.batch <= 2) return launch_nb<2>(d, xb, stream, dev);
+  if (m.batch <= 4) return launch_nb<4>(d, xb, stream, dev);
+  return launch_nb<8>(d, xb, stream, dev);
+}
+
+}  // namespace vn
