@@ -284,17 +284,23 @@ struct RawF32 { float4 a, b; };
 struct RawBf16 { uint4 a; };
 
 // The 8 weights of a chunk as fp32, minus 1.5*sigma: sigma*(1 + u) + (W - 1.5*sigma) = W + sigma*n.
-__device__ __forceinline__ void unpack_shift(const RawBf16& r, float shift, float (&w)[8]) {
-  const uint32_t wr[4] = {r.a.x, r.a.y, r.a.z, r.a.w};
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    w[2 * e] = __uint_as_float(wr[e] << 16) + shift;
-    w[2 * e + 1] = __uint_as_float(wr[e] & 0xFFFF0000u) + shift;
-  }
-}
 __device__ __forceinline__ void unpack_shift(const RawF32& r, float shift, float (&w)[8]) {
   w[0] = r.a.x + shift; w[1] = r.a.y + shift; w[2] = r.a.z + shift; w[3] = r.a.w + shift;
   w[4] = r.b.x + shift; w[5] = r.b.y + shift; w[6] = r.b.z + shift; w[7] = r.b.w + shift;
+}
+
+// float(bf16 half of w selected by kHi) + t, one fp32 rounding (mixed-precision add).
+template <bool kHi>
+__device__ __forceinline__ float add_bf16_f32(uint32_t w, float t) {
+  float d;
+  if constexpr (kHi) {
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.bf16 %0, hi, %2;\n\t}"
+        : "=f"(d) : "r"(w), "f"(t));
+  } else {
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.bf16 %0, lo, %2;\n\t}"
+        : "=f"(d) : "r"(w), "f"(t));
+  }
+  return d;
 }
 
 // A work unit; every field fits in 32 bits on this path (pop, batch, in and out
@@ -593,20 +599,23 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                             static_cast<uint64_t>(cc * 8));
       }
       for (int kc = 0; ok && kc < p.k_chunks; ++kc) {
-        // W - 1.5*sigma of this stage group's chunks, shared by its G
-        // individuals. Chunks outside the matrix (row >= out or k >= in, only
+        // This stage group's W chunks, shared by its G individuals: fp32 W is
+        // kept as W - 1.5*sigma and perturbed with one FMA per element; bf16 W
+        // stays packed and each element is formed as fp32(bf16 W) + sigma*n
+        // with one mixed-precision add (no unpacking on the integer pipe).
+        // Chunks outside the matrix (row >= out or k >= in, only
         // at ragged edges) are TMA's zero fill, so their values are finite:
         // their X columns are zero fill too (k >= in) or their output rows are
         // never stored (row >= out), and no masking is needed below.
         if (!(ok = mbar_wait(full_w(wr.s), wr.ph, s_abort))) break;
         float wm[kCPT][8];
+        Raw wraw[kCPT];
         {
           const uint32_t wb = wslot0 + wr.s * p.w_bytes;
 #pragma unroll
           for (int q = 0; q < kCPT; ++q) {
-            Raw r;
-            load_w(wb + woff(q), r);
-            unpack_shift(r, shift, wm[q]);
+            load_w(wb + woff(q), wraw[q]);
+            if constexpr (!kWBf16) unpack_shift(wraw[q], shift, wm[q]);
           }
         }
         // The slot's next tile is written by TMA (the async proxy): order this
@@ -632,7 +641,15 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
             float pv[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-              pv[e] = fmaf(sigma, __uint_as_float(mix_to_one_plus_u(slo, shi)), wm[q][e]);
+              if constexpr (kWBf16) {
+                // sigma*n = fma(sigma, 1 + u, -1.5*sigma), then + W straight from its bf16 bits.
+                const float t = fmaf(sigma, __uint_as_float(mix_to_one_plus_u(slo, shi)), shift);
+                const uint32_t wv = (e & 4) ? ((e & 2) ? wraw[q].a.w : wraw[q].a.z)
+                                            : ((e & 2) ? wraw[q].a.y : wraw[q].a.x);
+                pv[e] = (e & 1) ? add_bf16_f32<true>(wv, t) : add_bf16_f32<false>(wv, t);
+              } else {
+                pv[e] = fmaf(sigma, __uint_as_float(mix_to_one_plus_u(slo, shi)), wm[q][e]);
+              }
               add64(slo, shi, kGammaLo, kGammaHi);
             }
             st_shared_v4(a0 + soff(q), pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]),
