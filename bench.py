@@ -48,12 +48,14 @@ METRIC = "virtual-noise elem/s"
 UNIT = "noise elements/s"
 
 # Cost of one noise element in the definition, on 32-bit halves (the GPU has no
-# 64-bit integer unit). Integer ALU pipe (LOP3 / SHF / IADD): right shifts 6 (two
+# 64-bit integer unit). Integer ALU pipe (LOP3 / SHF / IADD3): right shifts 6 (two
 # funnel shifts and two plain shifts for the xor-shifts 30 and 27, two for the
-# final xor-shift 31 with the top-23-bit extraction), three-input logic ops 5,
-# state add 2  -> 13. IMAD pipe: the two products by GAMMA, 3 each -> 6. Plus the
-# float conversion and the FMA that consumes the noise -> 21 operations in all.
-ALU_OPS_PER_ELEMENT = 13
+# final xor-shift 31 with the top-23-bit extraction), three-input logic ops 5, and
+# the low word of the 64-bit state add 1 (its high word, an add with carry-in, can
+# issue on the IMAD pipe, as the compiler does in the gradient kernel) -> 12. IMAD
+# pipe: the two products by GAMMA, 3 each, plus that carry add -> 7. Plus the float
+# conversion and the FMA that consumes the noise -> 21 operations in all.
+ALU_OPS_PER_ELEMENT = 12
 OPS_PER_ELEMENT = 21
 SMS_NOMINAL = 152
 SM_CLOCK_MAX_HZ = 2.07e9
@@ -290,14 +292,14 @@ def barrier(world: int):
         dist.barrier()
 
 
-def traffic_for(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel's source
-    is unchanged since the capture (else None)."""
+def traffic_for(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel on this
+    workload, if the kernel's source is unchanged since the capture (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
-        rec = json.load(f).get(kernel)
+        rec = json.load(f).get(f"{kernel}@{workload}")
     if not rec:
         return None
     src = os.path.join(ROOT, "virtual_noise_perturbed_gb300", "csrc", rec["source"])
@@ -486,7 +488,7 @@ def main(argv=None) -> int:
     bound = max(cands, key=lambda b: cands[b][0] / cands[b][1])
     ach, peak, unit = cands[bound]
     roofline = {"bound": bound, "kernel": dom, "achieved": ach, "peak": peak, "unit": unit,
-                "frac": ach / peak, "traffic": traffic_for(dom),
+                "frac": ach / peak, "traffic": traffic_for(dom, wl.name),
                 "peak_source": ("derived: 152 SMs x 64 integer-ALU lanes x 2.07 GHz"
                                 if bound == "alu" else pk["source"]),
                 "ops_per_element": ALU_OPS_PER_ELEMENT if bound == "alu" else None,
