@@ -60,7 +60,10 @@ constexpr uint32_t kHalfBytes = 128 * 128;                    // 128 rows x 128 
 constexpr int kTmemCols = 512;
 constexpr unsigned long long kTimeoutNs = 4000000000ull;      // default limit of one wait: 4 s
 // Back-off between polls of roles that run stages ahead of their consumers.
-constexpr uint32_t kProducerSleepNs = 1024;
+// The TMA producer polls without one (its waits suspend on the barrier): with
+// one individual per unit every stage needs a fresh W tile, and a late copy
+// stalls all hashing warps.
+constexpr uint32_t kProducerSleepNs = 0;
 constexpr uint32_t kMmaSleepNs = 256;
 constexpr int kEpilogueFirstThread = 2 * 32;  // warps 2..5
 constexpr int kEpilogueThreads = 4 * 32;
