@@ -74,200 +74,206 @@ struct MlpDev {
   int n_layers;
   int x_shared;
   int act;
-  int p;        // individuals per group (<= kAcc / NB)
+  int x_bf16;   // x is bf16 (else fp32)
   int buf_len;  // floats per (individual, batch row) in an activation buffer, a multiple of 8
   float sigma;
 };
 
 // Eight weights of row j from column k (zeros outside the matrix).
-__device__ __forceinline__ void load_w8(const MlpLayerDev& L, int j, int k, float (&w)[8]) {
-  if (j < L.out && k < L.in) {
-    const float* src = L.w + static_cast<int64_t>(j) * L.in + k;
-    if (L.w_vec) {
+__device__ __forceinline__ void load_w8(const float* w, int in, int out, bool vec, int j, int k,
+                                        float (&v)[8]) {
+  if (j < out && k < in) {
+    const float* src = w + static_cast<int64_t>(j) * in + k;
+    if (vec) {
       const float4 a = __ldg(reinterpret_cast<const float4*>(src));
       const float4 b = __ldg(reinterpret_cast<const float4*>(src) + 1);
-      w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
-      w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+      v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+      v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
     } else {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) w[e] = (k + e < L.in) ? __ldg(src + e) : 0.f;
+      for (int e = 0; e < 8; ++e) v[e] = (k + e < in) ? __ldg(src + e) : 0.f;
     }
   } else {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) w[e] = 0.f;
+    for (int e = 0; e < 8; ++e) v[e] = 0.f;
   }
 }
 
-template <int NB, bool kXBf16>
+// CTA c runs individuals [c*kP, c*kP + kP) through every layer. The group size
+// kP is a compile-time constant so that the kP x 8 hashes of a chunk are
+// straight-line code the compiler can interleave; a CTA at the end of the
+// population with fewer individuals hashes its last one again in the empty
+// slots (the same wall time: the other CTAs have a full group) and stores
+// nothing for them.
+template <int NB, int kP>
 __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant__ MlpDev a) {
-  constexpr int kP = kAcc / NB;  // individuals per group, compile-time bound
   extern __shared__ float4 smem4[];
   float* smem = reinterpret_cast<float*>(smem4);
-  uint2* s_seed = reinterpret_cast<uint2*>(smem);                 // [P]
-  const int P = a.p;
+  uint2* s_seed = reinterpret_cast<uint2*>(smem);                 // [kP]
   const int blen = a.buf_len;
-  // Two activation buffers [P][NB][blen], `bstride` floats apart.
+  // Two activation buffers [kP][NB][blen], `bstride` floats apart.
   float* const s_buf0 = smem + kSeedFloats;
-  const int bstride = P * NB * blen;
+  const int bstride = kP * NB * blen;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const float sigma = a.sigma;
   const float shift = -1.5f * sigma;
-  const int64_t i_begin = a.pop * blockIdx.x / gridDim.x;
-  const int64_t i_end = a.pop * (blockIdx.x + 1) / gridDim.x;
+  const int64_t ib = static_cast<int64_t>(blockIdx.x) * kP;
+  const int np = static_cast<int>(min(static_cast<int64_t>(kP), a.pop - ib));
 
-  for (int64_t ib = i_begin; ib < i_end; ib += P) {
-    const int np = static_cast<int>(min(static_cast<int64_t>(P), i_end - ib));
-    __syncthreads();  // the previous group is done with the seeds and buffers
-    for (int t = threadIdx.x; t < np; t += kThreads) {
-      const uint64_t s = static_cast<uint64_t>(a.seeds[ib + t]);
-      s_seed[t] = make_uint2(static_cast<uint32_t>(s), static_cast<uint32_t>(s >> 32));
-    }
-    // Stage x: zero past `in`, for batch rows >= batch and for missing individuals.
-    {
-      const int in0 = a.layer[0].in;
-      const int per = NB * blen;
-      for (int t = threadIdx.x; t < P * per; t += kThreads) {
-        const int ii = t / per;
-        const int rem = t - ii * per;
-        const int r = rem / blen;
-        const int k = rem - r * blen;
-        float v = 0.f;
-        if (ii < np && r < a.batch && k < in0) {
-          const int64_t row = (a.x_shared ? 0 : (ib + ii) * a.batch) + r;
-          if constexpr (kXBf16)
-            v = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(a.x)[row * in0 + k]);
-          else
-            v = reinterpret_cast<const float*>(a.x)[row * in0 + k];
-        }
-        s_buf0[t] = v;
+  for (int t = threadIdx.x; t < kP; t += kThreads) {
+    const uint64_t s = static_cast<uint64_t>(a.seeds[ib + min(t, np - 1)]);
+    s_seed[t] = make_uint2(static_cast<uint32_t>(s), static_cast<uint32_t>(s >> 32));
+  }
+  // Stage x: zero past `in`, for batch rows >= batch and for the empty slots.
+  {
+    const int in0 = a.layer[0].in;
+    const int per = NB * blen;
+    const bool xb = a.x_bf16 != 0;
+    for (int t = threadIdx.x; t < kP * per; t += kThreads) {
+      const int ii = t / per;
+      const int rem = t - ii * per;
+      const int r = rem / blen;
+      const int k = rem - r * blen;
+      float v = 0.f;
+      if (ii < np && r < a.batch && k < in0) {
+        const int64_t row = (a.x_shared ? 0 : (ib + ii) * a.batch) + r;
+        v = xb ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(a.x)[row * in0 + k])
+               : reinterpret_cast<const float*>(a.x)[row * in0 + k];
       }
+      s_buf0[t] = v;
     }
-    __syncthreads();
+  }
+  __syncthreads();
 
-    for (int l = 0; l < a.n_layers; ++l) {
-      const MlpLayerDev& L = a.layer[l];
-      const float* src = s_buf0 + (l & 1) * bstride;
-      float* dst = s_buf0 + ((l & 1) ^ 1) * bstride;
-      const bool last = l + 1 == a.n_layers;
-      const int LR = 1 << L.lr_log2;
-      const int q = lane & (LR - 1);         // lane within its row group
-      const int rsub = lane >> L.lr_log2;    // row of this lane within the warp's group
-      const int rows_per_group = 32 >> L.lr_log2;
-      const int n_rg = (L.out + rows_per_group - 1) / rows_per_group;
-      const int my_rg = n_rg > warp ? (n_rg - warp + kWarps - 1) / kWarps : 0;
-      const int cpl = L.cpl;
-      const int steps = my_rg * cpl;
-      const uint64_t bias_base =
-          L.offset + static_cast<uint64_t>(L.out) * static_cast<uint64_t>(L.in);
+  for (int l = 0; l < a.n_layers; ++l) {
+    // The layer's parameters, read once into registers.
+    const float* const Lw = a.layer[l].w;
+    const float* const Lb = a.layer[l].b;
+    const uint64_t Loff = a.layer[l].offset;
+    const int Lin = a.layer[l].in;
+    const int Lout = a.layer[l].out;
+    const int lr_log2 = a.layer[l].lr_log2;
+    const int cpl = a.layer[l].cpl;
+    const bool wvec = a.layer[l].w_vec != 0;
+    const float* src = s_buf0 + (l & 1) * bstride;
+    float* dst = s_buf0 + ((l & 1) ^ 1) * bstride;
+    const bool last = l + 1 == a.n_layers;
+    const bool tanh_act = !last && a.act == VN_ACT_TANH;
+    const int LR = 1 << lr_log2;
+    const int q = lane & (LR - 1);         // lane within its row group
+    const int rsub = lane >> lr_log2;      // row of this lane within the warp's group
+    const int rows_per_group = 32 >> lr_log2;
+    const int n_rg = (Lout + rows_per_group - 1) / rows_per_group;
+    const int my_rg = n_rg > warp ? (n_rg - warp + kWarps - 1) / kWarps : 0;
+    const int steps = my_rg * cpl;
+    const uint64_t bias_base = Loff + static_cast<uint64_t>(Lout) * static_cast<uint64_t>(Lin);
 
-      float part[kP][NB];
-      float wn[8];
-      if (steps > 0) load_w8(L, warp * rows_per_group + rsub, q * 8, wn);
-      for (int s = 0, rgi = 0, m = 0; s < steps; ++s) {
-        const int j = (warp + rgi * kWarps) * rows_per_group + rsub;
-        const int k = (q + (m << L.lr_log2)) * 8;
-        if (m == 0) {
+    float part[kP][NB];
+    float wn[8];
+    if (steps > 0) load_w8(Lw, Lin, Lout, wvec, warp * rows_per_group + rsub, q * 8, wn);
+    for (int s = 0, rgi = 0, m = 0; s < steps; ++s) {
+      const int j = (warp + rgi * kWarps) * rows_per_group + rsub;
+      const int k = (q + (m << lr_log2)) * 8;
+      if (m == 0) {
+#pragma unroll
+        for (int ii = 0; ii < kP; ++ii)
+#pragma unroll
+          for (int r = 0; r < NB; ++r) part[ii][r] = 0.f;
+      }
+      float wm[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) wm[e] = wn[e] + shift;
+      // The next step's chunk: the same row's next one, or the next row group's first.
+      const int m1 = (m + 1 < cpl) ? m + 1 : 0;
+      const int rgi1 = (m + 1 < cpl) ? rgi : rgi + 1;
+      if (s + 1 < steps)
+        load_w8(Lw, Lin, Lout, wvec, (warp + rgi1 * kWarps) * rows_per_group + rsub,
+                (q + (m1 << lr_log2)) * 8, wn);
+      const uint64_t bst = index_term(Loff + static_cast<uint64_t>(j) * static_cast<uint64_t>(Lin) +
+                                      static_cast<uint64_t>(k));
+      const float* hk = src + k;
+#pragma unroll
+      for (int ii = 0; ii < kP; ++ii) {
+        const uint2 sd = s_seed[ii];
+        uint64_t st = bst + ((static_cast<uint64_t>(sd.y) << 32) | sd.x);
+        float wp[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          wp[e] = fmaf(sigma, __uint_as_float(mix_to_one_plus_u(st)), wm[e]);
+          st += kGamma;
+        }
+#pragma unroll
+        for (int r = 0; r < NB; ++r) {
+          const float4* h = reinterpret_cast<const float4*>(hk + (ii * NB + r) * blen);
+          const float4 xa = h[0], xb = h[1];
+          float acc = part[ii][r];
+          acc = fmaf(xa.x, wp[0], acc);
+          acc = fmaf(xa.y, wp[1], acc);
+          acc = fmaf(xa.z, wp[2], acc);
+          acc = fmaf(xa.w, wp[3], acc);
+          acc = fmaf(xb.x, wp[4], acc);
+          acc = fmaf(xb.y, wp[5], acc);
+          acc = fmaf(xb.z, wp[6], acc);
+          acc = fmaf(xb.w, wp[7], acc);
+          part[ii][r] = acc;
+        }
+      }
+      if (m + 1 == cpl) {
+        // Sum the row's LR partials (every lane of the group ends with the total).
+        for (int o = LR >> 1; o > 0; o >>= 1) {
 #pragma unroll
           for (int ii = 0; ii < kP; ++ii)
 #pragma unroll
-            for (int r = 0; r < NB; ++r) part[ii][r] = 0.f;
+            for (int r = 0; r < NB; ++r)
+              part[ii][r] += __shfl_xor_sync(0xffffffffu, part[ii][r], o);
         }
-        float wm[8];
+        if (j < Lout) {
+          const float bj = Lb != nullptr ? __ldg(Lb + j) : 0.f;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) wm[e] = wn[e] + shift;
-        // The next step's chunk: the same row's next one, or the next row group's first.
-        const int m1 = (m + 1 < cpl) ? m + 1 : 0;
-        const int rgi1 = (m + 1 < cpl) ? rgi : rgi + 1;
-        if (s + 1 < steps)
-          load_w8(L, (warp + rgi1 * kWarps) * rows_per_group + rsub, (q + (m1 << L.lr_log2)) * 8, wn);
-        const uint64_t bst = index_term(L.offset +
-                                        static_cast<uint64_t>(j) * static_cast<uint64_t>(L.in) +
-                                        static_cast<uint64_t>(k));
-#pragma unroll
-        for (int ii = 0; ii < kP; ++ii) {
-          if (ii < np) {
-            const uint2 sd = s_seed[ii];
-            uint64_t st = bst + ((static_cast<uint64_t>(sd.y) << 32) | sd.x);
-            float wp[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              wp[e] = fmaf(sigma, __uint_as_float(mix_to_one_plus_u(st)), wm[e]);
-              st += kGamma;
-            }
+          for (int ii = 0; ii < kP; ++ii) {
 #pragma unroll
             for (int r = 0; r < NB; ++r) {
-              const float4* h = reinterpret_cast<const float4*>(src + (ii * NB + r) * blen + k);
-              const float4 xa = h[0], xb = h[1];
-              float acc = part[ii][r];
-              acc = fmaf(xa.x, wp[0], acc);
-              acc = fmaf(xa.y, wp[1], acc);
-              acc = fmaf(xa.z, wp[2], acc);
-              acc = fmaf(xa.w, wp[3], acc);
-              acc = fmaf(xb.x, wp[4], acc);
-              acc = fmaf(xb.y, wp[5], acc);
-              acc = fmaf(xb.z, wp[6], acc);
-              acc = fmaf(xb.w, wp[7], acc);
-              part[ii][r] = acc;
-            }
-          }
-        }
-        if (m + 1 == cpl) {
-          // Sum the row's LR partials (every lane of the group ends with the total).
-          for (int o = LR >> 1; o > 0; o >>= 1) {
-#pragma unroll
-            for (int ii = 0; ii < kP; ++ii)
-#pragma unroll
-              for (int r = 0; r < NB; ++r)
-                part[ii][r] += __shfl_xor_sync(0xffffffffu, part[ii][r], o);
-          }
-          if (j < L.out) {
-            const float bj = L.b != nullptr ? __ldg(L.b + j) : 0.f;
-#pragma unroll
-            for (int ii = 0; ii < kP; ++ii) {
-#pragma unroll
-              for (int r = 0; r < NB; ++r) {
-                if (ii < np && ((ii * NB + r) & (LR - 1)) == q) {
-                  float v = part[ii][r];
-                  if (L.b != nullptr) {
-                    const uint2 sd = s_seed[ii];
-                    const uint64_t seed = (static_cast<uint64_t>(sd.y) << 32) | sd.x;
-                    v += fmaf(sigma, noise_at(seed, bias_base + static_cast<uint64_t>(j)), bj);
-                  }
-                  if (!last && a.act == VN_ACT_TANH) v = tanhf(v);
-                  dst[(ii * NB + r) * blen + j] = v;
+              if (((ii * NB + r) & (LR - 1)) == q) {
+                float v = part[ii][r];
+                if (Lb != nullptr) {
+                  const uint2 sd = s_seed[ii];
+                  const uint64_t seed = (static_cast<uint64_t>(sd.y) << 32) | sd.x;
+                  v += fmaf(sigma, noise_at(seed, bias_base + static_cast<uint64_t>(j)), bj);
                 }
+                if (tanh_act) v = tanhf(v);
+                dst[(ii * NB + r) * blen + j] = v;
               }
             }
           }
         }
-        if (++m == cpl) { m = 0; ++rgi; }
       }
-      // dst must read as zeros on [out, next layer's in_pad).
-      if (!last) {
-        const int pad = a.layer[l + 1].in_pad - L.out;
-        if (pad > 0) {
-          for (int t = threadIdx.x; t < P * NB * pad; t += kThreads) {
-            const int row = t / pad;
-            dst[row * blen + L.out + (t - row * pad)] = 0.f;
-          }
+      if (++m == cpl) { m = 0; ++rgi; }
+    }
+    // dst must read as zeros on [out, next layer's in_pad).
+    if (!last) {
+      const int pad = a.layer[l + 1].in_pad - Lout;
+      if (pad > 0) {
+        for (int t = threadIdx.x; t < kP * NB * pad; t += kThreads) {
+          const int row = t / pad;
+          dst[row * blen + Lout + (t - row * pad)] = 0.f;
         }
       }
-      __syncthreads();
     }
+    __syncthreads();
+  }
 
-    // y[i, r, j] from the last layer's buffer.
-    const float* fin = s_buf0 + (a.n_layers & 1) * bstride;
-    const int outl = a.layer[a.n_layers - 1].out;
-    const int per = a.batch * outl;
-    for (int t = threadIdx.x; t < np * per; t += kThreads) {
-      const int ii = t / per;
-      const int rem = t - ii * per;
-      const int r = rem / outl;
-      const int j = rem - r * outl;
-      a.y[(ib + ii) * per + rem] = fin[(ii * NB + r) * blen + j];
-    }
+  // y[i, r, j] from the last layer's buffer.
+  const float* fin = s_buf0 + (a.n_layers & 1) * bstride;
+  const int outl = a.layer[a.n_layers - 1].out;
+  const int per = a.batch * outl;
+  for (int t = threadIdx.x; t < np * per; t += kThreads) {
+    const int ii = t / per;
+    const int rem = t - ii * per;
+    const int r = rem / outl;
+    const int j = rem - r * outl;
+    a.y[(ib + ii) * per + rem] = fin[(ii * NB + r) * blen + j];
   }
 }
 
@@ -291,16 +297,9 @@ LayerShape layer_shape(int64_t in, int64_t out) {
   return sh;
 }
 
-template <int NB, bool kX>
-cudaError_t launch_typed(MlpDev& d, cudaStream_t stream, const DeviceInfo& dev) {
-  auto fn = mlp_kernel<NB, kX>;
-  constexpr int kP = kAcc / NB;
-  const size_t per_ind = 2ull * NB * static_cast<size_t>(d.buf_len) * sizeof(float);
-  const size_t base = kSeedFloats * sizeof(float);
-  const size_t budget = static_cast<size_t>(dev.smem_optin);
-  if (base + per_ind > budget) return cudaErrorInvalidValue;  // checked by the caller
-  d.p = static_cast<int>(std::min<size_t>(kP, (budget - base) / per_ind));
-  const size_t smem = base + static_cast<size_t>(d.p) * per_ind;
+template <int NB, int kP>
+cudaError_t launch_p(MlpDev& d, cudaStream_t stream, size_t smem) {
+  auto fn = mlp_kernel<NB, kP>;
   if (smem > 48 * 1024) {
     static size_t configured = 0;
     if (configured < smem) {
@@ -310,18 +309,48 @@ cudaError_t launch_typed(MlpDev& d, cudaStream_t stream, const DeviceInfo& dev) 
       configured = smem;
     }
   }
-  int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, kThreads, smem) != cudaSuccess ||
-      occ < 1)
-    occ = 1;
-  const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(d.pop, int64_t{dev.sm_count} * occ));
+  const int64_t grid = (d.pop + kP - 1) / kP;
   fn<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(d);
   return cudaGetLastError();
 }
 
+// Group size: enough individuals per CTA that one CTA per SM covers the
+// population (ceil(pop / SMs)), at most kAcc / NB, and no more than the shared
+// memory holds.
 template <int NB>
-cudaError_t launch_nb(MlpDev& d, bool xb, cudaStream_t stream, const DeviceInfo& dev) {
-  return xb ? launch_typed<NB, true>(d, stream, dev) : launch_typed<NB, false>(d, stream, dev);
+cudaError_t launch_nb(MlpDev& d, cudaStream_t stream, const DeviceInfo& dev) {
+  constexpr int kMaxP = kAcc / NB;
+  const size_t per_ind = 2ull * NB * static_cast<size_t>(d.buf_len) * sizeof(float);
+  const size_t base = kSeedFloats * sizeof(float);
+  const size_t budget = static_cast<size_t>(dev.smem_optin);
+  if (base + per_ind > budget) return cudaErrorInvalidValue;  // checked by the caller
+  int p = static_cast<int>(std::min<int64_t>(kMaxP, (d.pop + dev.sm_count - 1) / dev.sm_count));
+  p = static_cast<int>(std::min<size_t>(p, (budget - base) / per_ind));
+  p = std::max(p, 1);
+  const size_t smem = base + static_cast<size_t>(p) * per_ind;
+  if constexpr (NB == 1) {
+    switch (p) {
+      case 1: return launch_p<1, 1>(d, stream, smem);
+      case 2: return launch_p<1, 2>(d, stream, smem);
+      case 3: return launch_p<1, 3>(d, stream, smem);
+      case 4: return launch_p<1, 4>(d, stream, smem);
+      case 5: return launch_p<1, 5>(d, stream, smem);
+      case 6: return launch_p<1, 6>(d, stream, smem);
+      case 7: return launch_p<1, 7>(d, stream, smem);
+      default: return launch_p<1, 8>(d, stream, smem);
+    }
+  } else if constexpr (NB == 2) {
+    switch (p) {
+      case 1: return launch_p<2, 1>(d, stream, smem);
+      case 2: return launch_p<2, 2>(d, stream, smem);
+      case 3: return launch_p<2, 3>(d, stream, smem);
+      default: return launch_p<2, 4>(d, stream, smem);
+    }
+  } else if constexpr (NB == 4) {
+    return p == 1 ? launch_p<4, 1>(d, stream, smem) : launch_p<4, 2>(d, stream, smem);
+  } else {
+    return launch_p<8, 1>(d, stream, smem);
+  }
 }
 
 }  // namespace
@@ -363,11 +392,11 @@ cudaError_t launch_mlp(const MlpArgs& m, cudaStream_t stream) {
   d.act = m.act;
   d.buf_len = static_cast<int>(mlp_buffer_floats(m.n_layers, m.dims));
   d.sigma = m.sigma;
-  const bool xb = m.x_dt == VN_BF16;
-  if (m.batch <= 1) return launch_nb<1>(d, xb, stream, dev);
-  if (m.batch <= 2) return launch_nb<2>(d, xb, stream, dev);
-  if (m.batch <= 4) return launch_nb<4>(d, xb, stream, dev);
-  return launch_nb<8>(d, xb, stream, dev);
+  d.x_bf16 = m.x_dt == VN_BF16 ? 1 : 0;
+  if (m.batch <= 1) return launch_nb<1>(d, stream, dev);
+  if (m.batch <= 2) return launch_nb<2>(d, stream, dev);
+  if (m.batch <= 4) return launch_nb<4>(d, stream, dev);
+  return launch_nb<8>(d, stream, dev);
 }
 
 }  // namespace vn
