@@ -6,9 +6,11 @@ with tanh, fp32, sigma 0.02, centered-rank fitness). One step is one pass of the
 whole hot path over one population:
   * forward: the three perturbed linears in one launch (vn_perturbed_mlp: the
     activations stay on chip, tanh between layers),
+  * fitness shaping: the centered ranks of the population's returns,
   * gradients: grad_W and grad_b of all three layers; the six blocks are laid
     out by compute_offsets one after another, so they are one flat range of
     element indices and one reduction over the population computes them all,
+  * update: the flat parameter vector (the layers are views of it) += lr * grad,
   * noise dump: the centered-uniform noise of the whole flat parameter vector
     (84,488 elements) for every individual,
 so each step regenerates the population's parameter noise three times.
@@ -62,6 +64,7 @@ SM_CLOCK_MAX_HZ = 2.07e9
 ALU_LANES_PER_SM = 64             # integer ALU pipe: 16 lanes per scheduler, 4 schedulers
 ISSUE_LANES_PER_SM = 128          # 4 schedulers x 32 lanes, one instruction per clock each
 L2_FLUSH_BYTES = 256 << 20
+ES_LR = 0.01                      # learning rate of the bench's parameter update
 
 
 def peaks():
@@ -116,22 +119,37 @@ def build_step(wl, dev, stream_ptr):
     P = ctypes.c_void_p
     s = P(stream_ptr)
     d = wl.to(dev)
-    bufs = {"seeds": d.seeds, "fitness": d.fitness}
+    bufs = {"seeds": d.seeds}
     launches = []
     outputs = []
     pop, batch = wl.pop, wl.batch
     dt = {torch.float32: _lib.VN_F32, torch.bfloat16: _lib.VN_BF16}
+    n_params = sum(l.out_f * l.in_f + l.out_f for l in wl.layers)
+    flat = wl.grads and len(wl.layers) > 1 and contiguous_blocks(wl)
 
     fused = (wl.forward and len(d.layers) > 1 and batch <= 8 and d.x.dtype in (torch.float32, torch.bfloat16)
              and all(l.weight.dtype == torch.float32 and l.bias.dtype == torch.float32 for l in d.layers))
+    theta = None
+    if fused and flat:
+        # One flat parameter vector (W_0, b_0, W_1, b_1, ... as compute_offsets lays
+        # them out); the layers are views of it, so the update is one launch.
+        theta = torch.cat([t.reshape(-1) for l in d.layers for t in (l.weight, l.bias)]).contiguous()
+        pos = 0
+        for l in d.layers:
+            l.weight = theta[pos:pos + l.out_f * l.in_f].view(l.out_f, l.in_f)
+            pos += l.out_f * l.in_f
+            l.bias = theta[pos:pos + l.out_f]
+            pos += l.out_f
+        bufs["theta"] = theta
     if fused:
         # A policy (several fp32 layers, small batch): every layer in one launch,
         # the activations kept on chip (vn_perturbed_mlp).
         bufs["x"] = d.x
         n = len(d.layers)
         dims = [d.layers[0].in_f] + [l.out_f for l in d.layers]
-        for li, l in enumerate(d.layers):
-            bufs[f"w{li}"], bufs[f"b{li}"] = l.weight, l.bias
+        if theta is None:
+            for li, l in enumerate(d.layers):
+                bufs[f"w{li}"], bufs[f"b{li}"] = l.weight, l.bias
         y = torch.empty((pop, batch, dims[-1]), dtype=torch.float32, device=dev)
         c_dims = (ctypes.c_int64 * (n + 1))(*dims)
         c_w = (ctypes.c_void_p * n)(*[l.weight.data_ptr() for l in d.layers])
@@ -168,8 +186,17 @@ def build_step(wl, dev, stream_ptr):
             h = y
         outputs.append(h)
 
-    n_params = sum(l.out_f * l.in_f + l.out_f for l in wl.layers)
-    flat = wl.grads and len(wl.layers) > 1 and contiguous_blocks(wl)
+    # Fitness shaping: the returns' centered ranks, computed on the device, feed
+    # the gradient (workloads whose fitness is given as-is use it directly).
+    fit = d.fitness
+    if wl.grads and d.returns is not None:
+        bufs["returns"] = d.returns
+        fit = torch.empty_like(d.returns)
+        launches.append(Launch("es_ranks", lib.vn_centered_ranks,
+                               (P(d.returns.data_ptr()), pop, P(fit.data_ptr()), s), 0,
+                               hbm_bytes=pop * 8))
+    elif wl.grads:
+        bufs["fitness"] = d.fitness
     if flat:
         # The blocks (weights then bias, layer by layer) are laid out by
         # compute_offsets, so the gradients of all of them are one flat range of
@@ -177,21 +204,27 @@ def build_step(wl, dev, stream_ptr):
         # gradient as a slice (grad_W of layer l = flat[off_l : off_l + out*in]).
         g = torch.empty((n_params,), dtype=torch.float32, device=dev)
         launches.append(Launch("grad", lib.vn_bias_gradient,
-                               (P(d.fitness.data_ptr()), P(d.seeds.data_ptr()), pop, n_params,
+                               (P(fit.data_ptr()), P(d.seeds.data_ptr()), pop, n_params,
                                 float(wl.sigma), wl.layers[0].offset, P(g.data_ptr()), s),
                                pop * n_params, hbm_bytes=g.numel() * 4, grad_w_elems=sum(
                                    l.out_f * l.in_f for l in wl.layers)))
         outputs.append(g)
+        if theta is not None:
+            # The ES step on the parameters: theta += lr * grad (lr fixed for the bench).
+            launches.append(Launch("es_update", lib.vn_es_update,
+                                   (P(theta.data_ptr()), P(g.data_ptr()), n_params, ES_LR, s), 0,
+                                   hbm_bytes=n_params * 12))
+            outputs.append(theta)
     for li, l in enumerate(d.layers if (wl.grads and not flat) else []):
         gw = torch.empty((l.out_f, l.in_f), dtype=torch.float32, device=dev)
         gb = torch.empty((l.out_f,), dtype=torch.float32, device=dev)
         launches.append(Launch("grad", lib.vn_weight_gradient,
-                               (P(d.fitness.data_ptr()), P(d.seeds.data_ptr()), pop, l.out_f, l.in_f,
+                               (P(fit.data_ptr()), P(d.seeds.data_ptr()), pop, l.out_f, l.in_f,
                                 float(wl.sigma), l.offset, P(gw.data_ptr()), s),
                                pop * l.out_f * l.in_f, hbm_bytes=gw.numel() * 4,
                                grad_w_elems=l.out_f * l.in_f))
         launches.append(Launch("grad", lib.vn_bias_gradient,
-                               (P(d.fitness.data_ptr()), P(d.seeds.data_ptr()), pop, l.out_f,
+                               (P(fit.data_ptr()), P(d.seeds.data_ptr()), pop, l.out_f,
                                 float(wl.sigma), l.offset + l.out_f * l.in_f, P(gb.data_ptr()), s),
                                pop * l.out_f, hbm_bytes=gb.numel() * 4))
         outputs += [gw, gb]
@@ -315,14 +348,18 @@ def traffic_for(kernel: str, workload: str):
 
 def oracle_step(wl, individuals: int) -> int:
     """The oracle's pass over the first ``individuals`` of the population: forward,
-    the gradients' sums over those individuals, and their noise dump. Returns the
-    noise elements regenerated."""
+    the centered ranks of the returns (over the whole population: a rank is global),
+    the gradients' sums over those individuals, the parameter update and their noise
+    dump. Returns the noise elements regenerated."""
     import numpy as np
     from oracle import es
 
     s = slice(0, individuals)
     seeds = wl.seeds[s].numpy()
-    fit = wl.fitness[s].numpy()
+    if wl.grads and wl.returns is not None:
+        fit = es.centered_ranks(wl.returns.numpy())[s]
+    else:
+        fit = wl.fitness[s].numpy()
     n = 0
     if wl.forward:
         h = wl.x[s].float().numpy().astype(np.float64)
@@ -332,8 +369,11 @@ def oracle_step(wl, individuals: int) -> int:
                 h = np.tanh(h)
             n += individuals * l.out_f * l.in_f
     for l in (wl.layers if wl.grads else []):
-        es.weight_gradient(fit, seeds, (l.out_f, l.in_f), wl.sigma, individuals, l.offset)
-        es.bias_gradient(fit, seeds, (l.out_f,), wl.sigma, individuals, l.offset + l.out_f * l.in_f)
+        gw = es.weight_gradient(fit, seeds, (l.out_f, l.in_f), wl.sigma, individuals, l.offset)
+        gb = es.bias_gradient(fit, seeds, (l.out_f,), wl.sigma, individuals, l.offset + l.out_f * l.in_f)
+        if wl.forward and len(wl.layers) > 1:
+            es.es_update(l.weight.float().numpy(), gw, ES_LR)
+            es.es_update(l.bias.float().numpy(), gb, ES_LR)
         n += individuals * (l.out_f * l.in_f + l.out_f)
     if wl.number in (1, 2):
         n_params = sum(l.out_f * l.in_f + l.out_f for l in wl.layers)

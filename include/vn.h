@@ -186,6 +186,29 @@ vn_status vn_perturbed_mlp(const void* x, vn_dtype x_dt, int x_shared,
                            const int64_t* seeds, int64_t pop, int64_t batch,
                            double sigma, vn_act act, float* y, void* stream);
 
+/*
+ * vn_centered_ranks -- fitness shaping by centered ranks, the "fitness =
+ * centered ranks in [-0.5, 0.5]" of the ES policy workload (the page's
+ * gradient entries take the shaped fitness as given):
+ *     out[i] = rank_i / (pop - 1) - 0.5      (out[0] = -0.5 when pop == 1)
+ * rank_i = number of j with fitness[j] < fitness[i], plus the number of j < i
+ * with an equal value: ascending order, ties by index. The comparison is a
+ * total order on the float bit patterns (-0 below +0; NaNs beyond the
+ * infinities on their sign's side), so out is always a permutation of
+ * {r / (pop - 1) - 0.5}. fitness and out are fp32 [pop], 4-byte aligned, and
+ * must not overlap. 0 <= pop < 2^31. The work is pop^2 comparisons.
+ */
+vn_status vn_centered_ranks(const float* fitness, int64_t pop, float* out, void* stream);
+
+/*
+ * vn_es_update -- the ES parameter step on a flat parameter vector:
+ *     theta[k] = fma(lr, grad[k], theta[k]),  k < n   (fp32, in place)
+ * With grad from vn_weight_gradient / vn_bias_gradient over the blocks laid out
+ * by compute_offsets, lr > 0 ascends the fitness. lr finite; theta and grad
+ * fp32, 4-byte aligned (16-byte alignment of both takes a vector path).
+ */
+vn_status vn_es_update(float* theta, const float* grad, int64_t n, double lr, void* stream);
+
 /* Synchronises `stream`, then reads and clears the current device's status
  * word: VN_ERR_TIMEOUT if a kernel of this library recorded an expired wait
  * since the last call, VN_ERR_CUDA if synchronisation failed, else VN_OK. */

@@ -161,3 +161,35 @@ def reduce_metric(center, seeds, sigma: float, n_params: int, offset: int = 0,
     for r, i in enumerate(inds):
         out[r] = np.mean(np.abs(c + sigma * noise_np(s[i], idx)))
     return out
+
+
+def order_keys(values) -> np.ndarray:
+    """A total order on float32 values as unsigned keys: negative below positive,
+    -0 below +0, NaNs beyond the infinities on their sign's side. For a set sign bit
+    the key is the complement of the bits (larger magnitude -> smaller key); for a
+    clear one the bits with the sign bit set."""
+    b = np.asarray(values, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    neg = (b >> np.uint64(31)) == np.uint64(1)
+    return np.where(neg, np.uint64(0xFFFFFFFF) - b, b | np.uint64(0x80000000))
+
+
+def centered_ranks(fitness) -> np.ndarray:
+    """Fitness shaping of the ES workloads ("centered ranks in [-0.5, 0.5]"):
+    rank_i = #{j : f_j < f_i} + #{j < i : f_j == f_i} (ascending, ties by index),
+    out_i = rank_i / (pop - 1) - 0.5, the division and subtraction in float32.
+    Counted one element at a time against the whole population."""
+    k = order_keys(fitness)
+    pop = k.shape[0]
+    idx = np.arange(pop)
+    rank = np.empty(pop, dtype=np.int64)
+    for i in range(pop):
+        rank[i] = int(np.count_nonzero(k < k[i])) + int(np.count_nonzero((k == k[i]) & (idx < i)))
+    denom = np.float32(max(pop - 1, 1))
+    return rank.astype(np.float32) / denom - np.float32(0.5)
+
+
+def es_update(theta, grad, lr: float) -> np.ndarray:
+    """The ES parameter step theta + lr * grad, in float64 from the float32 inputs
+    (lr taken as its float32 value, as the library receives it)."""
+    lr32 = float(np.float32(lr))
+    return np.asarray(theta, dtype=np.float64) + lr32 * np.asarray(grad, dtype=np.float64)

@@ -128,3 +128,18 @@ def test_mlp_validation_refuses_before_launch(lib):
     assert call(pop=1 << 40, batch=8, dims=(4, 8, 1 << 30)) == 6
     assert call(pop=0, s=0, y=0, x=0) == 0        # empty output: valid, nothing launched
     assert call(dims=(4, 8, 0), y=0) == 0
+
+
+def test_ranks_and_update_validation(lib):
+    fake = 0x1000
+    assert lib.vn_centered_ranks(P(fake), -1, P(fake + 64), P(0)) == 2          # negative pop
+    assert lib.vn_centered_ranks(P(fake), 1 << 31, P(fake + 64), P(0)) == 2     # pop >= 2^31
+    assert lib.vn_centered_ranks(P(0), 0, P(0), P(0)) == 0                      # empty: nothing launched
+    assert lib.vn_centered_ranks(P(0), 4, P(fake), P(0)) == 1
+    assert lib.vn_centered_ranks(P(fake + 2), 4, P(fake + 64), P(0)) == 5
+    assert lib.vn_centered_ranks(P(fake), 4, P(fake + 8), P(0)) == 4            # overlapping in/out
+    assert lib.vn_es_update(P(fake), P(fake), -1, 0.1, P(0)) == 2
+    assert lib.vn_es_update(P(fake), P(fake), 4, float("inf"), P(0)) == 4
+    assert lib.vn_es_update(P(0), P(0), 0, 0.1, P(0)) == 0
+    assert lib.vn_es_update(P(0), P(fake), 4, 0.1, P(0)) == 1
+    assert lib.vn_es_update(P(fake), P(fake + 1), 4, 0.1, P(0)) == 5

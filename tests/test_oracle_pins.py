@@ -362,3 +362,43 @@ def test_reduce_metric_special_cases_and_brute_force():
     for i, s in enumerate(seeds.tolist()):
         want = sum(abs(center[k] + 0.3 * sm.noise(s, 7 + k)) for k in range(50)) / 50
         assert abs(got[i] - want) < 1e-13
+
+
+# ---------------------------------------------------------------------------
+# Centered ranks and the parameter update
+# ---------------------------------------------------------------------------
+
+def test_centered_ranks_hand_worked_example():
+    # ascending order: -1.0 (index 1), 0.3 (index 0), 0.3 (index 2, after the
+    # equal value at the lower index), 2.0 (index 3) -> ranks 1, 0, 2, 3
+    got = es.centered_ranks(np.array([0.3, -1.0, 0.3, 2.0], dtype=np.float32))
+    want = np.array([1, 0, 2, 3], dtype=np.float32) / np.float32(3) - np.float32(0.5)
+    assert got.dtype == np.float32 and np.array_equal(got, want)
+    assert np.array_equal(es.centered_ranks(np.array([7.0], dtype=np.float32)), np.float32([-0.5]))
+
+
+def test_centered_ranks_special_values_order():
+    vals = np.array([np.nan, -np.nan, np.inf, -np.inf, 0.0, -0.0], dtype=np.float32)
+    assert np.signbit(vals[1]) and not np.signbit(vals[0])
+    # -NaN < -inf < -0 < +0 < +inf < +NaN
+    want = np.array([5, 0, 4, 1, 3, 2], dtype=np.float32) / np.float32(5) - np.float32(0.5)
+    assert np.array_equal(es.centered_ranks(vals), want)
+
+
+def test_centered_ranks_match_a_stable_sort_and_are_a_permutation():
+    rng = np.random.default_rng(23)
+    f = rng.integers(-20, 20, size=300).astype(np.float32) * np.float32(0.25)  # many ties
+    got = es.centered_ranks(f)
+    order = np.argsort(f, kind="stable")           # an independent route to the ranks
+    rank = np.empty(300, dtype=np.int64)
+    rank[order] = np.arange(300)
+    assert np.array_equal(got, rank.astype(np.float32) / np.float32(299) - np.float32(0.5))
+    assert np.array_equal(np.sort(got), np.arange(300, dtype=np.float32) / np.float32(299) - np.float32(0.5))
+
+
+def test_es_update_is_theta_plus_lr_grad():
+    theta = np.array([1.0, -2.0, 0.5], dtype=np.float32)
+    grad = np.array([2.0, 4.0, -1.0], dtype=np.float32)
+    assert np.array_equal(es.es_update(theta, grad, 0.5), np.array([2.0, 0.0, 0.0]))
+    # lr is used at float32 precision, as the library receives it
+    assert es.es_update(np.zeros(1, np.float32), np.ones(1, np.float32), 0.1)[0] == float(np.float32(0.1))

@@ -10,8 +10,10 @@ and never materialised.
 
 from .api import (  # noqa: F401
     VNError,
+    centered_ranks,
     compute_offsets,
     device_status,
+    es_update,
     noise_dump,
     perturbed_linear_path,
     virtual_bias_gradient,
@@ -23,7 +25,7 @@ from .api import (  # noqa: F401
 )
 
 __all__ = [
-    "VNError", "compute_offsets", "device_status", "noise_dump", "perturbed_linear_path",
+    "VNError", "centered_ranks", "compute_offsets", "device_status", "es_update", "noise_dump", "perturbed_linear_path",
     "virtual_bias_gradient", "virtual_flat_gradient", "virtual_perturbed_linear", "virtual_perturbed_mlp",
     "virtual_reduce_metric",
     "virtual_weight_gradient",

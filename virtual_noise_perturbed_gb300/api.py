@@ -246,6 +246,33 @@ def virtual_reduce_metric(center: torch.Tensor, seeds: torch.Tensor, sigma: floa
     return f
 
 
+def centered_ranks(fitness: torch.Tensor, *, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Fitness shaping: rank (ascending, ties by index) / (pop - 1) - 0.5, float32 (pop,)."""
+    lib = load()
+    fitness = _cuda(fitness, "fitness").reshape(-1).to(torch.float32)
+    pop = fitness.numel()
+    if out is None:
+        out = torch.empty(pop, dtype=torch.float32, device=fitness.device)
+    elif out.shape != (pop,) or out.dtype != torch.float32 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous float32 tensor of shape (pop,)")
+    check(lib.vn_centered_ranks(_ptr(fitness), pop, _ptr(out), _stream(fitness)), "vn_centered_ranks")
+    return out
+
+
+def es_update(theta: torch.Tensor, grad: torch.Tensor, lr: float) -> torch.Tensor:
+    """theta += lr * grad in place (float32, contiguous, same number of elements); returns theta."""
+    lib = load()
+    if not isinstance(theta, torch.Tensor) or not theta.is_cuda or not theta.is_contiguous() \
+            or theta.dtype != torch.float32:
+        raise ValueError("theta must be a contiguous float32 CUDA tensor (updated in place)")
+    grad = _cuda(grad, "grad").to(torch.float32)
+    if grad.numel() != theta.numel():
+        raise ValueError("grad and theta differ in size")
+    check(lib.vn_es_update(_ptr(theta), _ptr(grad), theta.numel(), float(lr), _stream(theta)),
+          "vn_es_update")
+    return theta
+
+
 def compute_offsets(param_shapes: Sequence[Sequence[int]]) -> list:
     """Start offset of each parameter block: the element count of all blocks before it."""
     offsets, total = [], 0

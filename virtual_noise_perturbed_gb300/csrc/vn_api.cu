@@ -298,6 +298,27 @@ vn_status vn_perturbed_mlp(const void* x, vn_dtype x_dt, int x_shared, int64_t n
   return launched(vn::launch_mlp(m, static_cast<cudaStream_t>(stream)));
 }
 
+vn_status vn_centered_ranks(const float* fitness, int64_t pop, float* out, void* stream) {
+  if (pop < 0 || pop > (int64_t{1} << 31) - 1) return VN_ERR_SHAPE;
+  if (pop == 0) return VN_OK;
+  if (fitness == nullptr || out == nullptr) return VN_ERR_NULL;
+  if (!aligned(fitness, 4) || !aligned(out, 4)) return VN_ERR_ALIGN;
+  const uintptr_t f0 = reinterpret_cast<uintptr_t>(fitness), o0 = reinterpret_cast<uintptr_t>(out);
+  const uintptr_t bytes = static_cast<uintptr_t>(pop) * 4;
+  if (f0 < o0 + bytes && o0 < f0 + bytes) return VN_ERR_VALUE;  // in and out overlap
+  return launched(vn::launch_centered_ranks(fitness, pop, out, static_cast<cudaStream_t>(stream)));
+}
+
+vn_status vn_es_update(float* theta, const float* grad, int64_t n, double lr, void* stream) {
+  if (n < 0) return VN_ERR_SHAPE;
+  float lr_f;
+  if (!float_sigma(lr, &lr_f)) return VN_ERR_VALUE;
+  if (n == 0) return VN_OK;
+  if (theta == nullptr || grad == nullptr) return VN_ERR_NULL;
+  if (!aligned(theta, 4) || !aligned(grad, 4)) return VN_ERR_ALIGN;
+  return launched(vn::launch_es_update(theta, grad, n, lr_f, static_cast<cudaStream_t>(stream)));
+}
+
 vn_status vn_device_status(void* stream) {
   cudaError_t err = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (err != cudaSuccess) return cuda_failure(err);

@@ -92,6 +92,13 @@ inline size_t mlp_bytes_per_individual(int64_t batch, size_t buf_floats) {
 }
 cudaError_t launch_mlp(const MlpArgs& m, cudaStream_t stream);
 
+// out[i] = rank of fitness[i] (ascending, ties by index) / (pop - 1) - 0.5.
+cudaError_t launch_centered_ranks(const float* fitness, int64_t pop, float* out,
+                                  cudaStream_t stream);
+// theta[k] += lr * grad[k], k < n.
+cudaError_t launch_es_update(float* theta, const float* grad, int64_t n, float lr,
+                             cudaStream_t stream);
+
 // Reads and clears the device status word of the bounded-wait kernels (0 = fine).
 cudaError_t take_device_status(unsigned int* status, cudaStream_t stream);
 

@@ -44,12 +44,17 @@ class Workload:
     activation: Optional[str] = None   # between layers
     forward: bool = True               # the workload runs the forward
     grads: bool = True                 # the workload runs the gradient estimates
+    # Raw returns (pop,) fp32 for the workloads whose fitness is centered ranks: the
+    # full ES generation shapes them into ranks on the device. Drawn from a separate
+    # generator (seed 2000 + number), so the other tensors do not depend on them.
+    returns: Optional[torch.Tensor] = None
 
     def to(self, device) -> "Workload":
         d = dataclasses.replace(self)
         d.seeds = self.seeds.to(device)
         d.x = self.x.to(device)
         d.fitness = self.fitness.to(device)
+        d.returns = None if self.returns is None else self.returns.to(device)
         d.layers = [dataclasses.replace(l, weight=l.weight.to(device),
                                         bias=None if l.bias is None else l.bias.to(device))
                     for l in self.layers]
@@ -65,6 +70,12 @@ class Workload:
 def centered_ranks(pop: int, gen: torch.Generator) -> torch.Tensor:
     r = torch.randperm(pop, generator=gen).to(torch.float64)
     return (r / max(pop - 1, 1) - 0.5).to(torch.float32)
+
+
+def _returns(number: int, pop: int) -> torch.Tensor:
+    """Synthetic raw returns N(0, 1), rounded to multiples of 1/64 so that ties occur."""
+    g = torch.Generator().manual_seed(2000 + number)
+    return torch.round(torch.randn(pop, generator=g, dtype=torch.float32) * 64) / 64
 
 
 def _normal(shape, var: float, gen: torch.Generator) -> torch.Tensor:
@@ -108,7 +119,8 @@ def make(number: int) -> Workload:
             layers.append(Layer(a, c, w, torch.zeros(c), offs[2 * li]))
         f = centered_ranks(pop, g)
         return Workload(2, NAMES[2], DESCRIPTIONS[2], pop, batch, 0.02,
-                        torch.arange(pop, dtype=torch.int64), x, layers, f, activation="tanh")
+                        torch.arange(pop, dtype=torch.int64), x, layers, f, activation="tanh",
+                        returns=_returns(2, pop))
     if number == 3:
         pop, batch, in_f, out_f = 4096, 32, 1024, 1024
         x = _normal((pop, batch, in_f), 1.0, g).to(torch.bfloat16)
@@ -123,7 +135,7 @@ def make(number: int) -> Workload:
         layer = Layer(in_f, out_f, torch.empty(0), torch.empty(0), 123456789)
         return Workload(4, NAMES[4], DESCRIPTIONS[4], pop, 0, 0.005,
                         torch.arange(1, pop + 1, dtype=torch.int64), torch.empty(0), [layer], f,
-                        forward=False)
+                        forward=False, returns=_returns(4, pop))
     if number == 5:
         pop, batch, in_f, out_f = 256, 256, 4096, 4096
         x = _normal((pop, batch, in_f), 1.0, g).to(torch.bfloat16)
