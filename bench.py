@@ -58,6 +58,15 @@ UNIT = "noise elements/s"
 # pipe: the two products by GAMMA, 3 each, plus that carry add -> 7. Plus the float
 # conversion and the FMA that consumes the noise -> 21 operations in all.
 ALU_OPS_PER_ELEMENT = 12
+# The Gaussian variant: both halves of the last xor-shift and two mantissas
+# (13 ALU operations in all, per ncu's per-opcode counts), three transcendental
+# operations (log2, reciprocal square root, cos) and the floating-point glue of
+# Box-Muller: about 32 instructions per element, so the issue port (4 schedulers
+# x 32 lanes per SM) binds rather than the ALU pipe or the 32-lane MUFU pipe.
+ALU_OPS_GAUSSIAN = 13
+OPS_GAUSSIAN = 32
+MUFU_OPS_GAUSSIAN = 3
+MUFU_LANES_PER_SM = 32
 OPS_PER_ELEMENT = 21
 SMS_NOMINAL = 152
 SM_CLOCK_MAX_HZ = 2.07e9
@@ -110,8 +119,9 @@ def contiguous_blocks(wl) -> bool:
     return True
 
 
-def build_step(wl, dev, stream_ptr):
-    """Device buffers and the launches of one step of workload ``wl`` (on ``dev``)."""
+def build_step(wl, dev, stream_ptr, noise="uniform"):
+    """Device buffers and the launches of one step of workload ``wl`` (on ``dev``);
+    ``noise="gaussian"`` runs the gradient-only workload with the Box-Muller variant."""
     import torch
     from virtual_noise_perturbed_gb300 import _lib
 
@@ -215,7 +225,19 @@ def build_step(wl, dev, stream_ptr):
                                    (P(theta.data_ptr()), P(g.data_ptr()), n_params, ES_LR, s), 0,
                                    hbm_bytes=n_params * 12))
             outputs.append(theta)
-    for li, l in enumerate(d.layers if (wl.grads and not flat) else []):
+    for li, l in enumerate(d.layers if (wl.grads and not flat and noise == "gaussian") else []):
+        # The Gaussian-noise variant: the same flat ranges (weights row-major, then
+        # the bias block) through the noise-kind entry point.
+        gw = torch.empty((l.out_f, l.in_f), dtype=torch.float32, device=dev)
+        gb = torch.empty((l.out_f,), dtype=torch.float32, device=dev)
+        for blk, n_el, off in ((gw, l.out_f * l.in_f, l.offset), (gb, l.out_f, l.offset + l.out_f * l.in_f)):
+            launches.append(Launch("grad_gaussian", lib.vn_gradient_ex,
+                                   (P(fit.data_ptr()), P(d.seeds.data_ptr()), pop, n_el, float(wl.sigma),
+                                    off, _lib.VN_NOISE_GAUSSIAN, P(blk.data_ptr()), s),
+                                   pop * n_el, hbm_bytes=n_el * 4,
+                                   grad_w_elems=n_el if blk is gw else 0))
+        outputs += [gw, gb]
+    for li, l in enumerate(d.layers if (wl.grads and not flat and noise != "gaussian") else []):
         gw = torch.empty((l.out_f, l.in_f), dtype=torch.float32, device=dev)
         gb = torch.empty((l.out_f,), dtype=torch.float32, device=dev)
         launches.append(Launch("grad", lib.vn_weight_gradient,
@@ -346,7 +368,7 @@ def traffic_for(kernel: str, workload: str):
 # The oracle leg (cpu_baseline and --impl reference)
 # ---------------------------------------------------------------------------
 
-def oracle_step(wl, individuals: int) -> int:
+def oracle_step(wl, individuals: int, noise: str = "uniform") -> int:
     """The oracle's pass over the first ``individuals`` of the population: forward,
     the centered ranks of the returns (over the whole population: a rank is global),
     the gradients' sums over those individuals, the parameter update and their noise
@@ -369,6 +391,11 @@ def oracle_step(wl, individuals: int) -> int:
                 h = np.tanh(h)
             n += individuals * l.out_f * l.in_f
     for l in (wl.layers if wl.grads else []):
+        if noise == "gaussian":
+            es.gaussian_flat_gradient(fit, seeds, l.out_f * l.in_f, wl.sigma, individuals, l.offset)
+            es.gaussian_flat_gradient(fit, seeds, l.out_f, wl.sigma, individuals, l.offset + l.out_f * l.in_f)
+            n += individuals * (l.out_f * l.in_f + l.out_f)
+            continue
         gw = es.weight_gradient(fit, seeds, (l.out_f, l.in_f), wl.sigma, individuals, l.offset)
         gb = es.bias_gradient(fit, seeds, (l.out_f,), wl.sigma, individuals, l.offset + l.out_f * l.in_f)
         if wl.forward and len(wl.layers) > 1:
@@ -388,24 +415,24 @@ def cpu_cores_used() -> int:
     return 1
 
 
-def time_oracle(wl, budget_s: float, steps: int = 1):
+def time_oracle(wl, budget_s: float, steps: int = 1, noise: str = "uniform"):
     """Run ``steps`` oracle passes, each on as many individuals as fit ``budget_s``."""
     t = time.perf_counter()
-    oracle_step(wl, 1)
+    oracle_step(wl, 1, noise)
     per_ind = max(time.perf_counter() - t, 1e-4)
     inds = int(max(1, min(wl.pop, budget_s / per_ind)))
     total_el, total_t = 0, 0.0
     for _ in range(steps):
         t = time.perf_counter()
-        total_el += oracle_step(wl, inds)
+        total_el += oracle_step(wl, inds, noise)
         total_t += time.perf_counter() - t
     return total_el / total_t, inds, total_t
 
 
 # ---------------------------------------------------------------------------
 
-def config_for(wl, world):
-    return {"workload": wl.name, "description": wl.description, "pop": wl.pop, "batch": wl.batch,
+def config_for(wl, world, noise="uniform"):
+    return {"workload": wl.name, "description": wl.description, "noise": noise, "pop": wl.pop, "batch": wl.batch,
             "layers": [[l.in_f, l.out_f] for l in wl.layers], "sigma": wl.sigma,
             "noise_elements_per_step": None, "l2": "256 MiB buffer rewritten between timed steps",
             "parallelism": f"population shards x{world} (independent per rank)"}
@@ -417,9 +444,9 @@ def run_reference(args, wl, world, rank):
     from virtual_noise_perturbed_gb300 import workloads  # noqa: F401
     budget = min(2.0, 150.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
-        time_oracle(wl, budget / 4)
-    rate, inds, total_t = time_oracle(wl, budget, steps=args.steps)
-    cfg = config_for(wl, 1)
+        time_oracle(wl, budget / 4, noise=args.noise)
+    rate, inds, total_t = time_oracle(wl, budget, steps=args.steps, noise=args.noise)
+    cfg = config_for(wl, 1, args.noise)
     line = {"metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
@@ -441,11 +468,15 @@ def main(argv=None) -> int:
     ap.add_argument("--workload", default="es_mlp",
                     choices=["tiny", "es_mlp", "mid", "grad_only", "large_tc"])
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--noise", choices=["uniform", "gaussian"], default="uniform",
+                    help="gaussian: the Box-Muller noise variant (gradient-only workload)")
     ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.noise == "gaussian" and args.workload != "grad_only":
+        ap.error("--noise gaussian applies to the gradient-only workload")
 
     from virtual_noise_perturbed_gb300 import workloads
     number = {v: k for k, v in workloads.NAMES.items()}[args.workload]
@@ -469,7 +500,7 @@ def main(argv=None) -> int:
     from virtual_noise_perturbed_gb300 import _lib, build as vbuild
     vbuild.build()
     stream = torch.cuda.Stream(dev)
-    launches, bufs, outputs = build_step(wl, dev, stream.cuda_stream)
+    launches, bufs, outputs = build_step(wl, dev, stream.cuda_stream, args.noise)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     el_step = sum(l.elements for l in launches)
 
@@ -520,7 +551,12 @@ def main(argv=None) -> int:
     dom = max(per_kernel, key=lambda n: per_kernel[n]["ms"])
     r = per_kernel[dom]
     secs = r["ms"] * 1e-3
-    cands = {"alu": (r["elements"] * ALU_OPS_PER_ELEMENT / secs / 1e12, pk["alu_ops"] / 1e12, "Tops/s")}
+    alu_ops = ALU_OPS_GAUSSIAN if dom == "grad_gaussian" else ALU_OPS_PER_ELEMENT
+    cands = {"alu": (r["elements"] * alu_ops / secs / 1e12, pk["alu_ops"] / 1e12, "Tops/s")}
+    if dom == "grad_gaussian":
+        cands["mufu"] = (r["elements"] * MUFU_OPS_GAUSSIAN / secs / 1e12,
+                         SMS_NOMINAL * MUFU_LANES_PER_SM * SM_CLOCK_MAX_HZ / 1e12, "Tops/s")
+        cands["issue"] = (r["elements"] * OPS_GAUSSIAN / secs / 1e12, pk["issue_ops"] / 1e12, "Tops/s")
     if r["hbm_bytes"]:
         cands["hbm"] = (r["hbm_bytes"] / secs / 1e9, pk["hbm_gbs"], "GB/s")
     if r["flops"]:
@@ -529,9 +565,11 @@ def main(argv=None) -> int:
     ach, peak, unit = cands[bound]
     roofline = {"bound": bound, "kernel": dom, "achieved": ach, "peak": peak, "unit": unit,
                 "frac": ach / peak, "traffic": traffic_for(dom, wl.name),
-                "peak_source": ("derived: 152 SMs x 64 integer-ALU lanes x 2.07 GHz"
-                                if bound == "alu" else pk["source"]),
-                "ops_per_element": ALU_OPS_PER_ELEMENT if bound == "alu" else None,
+                "peak_source": ("derived: 152 SMs x 64 integer-ALU lanes x 2.07 GHz" if bound == "alu"
+                                else "derived: 152 SMs x 32 MUFU lanes x 2.07 GHz" if bound == "mufu"
+                                else "derived: 152 SMs x 128 issue lanes x 2.07 GHz" if bound == "issue"
+                                else pk["source"]),
+                "ops_per_element": {"alu": alu_ops, "mufu": MUFU_OPS_GAUSSIAN, "issue": OPS_GAUSSIAN}.get(bound),
                 # the stricter bound: every one of the 21 operations through the issue
                 # port (152 SMs x 128 lanes x 2.07 GHz)
                 "issue_frac": r["elements"] * OPS_PER_ELEMENT / secs / pk["issue_ops"],
@@ -546,7 +584,8 @@ def main(argv=None) -> int:
     grad_w_elems = sum(x.grad_w_elems for x in launches)
     extra = {
         "perturbed_linear_tflops": (sum(x.flops for x in fwd) * args.steps / (fwd_ms * 1e-3) / 1e12) if fwd else None,
-        "grad_w_elem_per_s": (grad_w_elems * args.steps / (per_kernel["grad"]["ms"] * 1e-3)) if "grad" in per_kernel else None,
+        "grad_w_elem_per_s": (grad_w_elems * args.steps / (sum(per_kernel[k]["ms"] for k in per_kernel if k.startswith("grad")) * 1e-3))
+                             if any(k.startswith("grad") for k in per_kernel) else None,
         "noise_elements_per_step": el_step,
     }
 
@@ -555,13 +594,13 @@ def main(argv=None) -> int:
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, inds, tt = time_oracle(wl, args.cpu_baseline_seconds)
+        rate, inds, tt = time_oracle(wl, args.cpu_baseline_seconds, noise=args.noise)
         cpu = {"value": rate, "unit": UNIT, "cores": cpu_cores_used(), "kind": "oracle",
                "sample": f"one oracle pass over the first {inds} of {wl.pop} individuals "
                          f"(forward, gradient sums, noise dump), {tt:.1f} s"}
 
     if rank == 0:
-        cfg = config_for(wl, world)
+        cfg = config_for(wl, world, args.noise)
         cfg["noise_elements_per_step"] = el_step
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": total_ms_max / args.steps, "higher_is_better": True,

@@ -73,6 +73,17 @@ typedef enum vn_path {
                      /* aligned, pop, batch, in and out below 2^31                 */
 } vn_path;
 
+/* Noise distribution of the _ex dump and gradient entry points. */
+typedef enum vn_noise {
+  VN_NOISE_UNIFORM = 0,  /* PRNG(seed, idx) above: the page's centered uniform, bit-exact  */
+  VN_NOISE_GAUSSIAN = 1  /* Box-Muller on the same finalizer output z (a variant; the page  */
+                         /* names Gaussian noise as the costly alternative):                */
+                         /*   u1 = 1 - (hi32(z) >> 9) 2^-23,  u2 = (lo32(z) >> 9) 2^-23,     */
+                         /*   G = sqrt(-2 ln u1) cos(2 pi u2)                                */
+                         /* computed with the hardware log2 and cos: |error| <= 6e-4 where   */
+                         /* u1 is within 2^-12 of 1 (G near 0), about 1e-6 elsewhere.        */
+} vn_noise;
+
 /* Element-wise activation applied to Y after the bias (vn_perturbed_linear_ex). */
 typedef enum vn_act { VN_ACT_NONE = 0, VN_ACT_TANH = 1 } vn_act;
 
@@ -141,6 +152,27 @@ vn_status vn_bias_gradient(const float* fitness, const int64_t* seeds, int64_t p
  */
 vn_status vn_noise_dump(const int64_t* seeds, int64_t pop, int64_t n, uint64_t offset,
                         float* out, void* stream);
+
+/*
+ * vn_noise_dump_ex -- vn_noise_dump with a choice of distribution:
+ *     out[i, t] = noise_kind(seed_i, offset + t),  out [pop, n] fp32.
+ * VN_NOISE_UNIFORM is bit-exact with vn_noise_dump; VN_NOISE_GAUSSIAN is the
+ * Box-Muller variant within the error stated at vn_noise. Same conventions and
+ * errors as vn_noise_dump; an unknown kind returns VN_ERR_VALUE.
+ */
+vn_status vn_noise_dump_ex(const int64_t* seeds, int64_t pop, int64_t n, uint64_t offset,
+                           vn_noise kind, float* out, void* stream);
+
+/*
+ * vn_gradient_ex -- the gradient estimate over a flat range of n elements with
+ * a choice of distribution:
+ *     grad[e] = sum_i fitness[i] * noise_kind(seed_i, offset + e) / (pop * sigma),  e < n.
+ * With VN_NOISE_UNIFORM this is vn_bias_gradient(fitness, seeds, pop, n, ...)
+ * (and a weight block's gradient is the same range, row-major). Same
+ * conventions and errors as vn_weight_gradient; an unknown kind returns VN_ERR_VALUE.
+ */
+vn_status vn_gradient_ex(const float* fitness, const int64_t* seeds, int64_t pop, int64_t n,
+                         double sigma, uint64_t offset, vn_noise kind, float* grad, void* stream);
 
 /*
  * vn_reduce_metric -- "virtual_reduce_metric" (API entry of the page):

@@ -34,7 +34,7 @@ from typing import Iterable, Optional, Sequence
 
 import numpy as np
 
-from .splitmix import element_indices, noise_np, seeds_u64
+from .splitmix import element_indices, gaussian_noise_np, noise_np, seeds_u64
 
 
 def _check_pop(seeds: np.ndarray, pop_size: int, other: Optional[np.ndarray] = None) -> None:
@@ -193,3 +193,26 @@ def es_update(theta, grad, lr: float) -> np.ndarray:
     (lr taken as its float32 value, as the library receives it)."""
     lr32 = float(np.float32(lr))
     return np.asarray(theta, dtype=np.float64) + lr32 * np.asarray(grad, dtype=np.float64)
+
+
+def gaussian_dump(seeds, n_elements: int, offset: int) -> np.ndarray:
+    """The Gaussian variant's dump (reading R16): D[i, t] = G(seed_i, offset + t), float64."""
+    s = seeds_u64(seeds)
+    idx = element_indices(offset, n_elements)
+    return np.stack([gaussian_noise_np(s[i], idx) for i in range(s.shape[0])]) if s.shape[0] else \
+        np.zeros((0, n_elements))
+
+
+def gaussian_flat_gradient(fitness, seeds, n_elements: int, sigma: float, pop_size: int,
+                           offset: int) -> np.ndarray:
+    """The gradient estimate with Gaussian-variant noise, float64:
+    grad[t] = sum_i fitness_i * G(seed_i, offset + t) / (pop_size * sigma)."""
+    f = np.asarray(fitness, dtype=np.float64)
+    s = np.asarray(seeds)
+    _check_pop(s, pop_size, f)
+    su = seeds_u64(s)
+    idx = element_indices(offset, n_elements)
+    acc = np.zeros(n_elements, dtype=np.float64)
+    for i in range(pop_size):
+        acc += f[i] * gaussian_noise_np(su[i], idx)
+    return acc / (pop_size * sigma)

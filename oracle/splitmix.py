@@ -35,6 +35,8 @@ Readings taken where the page is silent (each also listed in the design notes):
 
 from __future__ import annotations
 
+import math
+
 import numpy as np
 
 #: ``_SPLITMIX64_GAMMA`` as printed on the page (decimal).
@@ -118,3 +120,34 @@ def element_indices(offset: int, n: int) -> np.ndarray:
     off = np.uint64(offset & MASK64)
     with np.errstate(over="ignore"):
         return off + np.arange(n, dtype=np.uint64)
+
+
+# ----------------------------------------------------------------------------
+# Gaussian variant (reading R16). The page's forward docstring calls the noise
+# "Gaussian" while its RNG section uses a centered uniform and names Box-Muller
+# as the costly alternative. The variant takes both 32-bit halves of the same
+# finalizer output z as two uniforms and applies Box-Muller:
+#   u1 = 1 - (hi32(z) >> 9) * 2**-23   in (0, 1]   (never 0: the log is finite)
+#   u2 = (lo32(z) >> 9) * 2**-23       in [0, 1)   (the uniform variant's u)
+#   g  = sqrt(-2 ln u1) * cos(2 pi u2)
+# ----------------------------------------------------------------------------
+
+
+def gaussian_from_hash(h: int) -> float:
+    """Box-Muller on the halves of one finalizer output (reading R16), float64."""
+    u1 = 1.0 - ((h >> 32) >> 9) * 2.0 ** -23
+    u2 = ((h & MASK32) >> 9) * 2.0 ** -23
+    return math.sqrt(-2.0 * math.log(u1)) * math.cos(2.0 * math.pi * u2)
+
+
+def gaussian_noise(seed: int, idx: int) -> float:
+    """Gaussian-variant noise for element ``idx`` of individual ``seed``."""
+    return gaussian_from_hash(mix64(state64(seed, idx)))
+
+
+def gaussian_noise_np(seed_u64: np.ndarray, idx_u64: np.ndarray) -> np.ndarray:
+    """Gaussian-variant noise values, float64, vectorised."""
+    h = mix64_np(state64_np(seed_u64, idx_u64))
+    u1 = 1.0 - ((h >> np.uint64(32)) >> _S9).astype(np.float64) * 2.0 ** -23
+    u2 = ((h & _LO32) >> _S9).astype(np.float64) * 2.0 ** -23
+    return np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)

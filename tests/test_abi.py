@@ -143,3 +143,13 @@ def test_ranks_and_update_validation(lib):
     assert lib.vn_es_update(P(0), P(0), 0, 0.1, P(0)) == 0
     assert lib.vn_es_update(P(0), P(fake), 4, 0.1, P(0)) == 1
     assert lib.vn_es_update(P(fake), P(fake + 1), 4, 0.1, P(0)) == 5
+
+
+def test_noise_kind_validation(lib):
+    fake = 0x1000
+    assert lib.vn_noise_dump_ex(P(fake), 1, 4, 0, 7, P(fake), P(0)) == 4        # unknown kind
+    assert lib.vn_noise_dump_ex(P(fake), -1, 4, 0, 1, P(fake), P(0)) == 2
+    assert lib.vn_noise_dump_ex(P(0), 0, 4, 0, 1, P(0), P(0)) == 0               # empty
+    assert lib.vn_gradient_ex(P(fake), P(fake), 1, 4, 0.1, 0, 2, P(fake), P(0)) == 4
+    assert lib.vn_gradient_ex(P(fake), P(fake), 0, 4, 0.1, 0, 1, P(fake), P(0)) == 2
+    assert lib.vn_gradient_ex(P(fake), P(fake), 4, 4, 0.0, 0, 1, P(fake), P(0)) == 4

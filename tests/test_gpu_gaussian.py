@@ -1,0 +1,87 @@
+"""GPU parity of the Gaussian-noise variant (Box-Muller on the finalizer's two halves).
+
+The GPU evaluates log2, cos and sqrt with the hardware approximations; their error
+bounds (absolute 2^-22 for log2 on [1/2, 2], 2^-21.4 for cos on [-pi, pi]) give
+|G_gpu - G| <= sqrt(2 ln 2 * 2^-22) ~ 6e-4 where u1 is within ~2^-12 of 1 (G near 0)
+and ~1e-6 elsewhere; the tests use 1e-3 for the maximum and 2e-6 for the mean. The
+gradient keeps the usual 1e-4 of the oracle's RMS. The uniform kind through the same
+entry points is bit-identical to the plain entry points."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import es
+from tests.parity import TOL_FP32, assert_close, to_np
+from virtual_noise_perturbed_gb300 import (VNError, noise_dump, virtual_bias_gradient,
+                                           virtual_flat_gradient)
+from virtual_noise_perturbed_gb300.build import build
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build()
+
+
+@pytest.mark.parametrize("pop,n,offset", [(1, 3, 0), (4, 4099, 2 ** 32 - 5), (64, 12345, 2 ** 64 - 101),
+                                          (3, 8192 * 2 + 1, 7)])
+def test_gaussian_dump_within_the_error_bound(pop, n, offset):
+    seeds = torch.arange(pop, dtype=torch.int64) * 7 - 3
+    got = noise_dump(seeds.to(DEV), n, offset, noise="gaussian").cpu().numpy().astype(np.float64)
+    want = es.gaussian_dump(seeds.numpy(), n, offset)
+    err = np.abs(got - want)
+    assert np.all(np.isfinite(got))
+    assert err.max() <= 1e-3, err.max()
+    assert err.mean() <= 2e-6, err.mean()
+
+
+def test_uniform_kind_is_the_plain_dump():
+    seeds = torch.arange(5, dtype=torch.int64, device=DEV)
+    a = noise_dump(seeds, 9999, 11)
+    b = noise_dump(seeds, 9999, 11, noise="uniform")
+    assert torch.equal(a, b)
+    with pytest.raises(ValueError):
+        noise_dump(seeds, 10, 0, noise="cauchy")
+
+
+@pytest.mark.parametrize("pop,n", [(8, 1000), (1024, 3000), (4096, 256), (3, 70001)])
+def test_gaussian_gradient_matches_oracle(pop, n):
+    g = torch.Generator().manual_seed(pop + n)
+    f = torch.randn(pop, generator=g)
+    seeds = torch.arange(pop, dtype=torch.int64) + 100
+    got = virtual_flat_gradient(f.to(DEV), seeds.to(DEV), n, 0.02, pop, 555, noise="gaussian")
+    want = es.gaussian_flat_gradient(f.numpy(), seeds.numpy(), n, 0.02, pop, 555)
+    assert_close(to_np(got), want, TOL_FP32, f"gaussian gradient pop {pop} n {n}")
+
+
+def test_gaussian_gradient_one_hot_recovers_the_dump():
+    pop, n, sigma = 8, 777, 2.0 ** -7
+    seeds = torch.arange(pop, dtype=torch.int64, device=DEV) * 3
+    d = noise_dump(seeds, n, 99, noise="gaussian")
+    for m in (0, 5):
+        f = torch.zeros(pop, device=DEV)
+        f[m] = pop * sigma
+        got = virtual_flat_gradient(f, seeds, n, sigma, pop, 99, noise="gaussian")
+        assert torch.equal(got, d[m])
+
+
+def test_uniform_kind_is_the_plain_gradient():
+    g = torch.Generator().manual_seed(3)
+    f = torch.randn(300, generator=g).to(DEV)
+    seeds = torch.arange(300, dtype=torch.int64, device=DEV)
+    a = virtual_bias_gradient(f, seeds, (5000,), 0.01, 300, 42)
+    b = virtual_flat_gradient(f, seeds, 5000, 0.01, 300, 42, noise="uniform")
+    assert torch.equal(a, b)
+
+
+def test_unknown_kind_is_refused_by_the_library():
+    from virtual_noise_perturbed_gb300 import _lib
+    lib = _lib.load()
+    P = __import__("ctypes").c_void_p
+    assert lib.vn_noise_dump_ex(P(0x1000), 1, 4, 0, 7, P(0x1000), P(0)) == 4
+    assert lib.vn_gradient_ex(P(0x1000), P(0x1000), 1, 4, 0.1, 0, 2, P(0x1000), P(0)) == 4
+    with pytest.raises(VNError):
+        virtual_flat_gradient(torch.ones(2, device=DEV), torch.arange(2, device=DEV), 4, 0.0, 2)

@@ -402,3 +402,63 @@ def test_es_update_is_theta_plus_lr_grad():
     assert np.array_equal(es.es_update(theta, grad, 0.5), np.array([2.0, 0.0, 0.0]))
     # lr is used at float32 precision, as the library receives it
     assert es.es_update(np.zeros(1, np.float32), np.ones(1, np.float32), 0.1)[0] == float(np.float32(0.1))
+
+
+# ---------------------------------------------------------------------------
+# Gaussian variant (Box-Muller on the two halves of the finalizer output)
+# ---------------------------------------------------------------------------
+
+def test_gaussian_reads_both_halves_hand_values():
+    """Choose finalizer outputs, invert them to states, and check Box-Muller's value.
+
+    hi32 -> u1 = 1 - (hi32 >> 9) 2^-23 and lo32 -> u2 = (lo32 >> 9) 2^-23, by hand:
+    hi32 = 2^31 gives u1 = 1/2, lo32 = 0 gives u2 = 0 -> g = sqrt(2 ln 2);
+    hi32 < 2^9 gives u1 = 1 -> g = 0 whatever u2; lo32 = 2^31 gives u2 = 1/2 -> g = -sqrt(-2 ln u1)."""
+    rng = random.Random(11)
+    r_half = math.sqrt(2.0 * math.log(2.0))
+    cases = [
+        (0x80000000_00000000, r_half),
+        (0x80000000_000001FF, r_half),                     # bits below 9 of lo32 dropped
+        (0x000001FF_12345678, 0.0),                        # u1 = 1
+        (0x80000000_80000000, -r_half),                    # u2 = 1/2: cos = -1
+        (0xC0000000_00000000, math.sqrt(-2.0 * math.log(0.25))),   # u1 = 1 - 3/4
+    ]
+    for h, want in cases:
+        state = _inverse_finalizer(h, GAMMA_PAGE)
+        idx = rng.getrandbits(64)
+        seed = (state - (idx + 1) * GAMMA_PAGE) & M64
+        assert abs(sm.gaussian_noise(seed, idx) - want) < 1e-15
+
+
+def test_gaussian_numpy_matches_python_int():
+    rng = random.Random(12)
+    seeds = _rand_u64(rng, 50) + EDGE
+    idx = _rand_u64(rng, 50) + EDGE
+    got = sm.gaussian_noise_np(np.array(seeds, dtype=np.uint64), np.array(idx, dtype=np.uint64))
+    for g, s, i in zip(got, seeds, idx):
+        assert abs(g - sm.gaussian_noise(s, i)) < 1e-12
+
+
+def test_gaussian_statistics():
+    g = es.gaussian_dump(np.arange(4), 250000, 12345).ravel()
+    n = g.size
+    assert np.all(np.isfinite(g)) and np.max(np.abs(g)) < 5.8   # |g| <= sqrt(2*23*ln 2)
+    assert abs(g.mean()) < 5 / math.sqrt(n)
+    assert abs(g.var() - 1.0) < 5 * math.sqrt(2.0 / n)
+    assert abs(np.mean(np.abs(g) > 2.0) - math.erfc(2.0 / math.sqrt(2.0))) < 5e-4
+    # Kolmogorov-Smirnov distance to the standard normal CDF
+    s = np.sort(g[:200000])
+    cdf = 0.5 * (1.0 + np.vectorize(math.erf)(s / math.sqrt(2.0)))
+    emp = np.arange(1, s.size + 1) / s.size
+    assert np.max(np.abs(emp - cdf)) < 1.63 / math.sqrt(s.size) * 1.5
+
+
+def test_gaussian_gradient_one_hot_fitness_recovers_noise():
+    seeds = np.array([3, -4, 5, 9])
+    pop, sigma, off, n = 4, 2.0 ** -3, 77, 33
+    dump = es.gaussian_dump(seeds, n, off)
+    for m in range(pop):
+        f = np.zeros(pop)
+        f[m] = pop * sigma
+        np.testing.assert_allclose(es.gaussian_flat_gradient(f, seeds, n, sigma, pop, off), dump[m],
+                                   rtol=0, atol=1e-15)

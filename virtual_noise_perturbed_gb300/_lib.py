@@ -26,6 +26,8 @@ VN_F32, VN_BF16 = 0, 1
 VN_PATH_AUTO, VN_PATH_FFMA, VN_PATH_TC = 0, 1, 2
 # vn_act
 VN_ACT_NONE, VN_ACT_TANH = 0, 1
+# vn_noise
+VN_NOISE_UNIFORM, VN_NOISE_GAUSSIAN = 0, 1
 
 #: Every symbol the header declares, with (restype, argtypes).
 _P, _I64, _U64, _I, _D = ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_int, ctypes.c_double
@@ -41,6 +43,8 @@ SIGNATURES = {
     "vn_perturbed_mlp": (_I, [_P, _I, _I, _I64, _P, _P, _P, _P, _P, _I64, _I64, _D, _I, _P, _P]),
     "vn_centered_ranks": (_I, [_P, _I64, _P, _P]),
     "vn_es_update": (_I, [_P, _P, _I64, _D, _P]),
+    "vn_noise_dump_ex": (_I, [_P, _I64, _I64, _U64, _I, _P, _P]),
+    "vn_gradient_ex": (_I, [_P, _P, _I64, _I64, _D, _U64, _I, _P, _P]),
     "vn_device_status": (_I, [_P]),
     "vn_testhook_linear_tc_withhold": (_I, [_P, _I, _I, _P, _I, _P, _I, _P, _I64, _I64, _I64, _I64,
                                            _D, _U64, _P, _I, _I64, _D, _P]),

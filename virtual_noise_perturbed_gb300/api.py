@@ -25,6 +25,7 @@ from ._lib import VNError, check, load
 _DT = {torch.float32: _lib.VN_F32, torch.bfloat16: _lib.VN_BF16}
 _PATHS = {"auto": _lib.VN_PATH_AUTO, "ffma": _lib.VN_PATH_FFMA, "tc": _lib.VN_PATH_TC}
 _ACTS = {None: _lib.VN_ACT_NONE, "none": _lib.VN_ACT_NONE, "tanh": _lib.VN_ACT_TANH}
+_NOISE = {"uniform": _lib.VN_NOISE_UNIFORM, "gaussian": _lib.VN_NOISE_GAUSSIAN}
 _M64 = (1 << 64) - 1
 
 
@@ -209,24 +210,38 @@ def virtual_bias_gradient(fitness: torch.Tensor, seeds: torch.Tensor, bias_shape
 
 
 def virtual_flat_gradient(fitness: torch.Tensor, seeds: torch.Tensor, n_params: int, sigma: float,
-                          pop_size: int, offset: int = 0) -> torch.Tensor:
+                          pop_size: int, offset: int = 0, *, noise: str = "uniform") -> torch.Tensor:
     """grad[t] = sum_i fitness_i * PRNG(seed_i, offset + t) / (pop_size * sigma), t < n_params.
 
     With parameter blocks laid out by ``compute_offsets`` (weights then bias, one
     block after another), this is the gradient of every block in one launch:
     block b's gradient is ``grad[offsets[b] : offsets[b] + numel_b]`` reshaped to the
     block's shape, equal (up to the order of the fp32 sums) to
-    ``virtual_weight_gradient`` / ``virtual_bias_gradient`` on that block."""
-    return virtual_bias_gradient(fitness, seeds, (int(n_params),), sigma, pop_size, offset)
-
-
-def noise_dump(seeds: torch.Tensor, n_elements: int, offset: int) -> torch.Tensor:
-    """(pop, n) fp32 centered-uniform noise, D[i, t] = PRNG(seed_i, offset + t)."""
+    ``virtual_weight_gradient`` / ``virtual_bias_gradient`` on that block.
+    ``noise="gaussian"`` uses the Box-Muller variant of the noise instead."""
     lib = load()
+    if noise not in _NOISE:
+        raise ValueError("noise must be 'uniform' or 'gaussian'")
+    seeds = _seeds(seeds)
+    fitness = _fitness(fitness, pop_size, seeds)
+    g = torch.empty((int(n_params),), dtype=torch.float32, device=fitness.device)
+    st = lib.vn_gradient_ex(_ptr(fitness), _ptr(seeds), pop_size, int(n_params), float(sigma),
+                            int(offset) & _M64, _NOISE[noise], _ptr(g), _stream(g))
+    check(st, "vn_gradient_ex")
+    return g
+
+
+def noise_dump(seeds: torch.Tensor, n_elements: int, offset: int, *,
+               noise: str = "uniform") -> torch.Tensor:
+    """(pop, n) fp32 noise, D[i, t] = PRNG(seed_i, offset + t): the centered uniform
+    (bit-exact), or with ``noise="gaussian"`` the Box-Muller variant."""
+    lib = load()
+    if noise not in _NOISE:
+        raise ValueError("noise must be 'uniform' or 'gaussian'")
     seeds = _seeds(seeds)
     d = torch.empty((seeds.numel(), int(n_elements)), dtype=torch.float32, device=seeds.device)
-    st = lib.vn_noise_dump(_ptr(seeds), seeds.numel(), int(n_elements), int(offset) & _M64,
-                           _ptr(d), _stream(d))
+    st = lib.vn_noise_dump_ex(_ptr(seeds), seeds.numel(), int(n_elements), int(offset) & _M64,
+                              _NOISE[noise], _ptr(d), _stream(d))
     check(st, "vn_noise_dump")
     return d
 

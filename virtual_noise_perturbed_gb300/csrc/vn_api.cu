@@ -99,19 +99,26 @@ int vn_version(void) { return (1 << 16) | 0; }
 
 vn_status vn_noise_dump(const int64_t* seeds, int64_t pop, int64_t n, uint64_t offset,
                         float* out, void* stream) {
+  return vn_noise_dump_ex(seeds, pop, n, offset, VN_NOISE_UNIFORM, out, stream);
+}
+
+vn_status vn_noise_dump_ex(const int64_t* seeds, int64_t pop, int64_t n, uint64_t offset,
+                           vn_noise kind, float* out, void* stream) {
+  if (kind != VN_NOISE_UNIFORM && kind != VN_NOISE_GAUSSIAN) return VN_ERR_VALUE;
   if (pop < 0 || n < 0) return VN_ERR_SHAPE;
   int64_t total;
   if (!mul(pop, n, &total)) return VN_ERR_OVERFLOW;
   if (total == 0) return VN_OK;
   if (seeds == nullptr || out == nullptr) return VN_ERR_NULL;
   if (!aligned(seeds, 8) || !aligned(out, 4)) return VN_ERR_ALIGN;
-  return launched(vn::launch_noise_dump(seeds, pop, n, offset, out,
+  return launched(vn::launch_noise_dump(seeds, pop, n, offset, kind, out,
                                         static_cast<cudaStream_t>(stream)));
 }
 
 static vn_status gradient(const float* fitness, const int64_t* seeds, int64_t pop, int64_t m_rows,
-                          int64_t m_cols, double sigma, uint64_t offset, float* grad,
-                          void* stream) {
+                          int64_t m_cols, double sigma, uint64_t offset, vn_noise kind,
+                          float* grad, void* stream) {
+  if (kind != VN_NOISE_UNIFORM && kind != VN_NOISE_GAUSSIAN) return VN_ERR_VALUE;
   if (pop < 1 || m_rows < 0 || m_cols < 0) return VN_ERR_SHAPE;
   int64_t m;
   if (!mul(m_rows, m_cols, &m)) return VN_ERR_OVERFLOW;
@@ -123,20 +130,25 @@ static vn_status gradient(const float* fitness, const int64_t* seeds, int64_t po
   if (m == 0) return VN_OK;
   if (fitness == nullptr || seeds == nullptr || grad == nullptr) return VN_ERR_NULL;
   if (!aligned(fitness, 4) || !aligned(seeds, 8) || !aligned(grad, 4)) return VN_ERR_ALIGN;
-  return launched(vn::launch_grad(fitness, seeds, pop, m, offset, scale, grad,
+  return launched(vn::launch_grad(fitness, seeds, pop, m, offset, scale, kind, grad,
                                   static_cast<cudaStream_t>(stream)));
 }
 
 vn_status vn_weight_gradient(const float* fitness, const int64_t* seeds, int64_t pop,
                              int64_t out, int64_t in, double sigma, uint64_t offset,
                              float* grad_w, void* stream) {
-  return gradient(fitness, seeds, pop, out, in, sigma, offset, grad_w, stream);
+  return gradient(fitness, seeds, pop, out, in, sigma, offset, VN_NOISE_UNIFORM, grad_w, stream);
 }
 
 vn_status vn_bias_gradient(const float* fitness, const int64_t* seeds, int64_t pop,
                            int64_t out, double sigma, uint64_t offset, float* grad_b,
                            void* stream) {
-  return gradient(fitness, seeds, pop, out, 1, sigma, offset, grad_b, stream);
+  return gradient(fitness, seeds, pop, out, 1, sigma, offset, VN_NOISE_UNIFORM, grad_b, stream);
+}
+
+vn_status vn_gradient_ex(const float* fitness, const int64_t* seeds, int64_t pop, int64_t n,
+                         double sigma, uint64_t offset, vn_noise kind, float* grad, void* stream) {
+  return gradient(fitness, seeds, pop, n, 1, sigma, offset, kind, grad, stream);
 }
 
 vn_status vn_reduce_metric(const float* center, const int64_t* seeds, int64_t pop,

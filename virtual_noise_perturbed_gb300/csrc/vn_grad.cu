@@ -40,7 +40,7 @@ constexpr int kE = 8;           // consecutive elements per lane
 constexpr int kTile = 32 * kE;  // elements per CTA tile
 constexpr int kStage = 256;     // individuals staged per round
 
-template <bool kCluster>
+template <bool kCluster, int kKind>
 __global__ void __launch_bounds__(kThreads)
 grad_kernel(const float* __restrict__ fitness, const int64_t* __restrict__ seeds, int64_t pop,
             int64_t m, uint64_t offset, float scale, float* __restrict__ out, int64_t tiles) {
@@ -80,12 +80,16 @@ grad_kernel(const float* __restrict__ fitness, const int64_t* __restrict__ seeds
       __syncthreads();
       for (int q = warp; q < cn; q += kWarps) {
         const uint4 v = s_ind[q];
-        const float f = __uint_as_float(v.z);
+        // (the Gaussian variant's constant factor rides on the fitness weight)
+        const float f = kKind == kGaussian ? kGaussScale * __uint_as_float(v.z) : __uint_as_float(v.z);
 #pragma unroll
         for (int e = 0; e < kE; ++e) {
           uint32_t lo = blo[e], hi = bhi[e];
           add64(lo, hi, v.x, v.y);
-          acc[e] = fmaf(f, noise_from_bits(mix_to_one_plus_u(lo, hi)), acc[e]);
+          if constexpr (kKind == kGaussian)
+            acc[e] = fmaf(f, noise_value<kGaussian>(lo, hi), acc[e]);
+          else
+            acc[e] = fmaf(f, noise_from_bits(mix_to_one_plus_u(lo, hi)), acc[e]);
         }
       }
     }
@@ -129,15 +133,14 @@ int occupancy(const void* fn) {
   return blocks;
 }
 
-}  // namespace
-
-cudaError_t launch_grad(const float* fitness, const int64_t* seeds, int64_t pop, int64_t m,
-                        uint64_t offset, float scale, float* out, cudaStream_t stream) {
+template <int kKind>
+cudaError_t launch_grad_kind(const float* fitness, const int64_t* seeds, int64_t pop, int64_t m,
+                             uint64_t offset, float scale, float* out, cudaStream_t stream) {
   DeviceInfo dev;
   cudaError_t err = device_info(&dev);
   if (err != cudaSuccess) return err;
   const int64_t tiles = (m + kTile - 1) / kTile;
-  static const int occ = occupancy(reinterpret_cast<const void*>(&grad_kernel<false>));
+  static const int occ = occupancy(reinterpret_cast<const void*>(&grad_kernel<false, kKind>));
   const int64_t resident = static_cast<int64_t>(dev.sm_count) * occ;
 
   // Split the population across a cluster while the tiles alone leave the GPU
@@ -149,7 +152,7 @@ cudaError_t launch_grad(const float* fitness, const int64_t* seeds, int64_t pop,
 
   if (slices == 1) {
     const int64_t grid = std::min<int64_t>(tiles, resident * 4);
-    grad_kernel<false><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(
+    grad_kernel<false, kKind><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(
         fitness, seeds, pop, m, offset, scale, out, tiles);
     return cudaGetLastError();
   }
@@ -166,8 +169,17 @@ cudaError_t launch_grad(const float* fitness, const int64_t* seeds, int64_t pop,
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, grad_kernel<true>, fitness, seeds, pop, m, offset, scale, out,
-                            tiles);
+  return cudaLaunchKernelEx(&cfg, grad_kernel<true, kKind>, fitness, seeds, pop, m, offset, scale,
+                            out, tiles);
+}
+
+}  // namespace
+
+cudaError_t launch_grad(const float* fitness, const int64_t* seeds, int64_t pop, int64_t m,
+                        uint64_t offset, float scale, int kind, float* out, cudaStream_t stream) {
+  return kind == kGaussian
+             ? launch_grad_kind<kGaussian>(fitness, seeds, pop, m, offset, scale, out, stream)
+             : launch_grad_kind<kUniform>(fitness, seeds, pop, m, offset, scale, out, stream);
 }
 
 }  // namespace vn

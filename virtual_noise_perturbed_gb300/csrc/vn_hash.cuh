@@ -87,6 +87,73 @@ __device__ __forceinline__ void index_term(uint64_t idx, uint32_t& lo, uint32_t&
   hi = static_cast<uint32_t>(t >> 32);
 }
 
+// The full 64-bit finalizer output (zhi:zlo) of the state (hi:lo).
+__device__ __forceinline__ void mix64_halves(uint32_t lo, uint32_t hi, uint32_t& zlo,
+                                             uint32_t& zhi) {
+  const uint32_t l1 = lo ^ __funnelshift_r(lo, hi, 30);
+  const uint32_t h1 = hi ^ (hi >> 30);
+  uint32_t l2, h2;
+  mul_gamma(l1, h1, l2, h2);
+  const uint32_t l3 = l2 ^ __funnelshift_r(l2, h2, 27);
+  const uint32_t h3 = h2 ^ (h2 >> 27);
+  uint32_t l4, h4;
+  mul_gamma(l3, h3, l4, h4);
+  zlo = l4 ^ __funnelshift_r(l4, h4, 31);
+  zhi = h4 ^ (h4 >> 31);
+}
+
+// Gaussian variant: Box-Muller on the two halves of one finalizer output,
+//   u1 = 1 - (zhi >> 9) 2^-23 in (0, 1],  u2 = (zlo >> 9) 2^-23 in [0, 1),
+//   G = sqrt(-2 ln u1) cos(2 pi u2)
+//     = kGaussScale * sqrt(-log2 u1) * cos(2 pi (u2 - 1/2)),  kGaussScale = -sqrt(2 ln 2).
+// gaussian_unit() returns the last two factors; callers apply kGaussScale (the
+// gradient folds it into the fitness weight). Both uniforms are formed exactly
+// through the mantissa of 1.0f; log2, the reciprocal square root and cos (on
+// [-pi, pi)) are the hardware approximations, whose error bounds give
+// |G - exact| <= 6e-4 where u1 is within ~2^-12 of 1 (G near 0) and about 1e-6
+// elsewhere.
+// The three approximations are the PTX .approx.ftz instructions: every operand
+// here is either 0 or a normal number (u1 >= 2^-23, m + 1e-30 >= 1e-30), so flushing
+// subnormals changes nothing and saves the subnormal checks.
+constexpr float kGaussScale = -1.17741002f;
+__device__ __forceinline__ float lg2_approx(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rsqrt_approx(float x) {
+  float y;
+  asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float cos_approx(float x) {
+  float y;
+  asm("cos.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float gaussian_unit(uint32_t zlo, uint32_t zhi) {
+  const float u1 = 2.0f - __uint_as_float((zhi >> 9) | kOneBits);
+  const float a = __uint_as_float((zlo >> 9) | kOneBits) - 1.5f;  // u2 - 1/2 in [-1/2, 1/2)
+  const float m = -lg2_approx(u1);                               // -log2 u1 >= 0
+  // sqrt(m) as m * rsqrt(m + 1e-30): exact 0 for m = 0 (u1 = 1), and the added
+  // 1e-30 vanishes in the rounding for every other m (m >= 1.7e-7).
+  return m * rsqrt_approx(m + 1e-30f) * cos_approx(6.28318531f * a);
+}
+
+// The noise value of the state (hi:lo) for either kind (the Gaussian one
+// without kGaussScale: see gaussian_unit).
+enum NoiseKind { kUniform = 0, kGaussian = 1 };
+template <int kKind>
+__device__ __forceinline__ float noise_value(uint32_t lo, uint32_t hi) {
+  if constexpr (kKind == kGaussian) {
+    uint32_t zlo, zhi;
+    mix64_halves(lo, hi, zlo, zhi);
+    return gaussian_unit(zlo, zhi);
+  } else {
+    return __uint_as_float(mix_to_one_plus_u(lo, hi)) - 1.5f;
+  }
+}
+
 // PRNG(seed, idx) in one call (used where the cost does not matter).
 __device__ __forceinline__ float noise_at(uint64_t seed, uint64_t idx) {
   const uint64_t s = seed + (idx + 1ull) * kGamma;

@@ -21,13 +21,14 @@ struct DeviceInfo {
 };
 cudaError_t device_info(DeviceInfo* info);
 
-// out[i, t] = PRNG(seed_i, offset + t), t < n.
+// out[i, t] = PRNG(seed_i, offset + t), t < n; kind: VN_NOISE_UNIFORM (the
+// centered uniform, exact) or VN_NOISE_GAUSSIAN (the Box-Muller variant).
 cudaError_t launch_noise_dump(const int64_t* seeds, int64_t pop, int64_t n, uint64_t offset,
-                              float* out, cudaStream_t stream);
+                              int kind, float* out, cudaStream_t stream);
 
-// out[e] = scale * sum_i fitness[i] * PRNG(seed_i, offset + e), e < m.
+// out[e] = scale * sum_i fitness[i] * PRNG(seed_i, offset + e), e < m, with the noise of `kind`.
 cudaError_t launch_grad(const float* fitness, const int64_t* seeds, int64_t pop, int64_t m,
-                        uint64_t offset, float scale, float* out, cudaStream_t stream);
+                        uint64_t offset, float scale, int kind, float* out, cudaStream_t stream);
 
 // fitness[i] = inv_n * sum_k |center[k] + sigma * PRNG(seed_i, offset + k)|.
 cudaError_t launch_reduce_metric(const float* center, const int64_t* seeds, int64_t pop,

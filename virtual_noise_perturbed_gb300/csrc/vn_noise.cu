@@ -38,7 +38,18 @@ constexpr uint64_t kDumpStep = kGamma * static_cast<uint64_t>(kDumpStride);
 // vec4: every row starts 16-byte aligned (out aligned and n % 4 == 0).
 // kIdx32: the chunk count fits in 32 bits, so the row of a chunk is a 32-bit
 // division (a 64-bit one costs several instructions per element).
-template <bool kIdx32>
+// One dump value of the state st: the uniform's exact noise, or the Gaussian variant.
+template <int kKind>
+__device__ __forceinline__ float dump_value(uint64_t st) {
+  if constexpr (kKind == kGaussian) {
+    return kGaussScale *
+           noise_value<kGaussian>(static_cast<uint32_t>(st), static_cast<uint32_t>(st >> 32));
+  } else {
+    return noise_from_bits(mix_to_one_plus_u(st));
+  }
+}
+
+template <bool kIdx32, int kKind>
 __global__ void __launch_bounds__(kDumpThreads)
 noise_dump_kernel(const int64_t* __restrict__ seeds, int64_t n, uint64_t offset,
                   float* __restrict__ out, int64_t chunks_per_row, int64_t total_chunks,
@@ -59,7 +70,7 @@ noise_dump_kernel(const int64_t* __restrict__ seeds, int64_t n, uint64_t offset,
         float v[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          v[q] = noise_from_bits(mix_to_one_plus_u(st));
+          v[q] = dump_value<kKind>(st);
           st += kGamma;
         }
         __stcs(reinterpret_cast<float4*>(row + t0 + g * kDumpStride),
@@ -79,7 +90,7 @@ noise_dump_kernel(const int64_t* __restrict__ seeds, int64_t n, uint64_t offset,
         float v[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          v[q] = noise_from_bits(mix_to_one_plus_u(st));
+          v[q] = dump_value<kKind>(st);
           st += kGamma;
         }
         if (vec4 && t + 4 <= n) {
@@ -165,8 +176,19 @@ reduce_metric_kernel(const float* __restrict__ center, const int64_t* __restrict
 
 }  // namespace
 
+template <int kKind>
+void dump_launch(bool idx32, unsigned grid, cudaStream_t stream, const int64_t* seeds, int64_t n,
+                 uint64_t offset, float* out, int64_t chunks_per_row, int64_t total, int vec4) {
+  if (idx32)
+    noise_dump_kernel<true, kKind><<<grid, kDumpThreads, 0, stream>>>(
+        seeds, n, offset, out, chunks_per_row, total, vec4);
+  else
+    noise_dump_kernel<false, kKind><<<grid, kDumpThreads, 0, stream>>>(
+        seeds, n, offset, out, chunks_per_row, total, vec4);
+}
+
 cudaError_t launch_noise_dump(const int64_t* seeds, int64_t pop, int64_t n, uint64_t offset,
-                              float* out, cudaStream_t stream) {
+                              int kind, float* out, cudaStream_t stream) {
   DeviceInfo dev;
   cudaError_t err = device_info(&dev);
   if (err != cudaSuccess) return err;
@@ -174,12 +196,13 @@ cudaError_t launch_noise_dump(const int64_t* seeds, int64_t pop, int64_t n, uint
   const int64_t total = pop * chunks_per_row;
   const int vec4 = (n % 4 == 0) && (reinterpret_cast<uintptr_t>(out) % 16 == 0);
   const int64_t grid = std::min<int64_t>(total, static_cast<int64_t>(dev.sm_count) * 8);
-  if (total <= 0xFFFFFFFFll)
-    noise_dump_kernel<true><<<static_cast<unsigned>(grid), kDumpThreads, 0, stream>>>(
-        seeds, n, offset, out, chunks_per_row, total, vec4);
+  const bool idx32 = total <= 0xFFFFFFFFll;
+  if (kind == kGaussian)
+    dump_launch<kGaussian>(idx32, static_cast<unsigned>(grid), stream, seeds, n, offset, out,
+                           chunks_per_row, total, vec4);
   else
-    noise_dump_kernel<false><<<static_cast<unsigned>(grid), kDumpThreads, 0, stream>>>(
-        seeds, n, offset, out, chunks_per_row, total, vec4);
+    dump_launch<kUniform>(idx32, static_cast<unsigned>(grid), stream, seeds, n, offset, out,
+                          chunks_per_row, total, vec4);
   return cudaGetLastError();
 }
 
