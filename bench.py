@@ -468,6 +468,8 @@ def main(argv=None) -> int:
     ap.add_argument("--workload", default="es_mlp",
                     choices=["tiny", "es_mlp", "mid", "grad_only", "large_tc"])
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--pop", type=int, default=None,
+                    help="run only the workload's first POP individuals (smaller profiling cases)")
     ap.add_argument("--noise", choices=["uniform", "gaussian"], default="uniform",
                     help="gaussian: the Box-Muller noise variant (gradient-only workload)")
     ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
@@ -482,6 +484,8 @@ def main(argv=None) -> int:
     number = {v: k for k, v in workloads.NAMES.items()}[args.workload]
     world, rank, local = dist_env()
     wl = workloads.make(number)
+    if args.pop is not None:
+        wl = wl.first(args.pop)
     if rank > 0:  # independent population per rank
         wl.seeds = wl.seeds + rank * wl.pop
 

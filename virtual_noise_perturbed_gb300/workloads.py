@@ -60,6 +60,20 @@ class Workload:
                     for l in self.layers]
         return d
 
+    def first(self, pop: int) -> "Workload":
+        """The same workload restricted to its first ``pop`` individuals (smaller
+        cases of the same shapes, e.g. for profiling)."""
+        if not 1 <= pop <= self.pop:
+            raise ValueError(f"pop must be in [1, {self.pop}]")
+        d = dataclasses.replace(self)
+        d.pop = pop
+        d.seeds = self.seeds[:pop]
+        d.fitness = self.fitness[:pop]
+        d.returns = None if self.returns is None else self.returns[:pop]
+        if self.x.dim() == 3:
+            d.x = self.x[:pop]
+        return d
+
     @property
     def noise_elements(self) -> int:
         """pop * (parameters of every block): noise elements per full regeneration."""
