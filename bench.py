@@ -594,7 +594,9 @@ def main(argv=None) -> int:
     }
 
     # --- end to end: host buffers, copies inside the timed region
-    e2e = run_e2e(wl, dev, stream, launches, bufs, outputs, args.e2e_steps, world, el_step)
+    n_launches = len(launches)
+    del launches, bufs, outputs
+    e2e = run_e2e(wl, dev, stream, args.e2e_steps, world, el_step, args.noise)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -610,7 +612,7 @@ def main(argv=None) -> int:
                 "warmup": args.warmup, "ms_per_step": total_ms_max / args.steps, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f32" if wl.number in (1, 2) else "bf16",
                 "data": "synthetic", "config": cfg, "roofline": roofline, "cpu_baseline": cpu,
-                "e2e": e2e, "gpu_launches": len(launches) * args.steps, "clocks": clocks,
+                "e2e": e2e, "gpu_launches": n_launches * args.steps, "clocks": clocks,
                 "kernels": kernels, **extra, "wall_s_timed_region": wall}
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -619,35 +621,61 @@ def main(argv=None) -> int:
     return 0
 
 
-def run_e2e(wl, dev, stream, launches, bufs, outputs, steps, world, el_step):
+def run_e2e(wl, dev, stream, steps, world, el_step, noise):
     """The same step through the C ABI with inputs in pinned host memory: each step
-    copies its inputs host -> device, runs, and copies every result back."""
+    copies its inputs host -> device, runs, and copies every result back.
+
+    Two sets of device buffers alternate between steps, and the results are copied
+    back on a second stream, so step k's device->host copy overlaps step k+1's
+    host->device copy and kernels (the two copy directions use separate engines);
+    a set is reused only after its previous results have reached the host."""
     import torch
-    host_in = {k: v.detach().cpu().pin_memory() for k, v in bufs.items() if v is not None and v.numel()}
-    host_out = [o.detach().cpu().pin_memory() for o in outputs]
+    copy_stream = torch.cuda.Stream(dev)
+    sets = []
+    for _ in range(2):
+        launches, bufs, outputs = build_step(wl, dev, stream.cuda_stream, noise)
+        sets.append((launches, bufs, outputs))
+    host_in = {k: v.detach().cpu().pin_memory() for k, v in sets[0][1].items()
+               if v is not None and v.numel()}
+    host_out = [[o.detach().cpu().pin_memory() for o in st[2]] for st in sets]
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
-    d2h = sum(v.numel() * v.element_size() for v in host_out)
-    with torch.cuda.stream(stream):
-        def one():
-            for k, v in host_in.items():
-                bufs[k].copy_(v, non_blocking=True)
+    d2h = sum(v.numel() * v.element_size() for v in host_out[0])
+    computed = [torch.cuda.Event() for _ in sets]
+    copied = [torch.cuda.Event() for _ in sets]
+
+    def one(k):
+        launches, bufs, outputs = sets[k % 2]
+        with torch.cuda.stream(stream):
+            stream.wait_event(copied[k % 2])          # this set's last results are on the host
+            for name, v in host_in.items():
+                bufs[name].copy_(v, non_blocking=True)
             for l in launches:
                 l()
-            for o, h in zip(outputs, host_out):
+            computed[k % 2].record(stream)
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_event(computed[k % 2])
+            for o, h in zip(outputs, host_out[k % 2]):
                 h.copy_(o, non_blocking=True)
-        one()
-        torch.cuda.synchronize(dev)
-        barrier(world)
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(steps):
-            one()
-        b.record(stream)
-        torch.cuda.synchronize(dev)
+            copied[k % 2].record(copy_stream)
+
+    for c in copied:
+        c.record(copy_stream)
+    one(0)
+    one(1)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for k in range(steps):
+        one(k)
+    stream.wait_stream(copy_stream)
+    b.record(stream)
+    torch.cuda.synchronize(dev)
     ms = max_over_ranks(a.elapsed_time(b), world, dev)
     return {"value": el_step * steps * world / (ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": ms / steps}
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": ms / steps,
+            "copies": "results of step k copied back on a second stream while step k+1 runs"}
 
 
 if __name__ == "__main__":
