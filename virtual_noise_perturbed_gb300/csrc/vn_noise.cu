@@ -53,7 +53,9 @@ template <bool kIdx32, int kKind>
 __global__ void __launch_bounds__(kDumpThreads)
 noise_dump_kernel(const int64_t* __restrict__ seeds, int64_t n, uint64_t offset,
                   float* __restrict__ out, int64_t chunks_per_row, int64_t total_chunks,
-                  int vec4) {
+                  int vec4, uint32_t g_lo, uint32_t g_hi) {
+  // g_lo:g_hi = GAMMA, passed at run time: an add of register operands lets the
+  // compiler put the carry half of the state step on the IMAD pipe.
   for (int64_t c = blockIdx.x; c < total_chunks; c += gridDim.x) {
     const int64_t i = kIdx32 ? static_cast<int64_t>(static_cast<uint32_t>(c) /
                                                     static_cast<uint32_t>(chunks_per_row))
@@ -66,12 +68,12 @@ noise_dump_kernel(const int64_t* __restrict__ seeds, int64_t n, uint64_t offset,
       // The whole chunk lies inside the row: no per-group checks.
 #pragma unroll
       for (int g = 0; g < kDumpGroups; ++g) {
-        uint64_t st = gst;
+        uint32_t slo = static_cast<uint32_t>(gst), shi = static_cast<uint32_t>(gst >> 32);
         float v[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          v[q] = dump_value<kKind>(st);
-          st += kGamma;
+          v[q] = dump_value<kKind>((static_cast<uint64_t>(shi) << 32) | slo);
+          add64(slo, shi, g_lo, g_hi);
         }
         __stcs(reinterpret_cast<float4*>(row + t0 + g * kDumpStride),
                make_float4(v[0], v[1], v[2], v[3]));
@@ -181,10 +183,10 @@ void dump_launch(bool idx32, unsigned grid, cudaStream_t stream, const int64_t* 
                  uint64_t offset, float* out, int64_t chunks_per_row, int64_t total, int vec4) {
   if (idx32)
     noise_dump_kernel<true, kKind><<<grid, kDumpThreads, 0, stream>>>(
-        seeds, n, offset, out, chunks_per_row, total, vec4);
+        seeds, n, offset, out, chunks_per_row, total, vec4, kGammaLo, kGammaHi);
   else
     noise_dump_kernel<false, kKind><<<grid, kDumpThreads, 0, stream>>>(
-        seeds, n, offset, out, chunks_per_row, total, vec4);
+        seeds, n, offset, out, chunks_per_row, total, vec4, kGammaLo, kGammaHi);
 }
 
 cudaError_t launch_noise_dump(const int64_t* seeds, int64_t pop, int64_t n, uint64_t offset,
