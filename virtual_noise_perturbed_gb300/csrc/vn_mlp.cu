@@ -12,8 +12,9 @@
 // hundred units) a layer is a few microseconds of hashing, so separate
 // launches pay a launch gap and a full-device drain per layer, and the small
 // last layer cannot fill the GPU. Here an individual's activations never leave
-// shared memory: a CTA takes a contiguous slice of the population, P
-// individuals at a time, and runs them through every layer.
+// shared memory: a CTA takes a group of P consecutive individuals (P =
+// ceil(pop / SMs), at most 8 / batch, a compile-time constant) and runs them
+// through every layer.
 //
 // Work of one layer inside a CTA (16 warps):
 //   * A row of W_l is split into 8-element chunks; LR lanes (a power of two,
