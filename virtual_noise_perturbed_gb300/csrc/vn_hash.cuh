@@ -40,6 +40,17 @@ __device__ __forceinline__ void add64(uint32_t& lo, uint32_t& hi, uint32_t alo, 
       : "r"(alo), "r"(ahi));
 }
 
+// The same add with the high word as a multiply-add by `one` (a run-time 1
+// that the compiler cannot fold): the carry half then issues on the IMAD pipe
+// instead of the integer ALU, which the finalizer already keeps the busiest.
+// `one` must come from a kernel argument, not a literal.
+__device__ __forceinline__ void add64_madc(uint32_t& lo, uint32_t& hi, uint32_t alo, uint32_t ahi,
+                                           uint32_t one) {
+  asm("add.cc.u32 %0, %0, %2;\n\tmadc.lo.u32 %1, %1, %4, %3;"
+      : "+r"(lo), "+r"(hi)
+      : "r"(alo), "r"(ahi), "r"(one));
+}
+
 // (hi:lo) * GAMMA mod 2^64, on halves.
 __device__ __forceinline__ void mul_gamma(uint32_t lo, uint32_t hi, uint32_t& rlo, uint32_t& rhi) {
   const uint64_t p = static_cast<uint64_t>(lo) * kGammaLo;  // 32x32 -> 64

@@ -87,6 +87,7 @@ struct PopParams {
   int p;              // individuals staged at a time
   int kpw;            // k range of one pass = 8 warps * (32/R) * CPT * 8
   int w_vec;          // W rows are 16-byte aligned for 8-element vector loads
+  uint32_t g_lo, g_hi, one;  // GAMMA's halves and 1 at run time (the state step, add64_madc)
 };
 
 template <int NB, int CPT, bool kXBf16, bool kWBf16>
@@ -179,12 +180,13 @@ linear_pop_kernel(const LinearArgs a, const PopParams q) {
           for (int cq = 0; cq < CPT; ++cq) {
             {
               const int kk = min(8 * (slot + slots * cq), kpw - 8);
-              uint64_t st = bst[cq] + seed;
+              const uint64_t st = bst[cq] + seed;
+              uint32_t slo = static_cast<uint32_t>(st), shi = static_cast<uint32_t>(st >> 32);
               float wp[8];
 #pragma unroll
               for (int e = 0; e < 8; ++e) {
-                wp[e] = fmaf(sg[cq], __uint_as_float(mix_to_one_plus_u(st)), wm[cq][e]);
-                st += kGamma;
+                wp[e] = fmaf(sg[cq], __uint_as_float(mix_to_one_plus_u(slo, shi)), wm[cq][e]);
+                add64_madc(slo, shi, q.g_lo, q.g_hi, q.one);
               }
 #pragma unroll
               for (int r = 0; r < NB; ++r) {
@@ -260,6 +262,9 @@ cudaError_t launch_cfg(const LinearArgs& a, cudaStream_t stream, int sm_count, i
   const int LQ = 32 >> r_log2;
   PopParams q;
   q.r_log2 = r_log2;
+  q.g_lo = kGammaLo;
+  q.g_hi = kGammaHi;
+  q.one = 1u;
   // One pass covers kWarps * LQ * CPT chunks of 8; when `in` is shorter, only
   // its (8-rounded) length is staged.
   q.kpw = static_cast<int>(std::min<int64_t>(kWarps * LQ * CPT * 8,

@@ -82,9 +82,9 @@ struct TcParams {
   uint32_t stage_bytes, a_bytes, idesc;
   uint32_t w_bytes;  // one W tile in shared memory: 128 rows x 64 k of W's dtype
   unsigned long long timeout_ns;  // limit of every barrier wait
-  uint32_t g_lo, g_hi;            // GAMMA's halves, passed at run time: the state step is
-                                  // then a register-operand add whose carry half the
-                                  // compiler can issue on the IMAD pipe
+  uint32_t g_lo, g_hi, one;       // GAMMA's halves and 1, passed at run time: the state
+                                  // step's carry half is then a multiply-add on the IMAD
+                                  // pipe (add64_madc)
   long long withhold_stage;       // test hook: >= 0 makes one thread skip that stage's arrive
 };
 
@@ -558,7 +558,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
     auto rowq = [&](int q) { return row0 + q * kRowsPerPass; };
     const float sigma = p.sigma;
     const float shift = -1.5f * sigma;
-    const uint32_t g_lo = p.g_lo, g_hi = p.g_hi;
+    const uint32_t g_lo = p.g_lo, g_hi = p.g_hi, one = p.one;
 
     // This thread's chunk q inside a staged W tile (rows of 64 k, 256 bytes in
     // fp32, 128 in bf16). In fp32 the two 16-byte halves are read in an order
@@ -657,7 +657,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
               } else {
                 pv[e] = fmaf(sigma, __uint_as_float(mix_to_one_plus_u(slo, shi)), wm[q][e]);
               }
-              add64(slo, shi, g_lo, g_hi);
+              add64_madc(slo, shi, g_lo, g_hi, one);
             }
             st_shared_v4(a0 + soff(q), pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]),
                          pack_bf16x2(pv[4], pv[5]), pack_bf16x2(pv[6], pv[7]));
@@ -776,6 +776,7 @@ cudaError_t launch_linear_tc_hook(const LinearArgs& a, cudaStream_t stream, long
   p.timeout_ns = timeout_ns;
   p.g_lo = kGammaLo;
   p.g_hi = kGammaHi;
+  p.one = 1u;
   p.withhold_stage = withhold_stage;
   // Instruction descriptor: fp32 accumulator, bf16 A and B, both K-major,
   // N = nt (bits 17-22, N >> 3), M = 128 (bits 24-28, M >> 4).

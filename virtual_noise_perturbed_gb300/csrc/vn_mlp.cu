@@ -78,6 +78,7 @@ struct MlpDev {
   int x_bf16;   // x is bf16 (else fp32)
   int buf_len;  // floats per (individual, batch row) in an activation buffer, a multiple of 8
   float sigma;
+  uint32_t g_lo, g_hi, one;  // GAMMA's halves and 1, at run time (the state step, add64_madc)
 };
 
 // Eight weights of row j from column k (zeros outside the matrix).
@@ -198,12 +199,13 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant_
 #pragma unroll
       for (int ii = 0; ii < kP; ++ii) {
         const uint2 sd = s_seed[ii];
-        uint64_t st = bst + ((static_cast<uint64_t>(sd.y) << 32) | sd.x);
+        const uint64_t st = bst + ((static_cast<uint64_t>(sd.y) << 32) | sd.x);
+        uint32_t slo = static_cast<uint32_t>(st), shi = static_cast<uint32_t>(st >> 32);
         float wp[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          wp[e] = fmaf(sigma, __uint_as_float(mix_to_one_plus_u(st)), wm[e]);
-          st += kGamma;
+          wp[e] = fmaf(sigma, __uint_as_float(mix_to_one_plus_u(slo, shi)), wm[e]);
+          add64_madc(slo, shi, a.g_lo, a.g_hi, a.one);
         }
 #pragma unroll
         for (int r = 0; r < NB; ++r) {
@@ -393,6 +395,9 @@ cudaError_t launch_mlp(const MlpArgs& m, cudaStream_t stream) {
   d.act = m.act;
   d.buf_len = static_cast<int>(mlp_buffer_floats(m.n_layers, m.dims));
   d.sigma = m.sigma;
+  d.g_lo = kGammaLo;
+  d.g_hi = kGammaHi;
+  d.one = 1u;
   d.x_bf16 = m.x_dt == VN_BF16 ? 1 : 0;
   if (m.batch <= 1) return launch_nb<1>(d, stream, dev);
   if (m.batch <= 2) return launch_nb<2>(d, stream, dev);

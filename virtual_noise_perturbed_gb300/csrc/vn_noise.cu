@@ -53,9 +53,9 @@ template <bool kIdx32, int kKind>
 __global__ void __launch_bounds__(kDumpThreads)
 noise_dump_kernel(const int64_t* __restrict__ seeds, int64_t n, uint64_t offset,
                   float* __restrict__ out, int64_t chunks_per_row, int64_t total_chunks,
-                  int vec4, uint32_t g_lo, uint32_t g_hi) {
-  // g_lo:g_hi = GAMMA, passed at run time: an add of register operands lets the
-  // compiler put the carry half of the state step on the IMAD pipe.
+                  int vec4, uint32_t g_lo, uint32_t g_hi, uint32_t one) {
+  // g_lo:g_hi = GAMMA and one = 1, passed at run time: the carry half of the
+  // state step is then a multiply-add on the IMAD pipe (add64_madc).
   for (int64_t c = blockIdx.x; c < total_chunks; c += gridDim.x) {
     const int64_t i = kIdx32 ? static_cast<int64_t>(static_cast<uint32_t>(c) /
                                                     static_cast<uint32_t>(chunks_per_row))
@@ -73,7 +73,7 @@ noise_dump_kernel(const int64_t* __restrict__ seeds, int64_t n, uint64_t offset,
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           v[q] = dump_value<kKind>((static_cast<uint64_t>(shi) << 32) | slo);
-          add64(slo, shi, g_lo, g_hi);
+          add64_madc(slo, shi, g_lo, g_hi, one);
         }
         __stcs(reinterpret_cast<float4*>(row + t0 + g * kDumpStride),
                make_float4(v[0], v[1], v[2], v[3]));
@@ -119,7 +119,8 @@ template <bool kCluster>
 __global__ void __launch_bounds__(kMetricThreads)
 reduce_metric_kernel(const float* __restrict__ center, const int64_t* __restrict__ seeds,
                      int64_t pop, int64_t n, float sigma, float inv_n, uint64_t offset,
-                     float* __restrict__ fitness, int vec4) {
+                     float* __restrict__ fitness, int vec4, uint32_t g_lo, uint32_t g_hi,
+                     uint32_t one) {
   __shared__ float s_warp[kMetricThreads / 32];
   __shared__ float s_cta;
   const int slices = gridDim.y;
@@ -136,10 +137,11 @@ reduce_metric_kernel(const float* __restrict__ center, const int64_t* __restrict
       if (vec4 && k + 4 <= k_end) {  // the common case: four in-range elements, no checks
         const float4 c4 = __ldg(reinterpret_cast<const float4*>(center + k));
         const float c[4] = {c4.x, c4.y, c4.z, c4.w};
+        uint32_t slo = static_cast<uint32_t>(st), shi = static_cast<uint32_t>(st >> 32);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          acc += fabsf(fmaf(sigma, noise_from_bits(mix_to_one_plus_u(st)), c[q]));
-          st += kGamma;
+          acc += fabsf(fmaf(sigma, noise_from_bits(mix_to_one_plus_u(slo, shi)), c[q]));
+          add64_madc(slo, shi, g_lo, g_hi, one);
         }
       } else {
 #pragma unroll
@@ -183,10 +185,10 @@ void dump_launch(bool idx32, unsigned grid, cudaStream_t stream, const int64_t* 
                  uint64_t offset, float* out, int64_t chunks_per_row, int64_t total, int vec4) {
   if (idx32)
     noise_dump_kernel<true, kKind><<<grid, kDumpThreads, 0, stream>>>(
-        seeds, n, offset, out, chunks_per_row, total, vec4, kGammaLo, kGammaHi);
+        seeds, n, offset, out, chunks_per_row, total, vec4, kGammaLo, kGammaHi, 1u);
   else
     noise_dump_kernel<false, kKind><<<grid, kDumpThreads, 0, stream>>>(
-        seeds, n, offset, out, chunks_per_row, total, vec4, kGammaLo, kGammaHi);
+        seeds, n, offset, out, chunks_per_row, total, vec4, kGammaLo, kGammaHi, 1u);
 }
 
 cudaError_t launch_noise_dump(const int64_t* seeds, int64_t pop, int64_t n, uint64_t offset,
@@ -224,7 +226,7 @@ cudaError_t launch_reduce_metric(const float* center, const int64_t* seeds, int6
   if (slices == 1) {
     const int64_t grid = std::min<int64_t>(pop, resident);
     reduce_metric_kernel<false><<<static_cast<unsigned>(grid), kMetricThreads, 0, stream>>>(
-        center, seeds, pop, n, sigma, inv_n, offset, fitness, vec4);
+        center, seeds, pop, n, sigma, inv_n, offset, fitness, vec4, kGammaLo, kGammaHi, 1u);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
@@ -240,7 +242,7 @@ cudaError_t launch_reduce_metric(const float* center, const int64_t* seeds, int6
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, reduce_metric_kernel<true>, center, seeds, pop, n, sigma, inv_n,
-                            offset, fitness, vec4);
+                            offset, fitness, vec4, kGammaLo, kGammaHi, 1u);
 }
 
 }  // namespace vn
