@@ -583,19 +583,22 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
     // State term step from one k chunk to the next: 64 * GAMMA mod 2^64.
     constexpr uint64_t kChunkStep = static_cast<uint64_t>(kKC) * kGamma;
 
-    Ring rg, wr;
+    // Ring positions (slot, parity) of the stages and of the W tiles; barrier
+    // addresses are formed from them directly.
+    const uint32_t S32 = static_cast<uint32_t>(S);
+    const uint32_t stage_bytes = p.stage_bytes;
+    const uint32_t fa0 = full_a(0), em0 = empty(0), fw0 = full_w(0), ew0 = empty_w(0);
+    const uint32_t a_this = stage0 + soff0;   // this thread's first chunk in stage 0
+    const uint32_t w_this = wslot0 + woff(0);
+    const uint32_t w_bytes = p.w_bytes;
+    const int k_chunks = p.k_chunks;
+    uint32_t s = 0, ph = 0, ws = 0, wph = 0;
     // Test hook: the stage at which this thread skips its arrive (-1: never).
     int withhold_at = (kHook && p.withhold_stage >= 0 && p.withhold_stage < 0x7FFFFFFF &&
                        blockIdx.x == 0 && t == 0) ? static_cast<int>(p.withhold_stage) : -1;
-    bool ok = true;
-    int64_t u = blockIdx.x;
-    // The seed of the next stage is loaded one stage ahead.
-    uint64_t seed_next = (u < p.units) ? static_cast<uint64_t>(__ldg(p.seeds + decode(p, u, MH).i0))
-                                       : 0ull;
-    for (; ok && u < p.units; u += gridDim.x) {
+    for (int64_t u = blockIdx.x; u < p.units; u += gridDim.x) {
       const Unit un = decode(p, u, MH);
-      const bool has_next_unit = u + gridDim.x < p.units;
-      const int next_i0 = has_next_unit ? decode(p, u + gridDim.x, MH).i0 : un.i0;
+      const int64_t* seedp = p.seeds + un.i0;
       // (offset + j*in + k + 1) * GAMMA of each chunk's first element, k chunk 0;
       // advanced by kChunkStep per k chunk.
       uint64_t bst[kCPT];
@@ -605,7 +608,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                             static_cast<uint64_t>(un.m0 + rowq(q)) * static_cast<uint64_t>(p.in) +
                             static_cast<uint64_t>(cc * 8));
       }
-      for (int kc = 0; ok && kc < p.k_chunks; ++kc) {
+      for (int kc = 0; kc < k_chunks; ++kc) {
         // This stage group's W chunks, shared by its G individuals: fp32 W is
         // kept as W - 1.5*sigma and perturbed with one FMA per element; bf16 W
         // stays packed and each element is formed as fp32(bf16 W) + sigma*n
@@ -614,14 +617,14 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
         // at ragged edges) are TMA's zero fill, so their values are finite:
         // their X columns are zero fill too (k >= in) or their output rows are
         // never stored (row >= out), and no masking is needed below.
-        if (!(ok = mbar_wait(full_w(wr.s), wr.ph, s_abort))) break;
+        if (!mbar_wait(fw0 + 8u * ws, wph, s_abort)) goto hashing_done;
         float wm[kCPT][8];
         Raw wraw[kCPT];
         {
-          const uint32_t wb = wslot0 + wr.s * p.w_bytes;
+          const uint32_t wb = w_this + ws * w_bytes;
 #pragma unroll
           for (int q = 0; q < kCPT; ++q) {
-            load_w(wb + woff(q), wraw[q]);
+            load_w(wb + q * (kRowsPerPass * kWRow), wraw[q]);
             if constexpr (!kWBf16) unpack_shift(wraw[q], shift, wm[q]);
           }
         }
@@ -629,18 +632,12 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
         // thread's generic-proxy reads of it before that write. Without the
         // fence a late warp's reads could return the next tile's values.
         fence_proxy_async_smem();
-        mbar_arrive(empty_w(wr.s));
-        wr.next(2);
-        for (int ii = 0; ii < un.gcount; ++ii, rg.next(S)) {
-          const int s = rg.s;
-          const uint64_t seed = seed_next;
-          // the individual of the next stage: next in the group, else the group's
-          // first (next k chunk), else the next unit's first (selected, not branched)
-          const int nidx = (ii + 1 < un.gcount) ? un.i0 + ii + 1
-                           : (kc + 1 < p.k_chunks) ? un.i0 : next_i0;
-          seed_next = static_cast<uint64_t>(__ldg(p.seeds + nidx));
-          if (!(ok = mbar_wait(empty(s), rg.ph ^ 1u, s_abort))) break;
-          const uint32_t a0 = stage0 + s * p.stage_bytes;
+        mbar_arrive(ew0 + 8u * ws);
+        if (++ws == 2) { ws = 0; wph ^= 1u; }
+        for (int ii = 0; ii < un.gcount; ++ii) {
+          const uint64_t seed = static_cast<uint64_t>(__ldg(seedp + ii));
+          if (!mbar_wait(em0 + 8u * s, ph ^ 1u, s_abort)) goto hashing_done;
+          const uint32_t a0 = a_this + s * stage_bytes;
 #pragma unroll
           for (int q = 0; q < kCPT; ++q) {
             const uint64_t st0 = bst[q] + seed;
@@ -650,30 +647,33 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
             for (int e = 0; e < 8; ++e) {
               if constexpr (kWBf16) {
                 // sigma*n = fma(sigma, 1 + u, -1.5*sigma), then + W straight from its bf16 bits.
-                const float t = fmaf(sigma, __uint_as_float(mix_to_one_plus_u(slo, shi)), shift);
+                const float tt = fmaf(sigma, __uint_as_float(mix_to_one_plus_u(slo, shi)), shift);
                 const uint32_t wv = (e & 4) ? ((e & 2) ? wraw[q].a.w : wraw[q].a.z)
                                             : ((e & 2) ? wraw[q].a.y : wraw[q].a.x);
-                pv[e] = (e & 1) ? add_bf16_f32<true>(wv, t) : add_bf16_f32<false>(wv, t);
+                pv[e] = (e & 1) ? add_bf16_f32<true>(wv, tt) : add_bf16_f32<false>(wv, tt);
               } else {
                 pv[e] = fmaf(sigma, __uint_as_float(mix_to_one_plus_u(slo, shi)), wm[q][e]);
               }
               add64_madc(slo, shi, g_lo, g_hi, one);
             }
-            st_shared_v4(a0 + soff(q), pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]),
-                         pack_bf16x2(pv[4], pv[5]), pack_bf16x2(pv[6], pv[7]));
+            st_shared_v4(a0 + q * (kRowsPerPass * 128u), pack_bf16x2(pv[0], pv[1]),
+                         pack_bf16x2(pv[2], pv[3]), pack_bf16x2(pv[4], pv[5]),
+                         pack_bf16x2(pv[6], pv[7]));
           }
           fence_proxy_async_smem();
           if constexpr (kHook) {
-            if (withhold_at != 0) mbar_arrive(full_a(s));
+            if (withhold_at != 0) mbar_arrive(fa0 + 8u * s);
             if (withhold_at >= 0) --withhold_at;
           } else {
-            mbar_arrive(full_a(s));
+            mbar_arrive(fa0 + 8u * s);
           }
+          if (++s == S32) { s = 0; ph ^= 1u; }
         }
 #pragma unroll
         for (int q = 0; q < kCPT; ++q) bst[q] += kChunkStep;
       }
     }
+  hashing_done:;
   }
 
   tc_fence_before();
