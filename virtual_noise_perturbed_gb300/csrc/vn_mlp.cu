@@ -172,12 +172,20 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant_
     const int steps = my_rg * cpl;
     const uint64_t bias_base = Loff + static_cast<uint64_t>(Lout) * static_cast<uint64_t>(Lin);
 
+    // State term step between a lane's consecutive chunks of a row (8*LR elements).
+    const uint64_t chunk_step = static_cast<uint64_t>(8 << lr_log2) * kGamma;
+
     float part[kP][NB];
     float wn[8];
+    uint64_t bst = 0;  // (Loff + j*in + k + 1) * GAMMA of the current chunk's first element
     if (steps > 0) load_w8(Lw, Lin, Lout, wvec, warp * rows_per_group + rsub, q * 8, wn);
     for (int s = 0, rgi = 0, m = 0; s < steps; ++s) {
       const int j = (warp + rgi * kWarps) * rows_per_group + rsub;
       const int k = (q + (m << lr_log2)) * 8;
+      // A row's first chunk: its state term from the index; the next ones add chunk_step.
+      bst = (m == 0) ? index_term(Loff + static_cast<uint64_t>(j) * static_cast<uint64_t>(Lin) +
+                                  static_cast<uint64_t>(k))
+                     : bst + chunk_step;
       if (m == 0) {
 #pragma unroll
         for (int ii = 0; ii < kP; ++ii)
@@ -193,8 +201,6 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant_
       if (s + 1 < steps)
         load_w8(Lw, Lin, Lout, wvec, (warp + rgi1 * kWarps) * rows_per_group + rsub,
                 (q + (m1 << lr_log2)) * 8, wn);
-      const uint64_t bst = index_term(Loff + static_cast<uint64_t>(j) * static_cast<uint64_t>(Lin) +
-                                      static_cast<uint64_t>(k));
       const float* hk = src + k;
 #pragma unroll
       for (int ii = 0; ii < kP; ++ii) {
@@ -232,22 +238,25 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant_
             for (int r = 0; r < NB; ++r)
               part[ii][r] += __shfl_xor_sync(0xffffffffu, part[ii][r], o);
         }
+        // Lane q of the row's group finishes the (individual, batch row) pairs
+        // pr = ii*NB + r congruent to q mod LR: bias, bias noise, activation.
         if (j < Lout) {
           const float bj = Lb != nullptr ? __ldg(Lb + j) : 0.f;
+          constexpr int kPairs = kP * NB;
+          for (int base = 0; base < kPairs; base += LR) {
+            const int pr = base + q;
+            if (pr < kPairs) {
+              float v = part[0][0];
 #pragma unroll
-          for (int ii = 0; ii < kP; ++ii) {
-#pragma unroll
-            for (int r = 0; r < NB; ++r) {
-              if (((ii * NB + r) & (LR - 1)) == q) {
-                float v = part[ii][r];
-                if (Lb != nullptr) {
-                  const uint2 sd = s_seed[ii];
-                  const uint64_t seed = (static_cast<uint64_t>(sd.y) << 32) | sd.x;
-                  v += fmaf(sigma, noise_at(seed, bias_base + static_cast<uint64_t>(j)), bj);
-                }
-                if (tanh_act) v = tanhf(v);
-                dst[(ii * NB + r) * blen + j] = v;
+              for (int t = 1; t < kPairs; ++t)
+                if (pr == t) v = part[t / NB][t % NB];
+              if (Lb != nullptr) {
+                const uint2 sd = s_seed[pr / NB];
+                const uint64_t seed = (static_cast<uint64_t>(sd.y) << 32) | sd.x;
+                v += fmaf(sigma, noise_at(seed, bias_base + static_cast<uint64_t>(j)), bj);
               }
+              if (tanh_act) v = tanhf(v);
+              dst[pr * blen + j] = v;
             }
           }
         }
