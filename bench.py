@@ -11,6 +11,7 @@ whole hot path over one population:
     out by compute_offsets one after another, so they are one flat range of
     element indices and one reduction over the population computes them all,
   * update: the flat parameter vector (the layers are views of it) += lr * grad,
+    applied by the gradient launch as it stores each element (vn_gradient_update),
   * noise dump: the centered-uniform noise of the whole flat parameter vector
     (84,488 elements) for every individual,
 so each step regenerates the population's parameter noise three times.
@@ -20,10 +21,16 @@ Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl vn|reference]
 For N > 1 launch with torch.distributed.run: every rank runs its own population
 (seeds offset by rank * pop), no data-path collective (weak scaling).
 
-Timing: W untimed warm-up steps, then K steps between barriers and device
-synchronisations; every kernel launch is bracketed by CUDA events on the
-launching stream and a 256 MiB buffer is rewritten between steps (outside the
-events) so that each step starts with a cold L2. Rank 0 prints one JSON line.
+Timing: W untimed warm-up steps, then two timed passes between barriers and
+device synchronisations, each rewriting a 256 MiB buffer between steps (outside
+the events) so that every step starts with a cold L2:
+  * the step pass: K steps, each bracketed by one pair of CUDA events on the
+    launching stream -> ms_per_step and value;
+  * the kernel pass: the same launches again (--kernel-steps, default K), every
+    launch bracketed by its own pair of events -> per-kernel durations, shares
+    and the dominant kernel's roofline. (An event pair around each launch adds
+    its own gap between launches, so it is kept out of the step pass.)
+Rank 0 prints one JSON line.
 """
 
 from __future__ import annotations
@@ -213,18 +220,22 @@ def build_step(wl, dev, stream_ptr, noise="uniform"):
         # element indices: one reduction over the population gives every block's
         # gradient as a slice (grad_W of layer l = flat[off_l : off_l + out*in]).
         g = torch.empty((n_params,), dtype=torch.float32, device=dev)
-        launches.append(Launch("grad", lib.vn_bias_gradient,
-                               (P(fit.data_ptr()), P(d.seeds.data_ptr()), pop, n_params,
-                                float(wl.sigma), wl.layers[0].offset, P(g.data_ptr()), s),
-                               pop * n_params, hbm_bytes=g.numel() * 4, grad_w_elems=sum(
-                                   l.out_f * l.in_f for l in wl.layers)))
-        outputs.append(g)
+        gw_elems = sum(l.out_f * l.in_f for l in wl.layers)
         if theta is not None:
-            # The ES step on the parameters: theta += lr * grad (lr fixed for the bench).
-            launches.append(Launch("es_update", lib.vn_es_update,
-                                   (P(theta.data_ptr()), P(g.data_ptr()), n_params, ES_LR, s), 0,
-                                   hbm_bytes=n_params * 12))
-            outputs.append(theta)
+            # The estimate and the ES step on the parameters, theta += lr * grad (lr
+            # fixed for the bench), in one launch (vn_gradient_update).
+            launches.append(Launch("grad", lib.vn_gradient_update,
+                                   (P(fit.data_ptr()), P(d.seeds.data_ptr()), pop, n_params,
+                                    float(wl.sigma), wl.layers[0].offset, _lib.VN_NOISE_UNIFORM,
+                                    ES_LR, P(g.data_ptr()), P(theta.data_ptr()), s),
+                                   pop * n_params, hbm_bytes=n_params * 12, grad_w_elems=gw_elems))
+            outputs += [g, theta]
+        else:
+            launches.append(Launch("grad", lib.vn_bias_gradient,
+                                   (P(fit.data_ptr()), P(d.seeds.data_ptr()), pop, n_params,
+                                    float(wl.sigma), wl.layers[0].offset, P(g.data_ptr()), s),
+                                   pop * n_params, hbm_bytes=g.numel() * 4, grad_w_elems=gw_elems))
+            outputs.append(g)
     for li, l in enumerate(d.layers if (wl.grads and not flat and noise == "gaussian") else []):
         # The Gaussian-noise variant: the same flat ranges (weights row-major, then
         # the bias block) through the noise-kind entry point.
@@ -468,6 +479,8 @@ def main(argv=None) -> int:
     ap.add_argument("--workload", default="es_mlp",
                     choices=["tiny", "es_mlp", "mid", "grad_only", "large_tc"])
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--kernel-steps", type=int, default=None,
+                    help="steps of the per-kernel timing pass (default: --steps)")
     ap.add_argument("--pop", type=int, default=None,
                     help="run only the workload's first POP individuals (smaller profiling cases)")
     ap.add_argument("--noise", choices=["uniform", "gaussian"], default="uniform",
@@ -514,29 +527,46 @@ def main(argv=None) -> int:
                 l()
             flush.zero_()
         torch.cuda.synchronize(dev)
+        # Two timed passes over the same launches. The step pass brackets each step
+        # with one pair of events (an event pair around every launch would add its own
+        # gaps to the step); the kernel pass brackets every launch, for the per-kernel
+        # durations, shares and the roofline of the dominant kernel.
+        k_steps = args.steps
+        k_kern = args.kernel_steps if args.kernel_steps is not None else args.steps
+        ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(k_steps)]
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(launches))]
-              for _ in range(args.steps)]
+              for _ in range(k_kern)]
         barrier(world)
         torch.cuda.synchronize(dev)
         sampler = ClockSampler(gpu_id(dev))
         wall0 = time.perf_counter()
-        for k in range(args.steps):
+        for k in range(k_steps):
+            ev_step[k][0].record(stream)
+            for l in launches:
+                l()
+            ev_step[k][1].record(stream)
+            flush.zero_()
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - wall0
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        for k in range(k_kern):
             for j, l in enumerate(launches):
                 ev[k][2 * j].record(stream)
                 l()
                 ev[k][2 * j + 1].record(stream)
             flush.zero_()
         torch.cuda.synchronize(dev)
-        wall = time.perf_counter() - wall0
         clocks = sampler.stop()
         barrier(world)
     status = _lib.load().vn_device_status(ctypes.c_void_p(stream.cuda_stream))
     if status != 0:
         raise _lib.VNError(status, "bench")
 
-    step_ms = [ev[k][0].elapsed_time(ev[k][-1]) for k in range(args.steps)]
+    step_ms = [a.elapsed_time(b) for a, b in ev_step]
     per_kernel = {}
-    for k in range(args.steps):
+    for k in range(k_kern):
         for j, l in enumerate(launches):
             ms = ev[k][2 * j].elapsed_time(ev[k][2 * j + 1])
             rec = per_kernel.setdefault(l.kernel, {"ms": 0.0, "launches": 0, "elements": 0, "flops": 0.0,
@@ -612,7 +642,7 @@ def main(argv=None) -> int:
                 "warmup": args.warmup, "ms_per_step": total_ms_max / args.steps, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f32" if wl.number in (1, 2) else "bf16",
                 "data": "synthetic", "config": cfg, "roofline": roofline, "cpu_baseline": cpu,
-                "e2e": e2e, "gpu_launches": n_launches * args.steps, "clocks": clocks,
+                "e2e": e2e, "gpu_launches": n_launches * (k_steps + k_kern), "clocks": clocks,
                 "kernels": kernels, **extra, "wall_s_timed_region": wall}
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -175,6 +175,20 @@ vn_status vn_gradient_ex(const float* fitness, const int64_t* seeds, int64_t pop
                          double sigma, uint64_t offset, vn_noise kind, float* grad, void* stream);
 
 /*
+ * vn_gradient_update -- vn_gradient_ex and vn_es_update in one launch: the
+ * gradient estimate over a flat range of n parameters and the ES step on it,
+ *     grad[e]  = sum_i fitness[i] * noise_kind(seed_i, offset + e) / (pop * sigma)
+ *     theta[e] = fma(lr, grad[e], theta[e])                      (fp32, in place)
+ * for e < n (the module description's estimate, ascended with step lr). grad and
+ * theta are both bit-identical to vn_gradient_ex followed by vn_es_update(theta,
+ * grad, n, lr). theta [n] fp32, 4-byte aligned, must not overlap grad, fitness
+ * or seeds; lr finite. Other arguments, conventions and errors as vn_gradient_ex.
+ */
+vn_status vn_gradient_update(const float* fitness, const int64_t* seeds, int64_t pop, int64_t n,
+                             double sigma, uint64_t offset, vn_noise kind, double lr, float* grad,
+                             float* theta, void* stream);
+
+/*
  * vn_reduce_metric -- "virtual_reduce_metric" (API entry of the page):
  *     fitness[i] = mean_k | center[k] + sigma * PRNG(seed_i, offset + k) |
  * center [n_params] fp32, seeds [pop] int64, fitness [pop] fp32. n_params >= 1;

@@ -153,3 +153,17 @@ def test_noise_kind_validation(lib):
     assert lib.vn_gradient_ex(P(fake), P(fake), 1, 4, 0.1, 0, 2, P(fake), P(0)) == 4
     assert lib.vn_gradient_ex(P(fake), P(fake), 0, 4, 0.1, 0, 1, P(fake), P(0)) == 2
     assert lib.vn_gradient_ex(P(fake), P(fake), 4, 4, 0.0, 0, 1, P(fake), P(0)) == 4
+
+
+def test_gradient_update_validation(lib):
+    fake = 0x1000
+    gu = lib.vn_gradient_update
+    # (fitness, seeds, pop, n, sigma, offset, kind, lr, grad, theta, stream)
+    assert gu(P(fake), P(fake), 4, 4, 0.1, 0, 0, 0.1, P(fake), P(0), P(0)) == 1       # theta NULL
+    assert gu(P(fake), P(fake), 4, 4, 0.1, 0, 0, float("nan"), P(fake), P(fake + 64), P(0)) == 4
+    assert gu(P(fake), P(fake), 4, 4, 0.0, 0, 0, 0.1, P(fake), P(fake + 64), P(0)) == 4  # sigma 0
+    assert gu(P(fake), P(fake), 0, 4, 0.1, 0, 0, 0.1, P(fake), P(fake + 64), P(0)) == 2  # pop 0
+    assert gu(P(fake), P(fake), 4, 4, 0.1, 0, 3, 0.1, P(fake), P(fake + 64), P(0)) == 4  # kind
+    assert gu(P(fake), P(fake), 4, 4, 0.1, 0, 0, 0.1, P(fake), P(fake + 66), P(0)) == 5  # theta align
+    assert gu(P(fake), P(fake), 4, 4, 0.1, 0, 0, 0.1, P(fake), P(fake + 8), P(0)) == 4   # theta overlaps grad
+    assert gu(P(fake), P(fake), 4, 0, 0.1, 0, 0, 0.1, P(0), P(0), P(0)) == 0             # empty

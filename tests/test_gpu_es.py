@@ -12,7 +12,8 @@ import torch
 from oracle import es
 from tests.parity import TOL_FP32, assert_close, to_np
 from virtual_noise_perturbed_gb300 import (VNError, centered_ranks, compute_offsets, es_update,
-                                           virtual_flat_gradient, virtual_perturbed_mlp, workloads)
+                                           gradient_update, virtual_flat_gradient,
+                                           virtual_perturbed_mlp, workloads)
 from virtual_noise_perturbed_gb300.build import build
 
 pytestmark = pytest.mark.gpu
@@ -101,3 +102,35 @@ def test_one_es_generation_of_the_policy():
     assert_close(to_np(grad), grad_ref, TOL_FP32, "generation gradient")
     delta = theta.cpu().numpy().astype(np.float64) - theta0.numpy().astype(np.float64)
     assert_close(delta, float(np.float32(lr)) * grad_ref, TOL_FP32, "generation update")
+
+
+@pytest.mark.parametrize("n,pop,noise", [(1, 3, "uniform"), (255, 64, "uniform"), (84488, 1024, "uniform"),
+                                         (70001, 300, "uniform"), (4096 * 33 + 7, 4096, "uniform"),
+                                         (5000, 257, "gaussian")])
+def test_gradient_update_matches_the_two_launches(n, pop, noise):
+    """The fused estimate + step gives the same bits as vn_gradient_ex followed by
+    vn_es_update, for the cluster-split sizes (small n) and the plain ones (large n),
+    both noise kinds; and its gradient is the oracle's within the fp32 tolerance."""
+    g = torch.Generator().manual_seed(n + pop)
+    f = torch.randn(pop, generator=g).to(DEV)
+    seeds = (torch.arange(pop, dtype=torch.int64) * 7 - 3).to(DEV)
+    theta0 = torch.randn(n, generator=g).to(DEV)
+    sigma, lr, off = 0.02, 0.05, 12345
+    theta_fused = theta0.clone()
+    grad_fused = gradient_update(f, seeds, theta_fused, sigma, pop, lr, off, noise=noise)
+    grad_two = virtual_flat_gradient(f, seeds, n, sigma, pop, off, noise=noise)
+    theta_two = es_update(theta0.clone(), grad_two, lr)
+    torch.cuda.synchronize()
+    assert torch.equal(grad_fused, grad_two)
+    assert torch.equal(theta_fused, theta_two)
+    if noise == "uniform" and n * pop <= 10 ** 7:
+        want = es.bias_gradient(f.cpu().numpy(), seeds.cpu().numpy(), (n,), sigma, pop, off)
+        assert_close(to_np(grad_fused), want, TOL_FP32, "fused gradient")
+
+
+def test_gradient_update_refusals():
+    theta = torch.zeros(8, device=DEV)
+    with pytest.raises(ValueError):
+        gradient_update(torch.ones(4, device=DEV), torch.arange(4, device=DEV), theta.double(), 0.1, 4, 0.1)
+    with pytest.raises(VNError):
+        gradient_update(torch.ones(4, device=DEV), torch.arange(4, device=DEV), theta, 0.1, 4, float("inf"))

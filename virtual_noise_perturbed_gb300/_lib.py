@@ -45,6 +45,7 @@ SIGNATURES = {
     "vn_es_update": (_I, [_P, _P, _I64, _D, _P]),
     "vn_noise_dump_ex": (_I, [_P, _I64, _I64, _U64, _I, _P, _P]),
     "vn_gradient_ex": (_I, [_P, _P, _I64, _I64, _D, _U64, _I, _P, _P]),
+    "vn_gradient_update": (_I, [_P, _P, _I64, _I64, _D, _U64, _I, _D, _P, _P, _P]),
     "vn_device_status": (_I, [_P]),
     "vn_testhook_linear_tc_withhold": (_I, [_P, _I, _I, _P, _I, _P, _I, _P, _I64, _I64, _I64, _I64,
                                            _D, _U64, _P, _I, _I64, _D, _P]),

@@ -231,6 +231,28 @@ def virtual_flat_gradient(fitness: torch.Tensor, seeds: torch.Tensor, n_params: 
     return g
 
 
+def gradient_update(fitness: torch.Tensor, seeds: torch.Tensor, theta: torch.Tensor, sigma: float,
+                    pop_size: int, lr: float, offset: int = 0, *, noise: str = "uniform") -> torch.Tensor:
+    """The flat gradient estimate and the ES step in one launch (``vn_gradient_update``):
+    grad = virtual_flat_gradient(fitness, seeds, theta.numel(), sigma, pop_size, offset),
+    then theta += lr * grad in place (fp32 fma). Returns grad; both are bit-identical
+    to the two separate calls."""
+    lib = load()
+    if noise not in _NOISE:
+        raise ValueError("noise must be 'uniform' or 'gaussian'")
+    if not isinstance(theta, torch.Tensor) or not theta.is_cuda or not theta.is_contiguous() \
+            or theta.dtype != torch.float32:
+        raise ValueError("theta must be a contiguous float32 CUDA tensor (updated in place)")
+    seeds = _seeds(seeds)
+    fitness = _fitness(fitness, pop_size, seeds)
+    g = torch.empty((theta.numel(),), dtype=torch.float32, device=theta.device)
+    st = lib.vn_gradient_update(_ptr(fitness), _ptr(seeds), pop_size, theta.numel(), float(sigma),
+                                int(offset) & _M64, _NOISE[noise], float(lr), _ptr(g), _ptr(theta),
+                                _stream(g))
+    check(st, "vn_gradient_update")
+    return g
+
+
 def noise_dump(seeds: torch.Tensor, n_elements: int, offset: int, *,
                noise: str = "uniform") -> torch.Tensor:
     """(pop, n) fp32 noise, D[i, t] = PRNG(seed_i, offset + t): the centered uniform

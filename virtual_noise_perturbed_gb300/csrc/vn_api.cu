@@ -117,7 +117,7 @@ vn_status vn_noise_dump_ex(const int64_t* seeds, int64_t pop, int64_t n, uint64_
 
 static vn_status gradient(const float* fitness, const int64_t* seeds, int64_t pop, int64_t m_rows,
                           int64_t m_cols, double sigma, uint64_t offset, vn_noise kind,
-                          float* grad, void* stream) {
+                          float* grad, void* stream, float* theta = nullptr, double lr = 0.0) {
   if (kind != VN_NOISE_UNIFORM && kind != VN_NOISE_GAUSSIAN) return VN_ERR_VALUE;
   if (pop < 1 || m_rows < 0 || m_cols < 0) return VN_ERR_SHAPE;
   int64_t m;
@@ -127,11 +127,19 @@ static vn_status gradient(const float* fitness, const int64_t* seeds, int64_t po
   const double inv = 1.0 / (static_cast<double>(pop) * sigma);
   const float scale = static_cast<float>(inv);
   if (!std::isfinite(scale) || scale == 0.f) return VN_ERR_VALUE;
+  float lr_f = 0.f;
+  if (theta != nullptr && !float_sigma(lr, &lr_f)) return VN_ERR_VALUE;
   if (m == 0) return VN_OK;
   if (fitness == nullptr || seeds == nullptr || grad == nullptr) return VN_ERR_NULL;
   if (!aligned(fitness, 4) || !aligned(seeds, 8) || !aligned(grad, 4)) return VN_ERR_ALIGN;
+  if (theta != nullptr) {
+    if (!aligned(theta, 4)) return VN_ERR_ALIGN;
+    const uintptr_t t0 = reinterpret_cast<uintptr_t>(theta), g0 = reinterpret_cast<uintptr_t>(grad);
+    const uintptr_t bytes = static_cast<uintptr_t>(m) * 4;
+    if (t0 < g0 + bytes && g0 < t0 + bytes) return VN_ERR_VALUE;  // theta and grad overlap
+  }
   return launched(vn::launch_grad(fitness, seeds, pop, m, offset, scale, kind, grad,
-                                  static_cast<cudaStream_t>(stream)));
+                                  static_cast<cudaStream_t>(stream), theta, lr_f));
 }
 
 vn_status vn_weight_gradient(const float* fitness, const int64_t* seeds, int64_t pop,
@@ -149,6 +157,18 @@ vn_status vn_bias_gradient(const float* fitness, const int64_t* seeds, int64_t p
 vn_status vn_gradient_ex(const float* fitness, const int64_t* seeds, int64_t pop, int64_t n,
                          double sigma, uint64_t offset, vn_noise kind, float* grad, void* stream) {
   return gradient(fitness, seeds, pop, n, 1, sigma, offset, kind, grad, stream);
+}
+
+vn_status vn_gradient_update(const float* fitness, const int64_t* seeds, int64_t pop, int64_t n,
+                             double sigma, uint64_t offset, vn_noise kind, double lr, float* grad,
+                             float* theta, void* stream) {
+  if (n > 0 && theta == nullptr) return VN_ERR_NULL;
+  if (theta == nullptr) {  // n == 0: validate as the plain estimate does, launch nothing
+    float lr_f;
+    if (!float_sigma(lr, &lr_f)) return VN_ERR_VALUE;
+    return gradient(fitness, seeds, pop, n, 1, sigma, offset, kind, grad, stream);
+  }
+  return gradient(fitness, seeds, pop, n, 1, sigma, offset, kind, grad, stream, theta, lr);
 }
 
 vn_status vn_reduce_metric(const float* center, const int64_t* seeds, int64_t pop,

@@ -21,6 +21,9 @@
 //     S partial tiles are added through distributed shared memory in rank
 //     order. Every sum is taken in a fixed order, so the result is
 //     deterministic for a given device and shape.
+//   * With a parameter vector theta (the fused ES step), the thread that
+//     stores grad[e] also applies theta[e] = fma(lr, grad[e], theta[e]): the
+//     same values as a separate update launch, without it.
 #include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
@@ -40,10 +43,11 @@ constexpr int kE = 8;           // consecutive elements per lane
 constexpr int kTile = 32 * kE;  // elements per CTA tile
 constexpr int kStage = 256;     // individuals staged per round
 
-template <bool kCluster, int kKind>
+template <bool kCluster, int kKind, bool kUpdate>
 __global__ void __launch_bounds__(kThreads)
 grad_kernel(const float* __restrict__ fitness, const int64_t* __restrict__ seeds, int64_t pop,
-            int64_t m, uint64_t offset, float scale, float* __restrict__ out, int64_t tiles) {
+            int64_t m, uint64_t offset, float scale, float* __restrict__ out, int64_t tiles,
+            float* __restrict__ theta, float lr) {
   __shared__ uint4 s_ind[kStage];  // {seed lo, seed hi, fitness bits, 0}
   __shared__ float s_part[kWarps][kTile];
   __shared__ float s_red[kTile];
@@ -105,7 +109,11 @@ grad_kernel(const float* __restrict__ fitness, const int64_t* __restrict__ seeds
 
     if constexpr (!kCluster) {
       const int64_t e = tile * kTile + threadIdx.x;
-      if (e < m) out[e] = part * scale;
+      if (e < m) {
+        const float g = part * scale;
+        out[e] = g;
+        if constexpr (kUpdate) theta[e] = fmaf(lr, g, theta[e]);
+      }
     } else {
       cg::cluster_group cluster = cg::this_cluster();
       s_red[threadIdx.x] = part;
@@ -118,7 +126,11 @@ grad_kernel(const float* __restrict__ fitness, const int64_t* __restrict__ seeds
         float sum = 0.f;
         for (int q = 0; q < slices; ++q) sum += cluster.map_shared_rank(s_red, q)[t];
         const int64_t e = tile * kTile + t;
-        if (e < m) out[e] = sum * scale;
+        if (e < m) {
+          const float g = sum * scale;
+          out[e] = g;
+          if constexpr (kUpdate) theta[e] = fmaf(lr, g, theta[e]);
+        }
       }
       cluster.sync();  // no CTA may leave (or reuse s_red) while others read it
     }
@@ -133,14 +145,16 @@ int occupancy(const void* fn) {
   return blocks;
 }
 
-template <int kKind>
+template <int kKind, bool kUpdate>
 cudaError_t launch_grad_kind(const float* fitness, const int64_t* seeds, int64_t pop, int64_t m,
-                             uint64_t offset, float scale, float* out, cudaStream_t stream) {
+                             uint64_t offset, float scale, float* out, float* theta, float lr,
+                             cudaStream_t stream) {
   DeviceInfo dev;
   cudaError_t err = device_info(&dev);
   if (err != cudaSuccess) return err;
   const int64_t tiles = (m + kTile - 1) / kTile;
-  static const int occ = occupancy(reinterpret_cast<const void*>(&grad_kernel<false, kKind>));
+  static const int occ =
+      occupancy(reinterpret_cast<const void*>(&grad_kernel<false, kKind, kUpdate>));
   const int64_t resident = static_cast<int64_t>(dev.sm_count) * occ;
 
   // Split the population across a cluster while the tiles alone leave the GPU
@@ -152,8 +166,8 @@ cudaError_t launch_grad_kind(const float* fitness, const int64_t* seeds, int64_t
 
   if (slices == 1) {
     const int64_t grid = std::min<int64_t>(tiles, resident * 4);
-    grad_kernel<false, kKind><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(
-        fitness, seeds, pop, m, offset, scale, out, tiles);
+    grad_kernel<false, kKind, kUpdate><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(
+        fitness, seeds, pop, m, offset, scale, out, tiles, theta, lr);
     return cudaGetLastError();
   }
   const int64_t grid_x = std::min<int64_t>(tiles, std::max<int64_t>(1, resident * 4 / slices));
@@ -169,17 +183,24 @@ cudaError_t launch_grad_kind(const float* fitness, const int64_t* seeds, int64_t
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, grad_kernel<true, kKind>, fitness, seeds, pop, m, offset, scale,
-                            out, tiles);
+  return cudaLaunchKernelEx(&cfg, grad_kernel<true, kKind, kUpdate>, fitness, seeds, pop, m,
+                            offset, scale, out, tiles, theta, lr);
 }
 
 }  // namespace
 
 cudaError_t launch_grad(const float* fitness, const int64_t* seeds, int64_t pop, int64_t m,
-                        uint64_t offset, float scale, int kind, float* out, cudaStream_t stream) {
-  return kind == kGaussian
-             ? launch_grad_kind<kGaussian>(fitness, seeds, pop, m, offset, scale, out, stream)
-             : launch_grad_kind<kUniform>(fitness, seeds, pop, m, offset, scale, out, stream);
+                        uint64_t offset, float scale, int kind, float* out, cudaStream_t stream,
+                        float* theta, float lr) {
+  if (theta != nullptr)
+    return kind == kGaussian ? launch_grad_kind<kGaussian, true>(fitness, seeds, pop, m, offset,
+                                                                 scale, out, theta, lr, stream)
+                             : launch_grad_kind<kUniform, true>(fitness, seeds, pop, m, offset,
+                                                                scale, out, theta, lr, stream);
+  return kind == kGaussian ? launch_grad_kind<kGaussian, false>(fitness, seeds, pop, m, offset,
+                                                                scale, out, nullptr, 0.f, stream)
+                           : launch_grad_kind<kUniform, false>(fitness, seeds, pop, m, offset,
+                                                               scale, out, nullptr, 0.f, stream);
 }
 
 }  // namespace vn

@@ -26,9 +26,11 @@ cudaError_t device_info(DeviceInfo* info);
 cudaError_t launch_noise_dump(const int64_t* seeds, int64_t pop, int64_t n, uint64_t offset,
                               int kind, float* out, cudaStream_t stream);
 
-// out[e] = scale * sum_i fitness[i] * PRNG(seed_i, offset + e), e < m, with the noise of `kind`.
+// out[e] = scale * sum_i fitness[i] * PRNG(seed_i, offset + e), e < m, with the noise of `kind`;
+// with theta != NULL also theta[e] = fma(lr, out[e], theta[e]).
 cudaError_t launch_grad(const float* fitness, const int64_t* seeds, int64_t pop, int64_t m,
-                        uint64_t offset, float scale, int kind, float* out, cudaStream_t stream);
+                        uint64_t offset, float scale, int kind, float* out, cudaStream_t stream,
+                        float* theta = nullptr, float lr = 0.f);
 
 // fitness[i] = inv_n * sum_k |center[k] + sigma * PRNG(seed_i, offset + k)|.
 cudaError_t launch_reduce_metric(const float* center, const int64_t* seeds, int64_t pop,
