@@ -25,7 +25,8 @@ Timing: W untimed warm-up steps, then two timed passes between barriers and
 device synchronisations, each rewriting a 256 MiB buffer between steps (outside
 the events) so that every step starts with a cold L2:
   * the step pass: K steps, each bracketed by one pair of CUDA events on the
-    launching stream -> ms_per_step and value;
+    launching stream -> ms_per_step and value. The step's C-ABI calls are
+    captured once into a CUDA graph, replayed per step (--no-graph: direct calls);
   * the kernel pass: the same launches again (--kernel-steps, default K), every
     launch bracketed by its own pair of events -> per-kernel durations, shares
     and the dominant kernel's roofline. (An event pair around each launch adds
@@ -479,6 +480,8 @@ def main(argv=None) -> int:
     ap.add_argument("--workload", default="es_mlp",
                     choices=["tiny", "es_mlp", "mid", "grad_only", "large_tc"])
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--no-graph", action="store_true",
+                    help="step pass: direct C-ABI calls instead of a CUDA graph of them")
     ap.add_argument("--kernel-steps", type=int, default=None,
                     help="steps of the per-kernel timing pass (default: --steps)")
     ap.add_argument("--pop", type=int, default=None,
@@ -532,9 +535,26 @@ def main(argv=None) -> int:
         # gaps to the step); the kernel pass brackets every launch, for the per-kernel
         # durations, shares and the roofline of the dominant kernel.
         k_steps = args.steps
+        graph_error = None
         k_kern = args.kernel_steps if args.kernel_steps is not None else args.steps
         ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                    for _ in range(k_steps)]
+        # The step pass replays the step's C-ABI calls captured once as a CUDA graph
+        # (the same kernels and arguments; the graph only removes the host launch
+        # latency between them). If capture is refused, the calls are made directly.
+        graph = None
+        if not args.no_graph:
+            try:
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph, stream=stream):
+                    for l in launches:
+                        l()
+                graph.replay()
+                torch.cuda.synchronize(dev)
+            except Exception as exc:  # noqa: BLE001 -- reported in the JSON line
+                graph = None
+                graph_error = f"{type(exc).__name__}: {exc}"[:200]
+                torch.cuda.synchronize(dev)
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(launches))]
               for _ in range(k_kern)]
         barrier(world)
@@ -543,8 +563,11 @@ def main(argv=None) -> int:
         wall0 = time.perf_counter()
         for k in range(k_steps):
             ev_step[k][0].record(stream)
-            for l in launches:
-                l()
+            if graph is not None:
+                graph.replay()
+            else:
+                for l in launches:
+                    l()
             ev_step[k][1].record(stream)
             flush.zero_()
         torch.cuda.synchronize(dev)
@@ -638,6 +661,10 @@ def main(argv=None) -> int:
     if rank == 0:
         cfg = config_for(wl, world, args.noise)
         cfg["noise_elements_per_step"] = el_step
+        cfg["launch"] = ("step pass: one CUDA graph of the step's C-ABI calls per step"
+                         if graph is not None else
+                         "step pass: direct C-ABI calls" + (f" (graph capture failed: {graph_error})"
+                                                            if graph_error else ""))
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": total_ms_max / args.steps, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f32" if wl.number in (1, 2) else "bf16",
