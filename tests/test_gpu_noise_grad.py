@@ -203,8 +203,12 @@ def test_workload4_full_size_windows():
 
 
 @pytest.mark.parametrize("pop,n", [(1, 1), (5, 1000), (300, 4099), (16, 1 << 16), (2, 300001),
-                                   (8, 1 << 20)])
+                                   (8, 1 << 20), (1500, 1 << 16)])
 def test_reduce_metric_matches_oracle(pop, n):
+    """Sizes on every launch shape: one CTA per individual, an individual split
+    over a cluster of 2 to 8 CTAs when the population is small, and (1500
+    individuals) halves of individuals when whole ones would leave the last
+    round of CTAs mostly idle."""
     g = torch.Generator().manual_seed(n)
     c = torch.randn(n, generator=g)
     seeds = torch.arange(pop, dtype=torch.int64) * 11 - 4
