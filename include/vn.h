@@ -112,7 +112,11 @@ vn_status vn_perturbed_linear(const void* x, vn_dtype x_dt, int x_shared,
 
 /* vn_perturbed_linear with an explicit kernel choice and a fused activation
  * (applied after the bias). VN_PATH_TC returns VN_ERR_PATH when its conditions
- * do not hold and VN_ERR_DEVICE on a device that is not compute capability 10.x. */
+ * do not hold and VN_ERR_DEVICE on a device that is not compute capability 10.x.
+ * On the CUDA-core path, VN_PATH_AUTO with fp32 W and b, batch <= 8 and at least
+ * as many individuals as the device has SMs runs the kernel of vn_perturbed_mlp
+ * with one layer (its individuals share every W chunk they load); VN_PATH_FFMA
+ * always runs the single-layer kernel. Both compute in fp32. */
 vn_status vn_perturbed_linear_ex(const void* x, vn_dtype x_dt, int x_shared,
                                  const void* w, vn_dtype w_dt,
                                  const void* b, vn_dtype b_dt,

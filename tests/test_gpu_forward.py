@@ -101,6 +101,23 @@ def test_forward_one_hot_is_bit_exact(path):
         assert np.array_equal(y0[i].cpu().numpy(), gdump[i].reshape(out_f, in_f).T)
 
 
+@pytest.mark.parametrize("pop,batch,in_f,out_f,shared,bias,act", [
+    (152, 1, 64, 256, False, True, "tanh"), (300, 3, 67, 33, True, False, None),
+    (1000, 8, 40, 5, False, True, None), (157, 2, 0, 9, False, True, "tanh"),
+    (500, 1, 1030, 3, False, True, "tanh")])
+def test_auto_cuda_core_forward_of_large_populations(pop, batch, in_f, out_f, shared, bias, act):
+    """fp32 W, batch <= 8 and at least one individual per SM: the automatic path
+    runs the one-launch chain kernel with one layer (its activation included);
+    against the oracle and against the single-layer kernel (path="ffma")."""
+    x, w, b, seeds, sig, off = _case(pop, batch, in_f, out_f, shared=shared, bias=bias)
+    _run_and_check(x, w, b, seeds, sig, off, TOL_FP32, act=act)
+    args = (x.to(DEV), w.to(DEV), None if b is None else b.to(DEV), seeds.to(DEV), sig, off)
+    auto = virtual_perturbed_linear(*args, activation=act)
+    ffma = virtual_perturbed_linear(*args, activation=act, path="ffma")
+    scale = float(ffma.abs().max()) if ffma.numel() else 1.0
+    assert torch.allclose(auto, ffma, rtol=0, atol=1e-5 * max(scale, 1e-6))
+
+
 def test_workload1_forward():
     w = workloads.make(1)
     l = w.layers[0]

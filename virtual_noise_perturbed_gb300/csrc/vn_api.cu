@@ -242,6 +242,29 @@ vn_status vn_perturbed_linear_ex(const void* x, vn_dtype x_dt, int x_shared, con
   }
   if (tc_ok && batch >= kAutoTcMinBatch && device_is_cc10(dev))
     return launched(vn::launch_linear_tc(a, s));
+  // fp32 W (and bias), a policy-sized batch and enough individuals to give every
+  // SM a group of them: the one-launch chain kernel with one layer (its
+  // individuals share each loaded W chunk, which the single-layer CUDA-core
+  // kernel does not), when the layer fits its shared memory.
+  if (w_dt == VN_F32 && (b == nullptr || b_dt == VN_F32) && batch >= 1 &&
+      batch <= vn::kMlpMaxBatch && pop >= dev.sm_count && in < (int64_t{1} << 31) &&
+      out < (int64_t{1} << 31)) {
+    const int64_t dims[2] = {in, out};
+    const size_t buf = vn::mlp_buffer_floats(1, dims);
+    if (vn::mlp_bytes_per_individual(batch, buf) <= static_cast<size_t>(dev.smem_optin)) {
+      const float* wl[1] = {static_cast<const float*>(w)};
+      const float* bl[1] = {static_cast<const float*>(b)};
+      const uint64_t offs[1] = {offset};
+      vn::MlpArgs m;
+      m.x = x; m.x_dt = x_dt; m.x_shared = x_shared ? 1 : 0;
+      m.n_layers = 1;
+      m.dims = dims; m.w = wl; m.b = bl; m.offsets = offs;
+      m.seeds = seeds; m.pop = pop; m.batch = batch; m.sigma = sig; m.act = VN_ACT_NONE;
+      m.y = static_cast<float*>(y);
+      m.act_last = act;
+      return launched(vn::launch_mlp(m, s));
+    }
+  }
   return launched(vn::launch_linear_ffma(a, s));
 }
 

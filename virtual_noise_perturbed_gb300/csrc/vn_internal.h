@@ -83,8 +83,9 @@ struct MlpArgs {
   const int64_t* seeds;
   int64_t pop, batch;
   float sigma;
-  vn_act act;
+  vn_act act;        // between layers
   float* y;
+  vn_act act_last = VN_ACT_NONE;  // after the last layer (a single perturbed linear's own)
 };
 // Floats per (individual, batch row) of one activation buffer for these dims.
 size_t mlp_buffer_floats(int n_layers, const int64_t* dims);

@@ -74,7 +74,8 @@ struct MlpDev {
   int batch;
   int n_layers;
   int x_shared;
-  int act;
+  int act;       // between layers
+  int act_last;  // after the last layer
   int x_bf16;   // x is bf16 (else fp32)
   int buf_len;  // floats per (individual, batch row) in an activation buffer, a multiple of 8
   float sigma;
@@ -162,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant_
     const float* src = s_buf0 + (l & 1) * bstride;
     float* dst = s_buf0 + ((l & 1) ^ 1) * bstride;
     const bool last = l + 1 == a.n_layers;
-    const bool tanh_act = !last && a.act == VN_ACT_TANH;
+    const bool tanh_act = (last ? a.act_last : a.act) == VN_ACT_TANH;
     const int LR = 1 << lr_log2;
     const int q = lane & (LR - 1);         // lane within its row group
     const int rsub = lane >> lr_log2;      // row of this lane within the warp's group
@@ -402,6 +403,7 @@ cudaError_t launch_mlp(const MlpArgs& m, cudaStream_t stream) {
   d.n_layers = m.n_layers;
   d.x_shared = m.x_shared;
   d.act = m.act;
+  d.act_last = m.act_last;
   d.buf_len = static_cast<int>(mlp_buffer_floats(m.n_layers, m.dims));
   d.sigma = m.sigma;
   d.g_lo = kGammaLo;
