@@ -443,10 +443,23 @@ def time_oracle(wl, budget_s: float, steps: int = 1, noise: str = "uniform"):
 
 # ---------------------------------------------------------------------------
 
+def step_elements(wl) -> int:
+    """Noise elements one step of ``wl`` regenerates (forward, gradients, dump), as
+    ``build_step`` counts them: pop x weights for the forward, pop x parameters for
+    the gradients and for the dump of the ES workloads."""
+    n_params = sum(l.out_f * l.in_f + l.out_f for l in wl.layers)
+    el = wl.pop * sum(l.out_f * l.in_f for l in wl.layers) if wl.forward else 0
+    if wl.grads:
+        el += wl.pop * n_params
+    if wl.number in (1, 2):
+        el += wl.pop * n_params
+    return el
+
+
 def config_for(wl, world, noise="uniform"):
     return {"workload": wl.name, "description": wl.description, "noise": noise, "pop": wl.pop, "batch": wl.batch,
             "layers": [[l.in_f, l.out_f] for l in wl.layers], "sigma": wl.sigma,
-            "noise_elements_per_step": None, "l2": "256 MiB buffer rewritten between timed steps",
+            "noise_elements_per_step": step_elements(wl), "l2": "256 MiB buffer rewritten between timed steps",
             "parallelism": f"population shards x{world} (independent per rank)"}
 
 
