@@ -511,24 +511,29 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                 static_cast<uint64_t>(j);
             bias = fmaf(p.sigma, noise_at(seed, bidx), bj);
           }
-          for (int c0 = 0; c0 < p.nt; c0 += 16) {
+          // Y[i, n, j] for the unit's batch rows n = n0 + c0 + q: one row pointer
+          // per 16 columns, batch rows `out` elements apart.
+          using YT = typename std::conditional<kYBf16, unsigned short, float>::type;
+          YT* yrow = reinterpret_cast<YT*>(p.y) + (i * p.batch + un.n0) * p.out + j;
+          const int64_t ystride = p.out;
+          const int n_left = static_cast<int>(min(static_cast<int64_t>(p.nt), p.batch - un.n0));
+          const bool tanh_act = p.act == VN_ACT_TANH;
+          for (int c0 = 0; c0 < p.nt; c0 += 16, yrow += 16 * ystride) {
             uint32_t v[16];
             tmem_ld16(dcol + (ii * MH + h) * p.nt + c0, v);
             tmem_wait_ld();
             if (jok) {
+              const int valid = n_left - c0;  // columns of this group that are batch rows
 #pragma unroll
               for (int q = 0; q < 16; ++q) {
-                const int64_t n = un.n0 + c0 + q;
-                if (n < p.batch) {
+                if (q < valid) {
                   float val = __uint_as_float(v[q]) + bias;
-                  if (p.act == VN_ACT_TANH) val = tanhf(val);
-                  const int64_t o = (i * p.batch + n) * p.out + j;
+                  if (tanh_act) val = tanhf(val);
                   if constexpr (kYBf16) {
                     const __nv_bfloat16 hv = __float2bfloat16_rn(val);
-                    __stcs(reinterpret_cast<unsigned short*>(p.y) + o,
-                           *reinterpret_cast<const unsigned short*>(&hv));
+                    __stcs(yrow + q * ystride, *reinterpret_cast<const unsigned short*>(&hv));
                   } else {
-                    __stcs(reinterpret_cast<float*>(p.y) + o, val);
+                    __stcs(yrow + q * ystride, val);
                   }
                 }
               }
