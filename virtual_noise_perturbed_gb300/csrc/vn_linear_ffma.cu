@@ -7,10 +7,11 @@
 // The noise is "generated on-the-fly ... and added to the weight tile in
 // registers" (module description): no noise tensor exists in memory.
 //
-// This path serves small per-individual batches with bf16 W or X, populations
-// smaller than the SM count, and every call that forces it; fp32 layers of
-// larger populations with batches up to 8 go to the chain kernel (vn_mlp.cu)
-// with one layer, whose individuals share each W chunk a lane loads. Each
+// This path serves small per-individual batches with bf16 W (or bias), batches
+// of 9 to 15, populations smaller than the SM count, and every call that forces
+// it; layers with fp32 W of larger populations with batches up to 8 go to the
+// chain kernel (vn_mlp.cu) with one layer, whose individuals share each W chunk
+// a lane loads. Each
 // perturbed weight meets only a few rows of X: the work is one hash per
 // (i, j, k) plus `batch` FMAs.
 //
