@@ -63,9 +63,13 @@ def compute_offsets(param_shapes: Sequence[Sequence[int]]) -> list:
     return offsets
 
 
+_NOISE_KINDS = {"uniform": noise_np, "gaussian": gaussian_noise_np}
+
+
 def weight_noise(seed, out_f: int, in_f: int, offset: int,
-                 rows: Optional[Iterable[int]] = None) -> np.ndarray:
-    """N_i[j, k] = PRNG(seed_i, offset + j*in + k) ("Noise indexing scheme"), float64.
+                 rows: Optional[Iterable[int]] = None, noise: str = "uniform") -> np.ndarray:
+    """N_i[j, k] = PRNG(seed_i, offset + j*in + k) ("Noise indexing scheme"), float64;
+    ``noise="gaussian"``: the Gaussian variant's value at the same index (R16).
 
     ``rows`` selects which j to return (default: all, in order)."""
     s = seeds_u64([seed])[0]
@@ -73,25 +77,27 @@ def weight_noise(seed, out_f: int, in_f: int, offset: int,
     with np.errstate(over="ignore"):
         idx = (np.uint64(offset & ((1 << 64) - 1)) + rows[:, None] * np.uint64(in_f)
                + np.arange(in_f, dtype=np.uint64)[None, :])        # offset + j*in + k
-    return noise_np(s, idx)
+    return _NOISE_KINDS[noise](s, idx)
 
 
-def bias_noise(seed, out_f: int, bias_offset: int) -> np.ndarray:
-    """nb_i[j] = PRNG(seed_i, bias_offset + j), float64."""
+def bias_noise(seed, out_f: int, bias_offset: int, noise: str = "uniform") -> np.ndarray:
+    """nb_i[j] = PRNG(seed_i, bias_offset + j), float64 (or the Gaussian variant's)."""
     s = seeds_u64([seed])[0]
-    return noise_np(s, element_indices(bias_offset, out_f))
+    return _NOISE_KINDS[noise](s, element_indices(bias_offset, out_f))
 
 
 def perturbed_linear(x, weight, bias, seeds, sigma: float, offset: int,
                      individuals: Optional[Iterable[int]] = None,
-                     rows: Optional[Iterable[int]] = None) -> np.ndarray:
+                     rows: Optional[Iterable[int]] = None, noise: str = "uniform") -> np.ndarray:
     """``virtual_perturbed_linear`` in float64.
 
     x: [B, in] (shared by all individuals) or [pop, B, in]; weight: [out, in];
     bias: [out] or None; seeds: [pop]. Returns [len(individuals), B, len(rows)]
     (the full [pop, B, out] by default):
         Y[i] = X[i] @ (W + sigma*N_i)^T + (b + sigma*nb_i),
-    N_i at ``offset + j*in + k`` and nb_i at ``offset + out*in + j``.
+    N_i at ``offset + j*in + k`` and nb_i at ``offset + out*in + j``; with
+    ``noise="gaussian"`` N_i and nb_i are the Gaussian variant's values at the
+    same indices (reading R16).
     """
     w = np.asarray(weight, dtype=np.float64)
     out_f, in_f = w.shape
@@ -107,12 +113,12 @@ def perturbed_linear(x, weight, bias, seeds, sigma: float, offset: int,
     batch = x.shape[-2]
     y = np.empty((len(inds), batch, len(rows)), dtype=np.float64)
     for r, i in enumerate(inds):
-        n_i = weight_noise(s[i], out_f, in_f, offset, rows)          # [rows, in]
+        n_i = weight_noise(s[i], out_f, in_f, offset, rows, noise)   # [rows, in]
         w_pert = w[rows] + sigma * n_i                                # W + sigma*N_i
         xi = x if shared else x[i]                                    # [B, in]
         yi = xi @ w_pert.T                                            # [B, rows]
         if b is not None:
-            nb_i = bias_noise(s[i], out_f, offset + out_f * in_f)[rows]
+            nb_i = bias_noise(s[i], out_f, offset + out_f * in_f, noise)[rows]
             yi = yi + (b[rows] + sigma * nb_i)[None, :]
         y[r] = yi
     return y

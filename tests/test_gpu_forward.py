@@ -80,6 +80,19 @@ def test_forward_in_zero_is_bias_plus_bias_noise():
     assert_close(to_np(y), np.broadcast_to(want, (pop, 2, out_f)), TOL_FP32, "in=0")
 
 
+@pytest.mark.parametrize("path,pop,batch,xdt,wdt", [
+    ("ffma", 9, 3, torch.float32, torch.float32), ("auto", 200, 2, torch.float32, torch.float32),
+    ("tc", 5, 40, torch.bfloat16, torch.float32), ("tc", 3, 33, torch.bfloat16, torch.bfloat16)])
+def test_sigma_zero_is_a_plain_linear_layer(path, pop, batch, xdt, wdt):
+    """sigma = 0 removes the noise: Y[i] = X[i] W^T + b on every path, against a
+    float64 matmul of the same (bf16-rounded where the path takes bf16) inputs."""
+    x, w, b, seeds, _, off = _case(pop, batch, 72, 150, xdt=xdt, wdt=wdt, bdt=wdt)
+    y = virtual_perturbed_linear(x.to(DEV), w.to(DEV), b.to(DEV), seeds.to(DEV), 0.0, off, path=path)
+    want = (x.double() @ w.double().T + b.double()).numpy()
+    tol = TOL_BF16 if path == "tc" else TOL_FP32
+    assert_close(to_np(y), want, tol, f"sigma 0 {path}")
+
+
 @pytest.mark.parametrize("path", ["ffma"])
 def test_forward_one_hot_is_bit_exact(path):
     """X rows = e_k, W = 0, b = 0, sigma = 1: Y[i, k, :] = N_i[:, k] + nb_i exactly."""

@@ -93,6 +93,23 @@ def test_mlp_shared_x_bf16_x_no_act_partial_biases():
     _check([24, 40, 8], 10, 2, base_offset=(1 << 64) - 5000)   # indices wrap mod 2^64
 
 
+def test_mlp_sigma_zero_is_a_plain_tanh_network():
+    """sigma = 0: the chain is tanh(tanh(x W0^T + b0) W1^T + b1) W2^T + b2, against
+    float64 matmuls of the same inputs."""
+    dims, pop, batch = [40, 96, 64, 5], 10, 2
+    ws, bs = _layers(dims, 3, None)
+    x = torch.randn((pop, batch, dims[0]), generator=torch.Generator().manual_seed(4))
+    seeds = torch.arange(pop, dtype=torch.int64)
+    y = virtual_perturbed_mlp(x.to(DEV), [w.to(DEV) for w in ws], [b.to(DEV) for b in bs],
+                              seeds.to(DEV), 0.0, _offsets(dims), activation="tanh")
+    h = x.double()
+    for li, (w, b) in enumerate(zip(ws, bs)):
+        h = h @ w.double().T + b.double()
+        if li < len(ws) - 1:
+            h = torch.tanh(h)
+    assert_close(to_np(y), h.numpy(), TOL_FP32, "mlp sigma 0")
+
+
 def test_mlp_zero_width_layer_gives_bias_plus_bias_noise():
     # A hidden layer of width 0: the next layer sees in = 0, so its output is
     # b + sigma*nb (the in == 0 case of the single-layer entry point).

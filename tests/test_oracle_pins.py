@@ -462,3 +462,41 @@ def test_gaussian_gradient_one_hot_fitness_recovers_noise():
         f[m] = pop * sigma
         np.testing.assert_allclose(es.gaussian_flat_gradient(f, seeds, n, sigma, pop, off), dump[m],
                                    rtol=0, atol=1e-15)
+
+
+def test_gaussian_forward_one_hot_recovers_the_dump_and_bias_noise():
+    """Forward with the Gaussian variant, indexing pinned to the dump's: with X rows
+    e_k, W = 0, sigma = 1 and a zero bias, Y[i, r, :] = G(seed_i, offset + j*in + k_r)
+    + G(seed_i, offset + out*in + j); without a bias, the column alone."""
+    seeds = np.array([5, -2, 17])
+    pop, out_f, in_f, off = 3, 6, 5, 999
+    dump = es.gaussian_dump(seeds, out_f * in_f + out_f, off)          # [pop, out*in + out]
+    x = np.eye(in_f)[None].repeat(pop, axis=0)                          # row r = e_r
+    y = es.perturbed_linear(x, np.zeros((out_f, in_f)), None, seeds, 1.0, off, noise="gaussian")
+    for i in range(pop):
+        n_i = dump[i, :out_f * in_f].reshape(out_f, in_f)
+        np.testing.assert_array_equal(y[i], n_i.T)                      # Y[i, k, j] = N_i[j, k]
+    yb = es.perturbed_linear(x, np.zeros((out_f, in_f)), np.zeros(out_f), seeds, 1.0, off,
+                             noise="gaussian")
+    for i in range(pop):
+        np.testing.assert_allclose(yb[i] - y[i], np.broadcast_to(dump[i, out_f * in_f:], (in_f, out_f)),
+                                   rtol=0, atol=1e-15)
+
+
+def test_gaussian_forward_identity_and_linearity_in_sigma():
+    """(Y - X W^T - b) / sigma = X G_i^T + gb_i: the same for two sigmas, and zero noise
+    at sigma = 0 (a plain linear layer, against numpy's matmul)."""
+    rng = np.random.default_rng(9)
+    pop, batch, in_f, out_f, off = 3, 2, 7, 4, 31
+    x = rng.standard_normal((pop, batch, in_f))
+    w = rng.standard_normal((out_f, in_f))
+    b = rng.standard_normal(out_f)
+    seeds = np.arange(pop) + 40
+    plain = x @ w.T + b
+    np.testing.assert_allclose(es.perturbed_linear(x, w, b, seeds, 0.0, off, noise="gaussian"), plain,
+                               rtol=0, atol=1e-12)
+    e1 = (es.perturbed_linear(x, w, b, seeds, 0.25, off, noise="gaussian") - plain) / 0.25
+    e2 = (es.perturbed_linear(x, w, b, seeds, 0.75, off, noise="gaussian") - plain) / 0.75
+    np.testing.assert_allclose(e1, e2, rtol=0, atol=1e-12)
+    eu = (es.perturbed_linear(x, w, b, seeds, 0.25, off) - plain) / 0.25       # the uniform kind
+    assert np.max(np.abs(eu - e1)) > 0.1                                         # differs from it
