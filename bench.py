@@ -15,6 +15,8 @@ whole hot path over one population:
   * noise dump: the centered-uniform noise of the whole flat parameter vector
     (84,488 elements) for every individual,
 so each step regenerates the population's parameter noise three times.
+`--noise gaussian` runs the same step (or the gradient-only workload) with the
+Box-Muller variant of the noise throughout.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl vn|reference]
                        [--workload es_mlp|tiny|mid|grad_only|large_tc]
@@ -144,6 +146,7 @@ def build_step(wl, dev, stream_ptr, noise="uniform"):
     dt = {torch.float32: _lib.VN_F32, torch.bfloat16: _lib.VN_BF16}
     n_params = sum(l.out_f * l.in_f + l.out_f for l in wl.layers)
     flat = wl.grads and len(wl.layers) > 1 and contiguous_blocks(wl)
+    suffix = "_gaussian" if noise == "gaussian" else ""
 
     fused = (wl.forward and len(d.layers) > 1 and batch <= 8 and d.x.dtype in (torch.float32, torch.bfloat16)
              and all(l.weight.dtype == torch.float32 and l.bias.dtype == torch.float32 for l in d.layers))
@@ -174,13 +177,14 @@ def build_step(wl, dev, stream_ptr, noise="uniform"):
         c_b = (ctypes.c_void_p * n)(*[l.bias.data_ptr() for l in d.layers])
         c_off = (ctypes.c_uint64 * n)(*[l.offset for l in d.layers])
         act = _lib.VN_ACT_TANH if wl.activation == "tanh" else _lib.VN_ACT_NONE
+        kind = _lib.VN_NOISE_GAUSSIAN if noise == "gaussian" else _lib.VN_NOISE_UNIFORM
         args = (P(d.x.data_ptr()), dt[d.x.dtype], 0, n, c_dims, c_w, c_b, c_off, P(d.seeds.data_ptr()),
-                pop, batch, float(wl.sigma), act, P(y.data_ptr()), s)
+                pop, batch, float(wl.sigma), act, kind, P(y.data_ptr()), s)
         el = pop * sum(l.out_f * l.in_f for l in d.layers)
         hbm = (d.x.numel() * d.x.element_size() + y.numel() * 4
                + sum(l.weight.numel() * 4 + l.bias.numel() * 4 for l in d.layers))
-        launches.append(Launch("linear_mlp", lib.vn_perturbed_mlp, args, el, flops=2.0 * el * batch,
-                               hbm_bytes=hbm))
+        launches.append(Launch("linear_mlp" + suffix, lib.vn_perturbed_mlp_ex, args, el,
+                               flops=2.0 * el * batch, hbm_bytes=hbm))
         outputs.append(y)
     elif wl.forward:
         h = d.x
@@ -225,9 +229,10 @@ def build_step(wl, dev, stream_ptr, noise="uniform"):
         if theta is not None:
             # The estimate and the ES step on the parameters, theta += lr * grad (lr
             # fixed for the bench), in one launch (vn_gradient_update).
-            launches.append(Launch("grad", lib.vn_gradient_update,
+            launches.append(Launch("grad" + suffix, lib.vn_gradient_update,
                                    (P(fit.data_ptr()), P(d.seeds.data_ptr()), pop, n_params,
-                                    float(wl.sigma), wl.layers[0].offset, _lib.VN_NOISE_UNIFORM,
+                                    float(wl.sigma), wl.layers[0].offset,
+                                    _lib.VN_NOISE_GAUSSIAN if noise == "gaussian" else _lib.VN_NOISE_UNIFORM,
                                     ES_LR, P(g.data_ptr()), P(theta.data_ptr()), s),
                                    pop * n_params, hbm_bytes=n_params * 12, grad_w_elems=gw_elems))
             outputs += [g, theta]
@@ -265,8 +270,9 @@ def build_step(wl, dev, stream_ptr, noise="uniform"):
 
     if wl.number in (1, 2):
         dump = torch.empty((pop, n_params), dtype=torch.float32, device=dev)
-        launches.append(Launch("noise_dump", lib.vn_noise_dump,
+        launches.append(Launch("noise_dump" + suffix, lib.vn_noise_dump_ex,
                                (P(d.seeds.data_ptr()), pop, n_params, wl.layers[0].offset,
+                                _lib.VN_NOISE_GAUSSIAN if noise == "gaussian" else _lib.VN_NOISE_UNIFORM,
                                 P(dump.data_ptr()), s),
                                pop * n_params, hbm_bytes=dump.numel() * 4))
         outputs.append(dump)
@@ -398,7 +404,8 @@ def oracle_step(wl, individuals: int, noise: str = "uniform") -> int:
     if wl.forward:
         h = wl.x[s].float().numpy().astype(np.float64)
         for li, l in enumerate(wl.layers):
-            h = es.perturbed_linear(h, l.weight.float().numpy(), l.bias.float().numpy(), seeds, wl.sigma, l.offset)
+            h = es.perturbed_linear(h, l.weight.float().numpy(), l.bias.float().numpy(), seeds, wl.sigma,
+                                    l.offset, noise=noise)
             if wl.activation == "tanh" and li < len(wl.layers) - 1:
                 h = np.tanh(h)
             n += individuals * l.out_f * l.in_f
@@ -416,7 +423,7 @@ def oracle_step(wl, individuals: int, noise: str = "uniform") -> int:
         n += individuals * (l.out_f * l.in_f + l.out_f)
     if wl.number in (1, 2):
         n_params = sum(l.out_f * l.in_f + l.out_f for l in wl.layers)
-        es.noise_dump(seeds, n_params, wl.layers[0].offset)
+        (es.gaussian_dump if noise == "gaussian" else es.noise_dump)(seeds, n_params, wl.layers[0].offset)
         n += individuals * n_params
     return n
 
@@ -500,14 +507,14 @@ def main(argv=None) -> int:
     ap.add_argument("--pop", type=int, default=None,
                     help="run only the workload's first POP individuals (smaller profiling cases)")
     ap.add_argument("--noise", choices=["uniform", "gaussian"], default="uniform",
-                    help="gaussian: the Box-Muller noise variant (gradient-only workload)")
+                    help="gaussian: the Box-Muller noise variant (gradient-only and ES policy workloads)")
     ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.noise == "gaussian" and args.workload != "grad_only":
-        ap.error("--noise gaussian applies to the gradient-only workload")
+    if args.noise == "gaussian" and args.workload not in ("grad_only", "es_mlp"):
+        ap.error("--noise gaussian applies to the gradient-only and ES policy workloads")
 
     from virtual_noise_perturbed_gb300 import workloads
     number = {v: k for k, v in workloads.NAMES.items()}[args.workload]
@@ -621,9 +628,10 @@ def main(argv=None) -> int:
     dom = max(per_kernel, key=lambda n: per_kernel[n]["ms"])
     r = per_kernel[dom]
     secs = r["ms"] * 1e-3
-    alu_ops = ALU_OPS_GAUSSIAN if dom == "grad_gaussian" else ALU_OPS_PER_ELEMENT
+    gaussian = dom.endswith("_gaussian")
+    alu_ops = ALU_OPS_GAUSSIAN if gaussian else ALU_OPS_PER_ELEMENT
     cands = {"alu": (r["elements"] * alu_ops / secs / 1e12, pk["alu_ops"] / 1e12, "Tops/s")}
-    if dom == "grad_gaussian":
+    if gaussian:
         cands["mufu"] = (r["elements"] * MUFU_OPS_GAUSSIAN / secs / 1e12,
                          SMS_NOMINAL * MUFU_LANES_PER_SM * SM_CLOCK_MAX_HZ / 1e12, "Tops/s")
         cands["issue"] = (r["elements"] * OPS_GAUSSIAN / secs / 1e12, pk["issue_ops"] / 1e12, "Tops/s")
@@ -640,9 +648,10 @@ def main(argv=None) -> int:
                                 else "derived: 152 SMs x 128 issue lanes x 2.07 GHz" if bound == "issue"
                                 else pk["source"]),
                 "ops_per_element": {"alu": alu_ops, "mufu": MUFU_OPS_GAUSSIAN, "issue": OPS_GAUSSIAN}.get(bound),
-                # the stricter bound: every one of the 21 operations through the issue
-                # port (152 SMs x 128 lanes x 2.07 GHz)
-                "issue_frac": r["elements"] * OPS_PER_ELEMENT / secs / pk["issue_ops"],
+                # every operation of the element (21, or 32 for the Gaussian variant)
+                # through the issue port (152 SMs x 128 lanes x 2.07 GHz)
+                "issue_frac": r["elements"] * (OPS_GAUSSIAN if gaussian else OPS_PER_ELEMENT) / secs
+                              / pk["issue_ops"],
                 "launches": r["launches"], "avg_launch_us": 1e3 * r["ms"] / r["launches"]}
     kernels = {n: {"launches": v["launches"], "share": v["ms"] / sum(x["ms"] for x in per_kernel.values()),
                    "avg_us": 1e3 * v["ms"] / v["launches"],

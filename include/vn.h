@@ -237,6 +237,23 @@ vn_status vn_perturbed_mlp(const void* x, vn_dtype x_dt, int x_shared,
                            double sigma, vn_act act, float* y, void* stream);
 
 /*
+ * vn_perturbed_mlp_ex -- vn_perturbed_mlp with a choice of noise distribution:
+ * every N_{i,l} and nb_{i,l} is noise_kind(seed_i, index) at the same indices
+ * (VN_NOISE_UNIFORM: vn_perturbed_mlp exactly; VN_NOISE_GAUSSIAN: the Box-Muller
+ * variant of vn_noise, within its stated error, so that a Gaussian ES generation
+ * pairs this forward with vn_gradient_ex / vn_gradient_update of the same kind).
+ * With n_layers = 1 it is the single perturbed linear (fp32 W, batch <= 8) with
+ * either noise. Same arguments, conventions and errors as vn_perturbed_mlp; an
+ * unknown kind returns VN_ERR_VALUE.
+ */
+vn_status vn_perturbed_mlp_ex(const void* x, vn_dtype x_dt, int x_shared,
+                              int64_t n_layers, const int64_t* dims,
+                              const float* const* w, const float* const* b,
+                              const uint64_t* offsets,
+                              const int64_t* seeds, int64_t pop, int64_t batch,
+                              double sigma, vn_act act, vn_noise kind, float* y, void* stream);
+
+/*
  * vn_centered_ranks -- fitness shaping by centered ranks, the "fitness =
  * centered ranks in [-0.5, 0.5]" of the ES policy workload (the page's
  * gradient entries take the shaped fitness as given):

@@ -167,3 +167,13 @@ def test_gradient_update_validation(lib):
     assert gu(P(fake), P(fake), 4, 4, 0.1, 0, 0, 0.1, P(fake), P(fake + 66), P(0)) == 5  # theta align
     assert gu(P(fake), P(fake), 4, 4, 0.1, 0, 0, 0.1, P(fake), P(fake + 8), P(0)) == 4   # theta overlaps grad
     assert gu(P(fake), P(fake), 4, 0, 0.1, 0, 0, 0.1, P(0), P(0), P(0)) == 0             # empty
+
+
+def test_mlp_ex_refuses_unknown_noise_kind(lib):
+    fake = 0x1000
+    dims = (ctypes.c_int64 * 2)(4, 4)
+    ptrs = (ctypes.c_void_p * 1)(fake)
+    offs = (ctypes.c_uint64 * 1)(0)
+    f = lib.vn_perturbed_mlp_ex
+    assert f(P(fake), 0, 0, 1, dims, ptrs, None, offs, P(fake), 4, 1, 0.1, 1, 2, P(fake), P(0)) == 4
+    assert f(P(fake), 0, 0, 1, dims, ptrs, None, offs, P(fake), 4, 9, 0.1, 1, 1, P(fake), P(0)) == 2

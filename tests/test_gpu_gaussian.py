@@ -13,8 +13,9 @@ import torch
 
 from oracle import es
 from tests.parity import TOL_FP32, assert_close, to_np
-from virtual_noise_perturbed_gb300 import (VNError, noise_dump, virtual_bias_gradient,
-                                           virtual_flat_gradient)
+from virtual_noise_perturbed_gb300 import (VNError, compute_offsets, noise_dump,
+                                           virtual_bias_gradient, virtual_flat_gradient,
+                                           virtual_perturbed_mlp)
 from virtual_noise_perturbed_gb300.build import build
 
 pytestmark = pytest.mark.gpu
@@ -85,3 +86,55 @@ def test_unknown_kind_is_refused_by_the_library():
     assert lib.vn_gradient_ex(P(0x1000), P(0x1000), 1, 4, 0.1, 0, 2, P(0x1000), P(0)) == 4
     with pytest.raises(VNError):
         virtual_flat_gradient(torch.ones(2, device=DEV), torch.arange(2, device=DEV), 4, 0.0, 2)
+
+
+def _chain_case(dims, pop, batch, seed):
+    g = torch.Generator().manual_seed(seed)
+    ws = [torch.randn((c, a), generator=g) / a ** 0.5 for a, c in zip(dims[:-1], dims[1:])]
+    bs = [torch.randn(c, generator=g) * 0.1 for c in dims[1:]]
+    x = torch.randn((pop, batch, dims[0]), generator=g)
+    seeds = torch.arange(pop, dtype=torch.int64) * 3 + 1
+    shapes = []
+    for a, c in zip(dims[:-1], dims[1:]):
+        shapes += [(c, a), (c,)]
+    return x, ws, bs, seeds, compute_offsets(shapes)[0::2]
+
+
+@pytest.mark.parametrize("dims,pop,batch", [([64, 256, 256, 8], 5, 1), ([13, 37, 5], 11, 3),
+                                            ([32, 64, 16], 7, 8), ([40, 24], 300, 2)])
+def test_gaussian_forward_chain_matches_oracle(dims, pop, batch):
+    """The policy forward with Gaussian-variant noise (vn_perturbed_mlp_ex) against the
+    oracle's layer-by-layer chain with the same noise: within 1e-4 of the output RMS
+    (the approximations' error, at most 6e-4 on a rare element, is scaled by sigma)."""
+    x, ws, bs, seeds, offs = _chain_case(dims, pop, batch, len(dims) + pop)
+    sigma = 0.05
+    y = virtual_perturbed_mlp(x.to(DEV), [w.to(DEV) for w in ws], [b.to(DEV) for b in bs],
+                              seeds.to(DEV), sigma, offs, activation="tanh", noise="gaussian")
+    h = x.numpy().astype(np.float64)
+    for l, (w, b) in enumerate(zip(ws, bs)):
+        h = es.perturbed_linear(h, w.numpy(), b.numpy(), seeds.numpy(), sigma, offs[l], noise="gaussian")
+        if l + 1 < len(ws):
+            h = np.tanh(h)
+    assert_close(to_np(y), h, TOL_FP32, f"gaussian chain {dims}")
+
+
+def test_gaussian_forward_one_hot_reads_the_dump_bit_for_bit():
+    """X rows e_k, W = 0, sigma = 1, no bias: Y[i, k, j] is the GPU's own Gaussian dump
+    at offset + j*in + k, bit for bit (same noise, same scaling, no other arithmetic)."""
+    pop, in_f, out_f, off = 6, 8, 40, 2 ** 40 + 3
+    x = torch.eye(in_f).repeat(pop, 1, 1)
+    seeds = torch.arange(pop, dtype=torch.int64) - 2
+    y = virtual_perturbed_mlp(x.to(DEV), [torch.zeros(out_f, in_f, device=DEV)], None, seeds.to(DEV),
+                              1.0, [off], activation=None, noise="gaussian").cpu()
+    d = noise_dump(seeds.to(DEV), out_f * in_f, off, noise="gaussian").cpu().view(pop, out_f, in_f)
+    assert torch.equal(y, d.transpose(1, 2))
+
+
+def test_gaussian_forward_uniform_kind_is_the_plain_chain():
+    x, ws, bs, seeds, offs = _chain_case([24, 48, 6], 9, 2, 5)
+    args = (x.to(DEV), [w.to(DEV) for w in ws], [b.to(DEV) for b in bs], seeds.to(DEV), 0.1, offs)
+    a = virtual_perturbed_mlp(*args, noise="uniform")
+    g = virtual_perturbed_mlp(*args, noise="gaussian")
+    assert not torch.equal(a, g)
+    with pytest.raises(ValueError):
+        virtual_perturbed_mlp(*args, noise="cauchy")

@@ -43,7 +43,7 @@ def _noise_np_high_half(seed_u64, idx_u64):
     return ((h >> np.uint64(41)).astype(np.float64)) * 2.0 ** -23 - 0.5
 
 
-def _weight_noise_transposed(seed, out_f, in_f, offset, rows=None):
+def _weight_noise_transposed(seed, out_f, in_f, offset, rows=None, noise="uniform"):
     s = sm.seeds_u64([seed])[0]
     rows = range(out_f) if rows is None else list(rows)
     n = np.empty((len(rows), in_f))
@@ -54,8 +54,9 @@ def _weight_noise_transposed(seed, out_f, in_f, offset, rows=None):
     return n
 
 
-def _perturbed_linear_no_bias_noise(x, weight, bias, seeds, sigma, offset, individuals=None, rows=None):
-    y = _ORIG["perturbed_linear"](x, weight, None, seeds, sigma, offset, individuals, rows)
+def _perturbed_linear_no_bias_noise(x, weight, bias, seeds, sigma, offset, individuals=None, rows=None,
+                                    noise="uniform"):
+    y = _ORIG["perturbed_linear"](x, weight, None, seeds, sigma, offset, individuals, rows, noise)
     if bias is not None:
         b = np.asarray(bias, dtype=np.float64)
         rows_l = list(range(np.asarray(weight).shape[0])) if rows is None else list(rows)

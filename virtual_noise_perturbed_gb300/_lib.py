@@ -41,6 +41,8 @@ SIGNATURES = {
     "vn_noise_dump": (_I, [_P, _I64, _I64, _U64, _P, _P]),
     "vn_reduce_metric": (_I, [_P, _P, _I64, _I64, _D, _U64, _P, _P]),
     "vn_perturbed_mlp": (_I, [_P, _I, _I, _I64, _P, _P, _P, _P, _P, _I64, _I64, _D, _I, _P, _P]),
+    "vn_perturbed_mlp_ex": (_I, [_P, _I, _I, _I64, _P, _P, _P, _P, _P, _I64, _I64, _D, _I, _I, _P,
+                                 _P]),
     "vn_centered_ranks": (_I, [_P, _I64, _P, _P]),
     "vn_es_update": (_I, [_P, _P, _I64, _D, _P]),
     "vn_noise_dump_ex": (_I, [_P, _I64, _I64, _U64, _I, _P, _P]),

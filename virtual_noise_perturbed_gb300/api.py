@@ -110,8 +110,10 @@ def virtual_perturbed_mlp(x: torch.Tensor, weights: Sequence[torch.Tensor],
                           biases: Optional[Sequence[Optional[torch.Tensor]]], seeds: torch.Tensor,
                           sigma: float, offsets: Optional[Sequence[int]] = None, *,
                           activation: Optional[str] = "tanh",
-                          out: Optional[torch.Tensor] = None) -> torch.Tensor:
+                          out: Optional[torch.Tensor] = None, noise: str = "uniform") -> torch.Tensor:
     """A chain of perturbed linear layers in one launch (fp32 weights, batch <= 8).
+    ``noise="gaussian"`` perturbs with the Box-Muller variant of the noise
+    (``vn_perturbed_mlp_ex``), the counterpart of the Gaussian gradient.
 
     Layer l computes ``act(h @ (W_l + sigma*N_{i,l})^T + b_l + sigma*nb_{i,l})``
     with the activation on every layer but the last. ``offsets`` are the weight
@@ -158,6 +160,8 @@ def virtual_perturbed_mlp(x: torch.Tensor, weights: Sequence[torch.Tensor],
         raise ValueError(f"x has {x.shape[-1]} features, the first layer expects {dims[0]}")
     if activation not in _ACTS:
         raise ValueError("activation must be None or 'tanh'")
+    if noise not in _NOISE:
+        raise ValueError("noise must be 'uniform' or 'gaussian'")
     if out is None:
         out = torch.empty((pop, batch, dims[-1]), dtype=torch.float32, device=x.device)
     elif out.shape != (pop, batch, dims[-1]) or out.dtype != torch.float32 or not out.is_contiguous():
@@ -166,10 +170,10 @@ def virtual_perturbed_mlp(x: torch.Tensor, weights: Sequence[torch.Tensor],
     c_w = (ctypes.c_void_p * n)(*[_ptr(w).value for w in weights])
     c_b = (ctypes.c_void_p * n)(*[_ptr(b).value for b in biases])
     c_off = (ctypes.c_uint64 * n)(*[int(o) & _M64 for o in offsets])
-    st = lib.vn_perturbed_mlp(_ptr(x), _dt(x, "x"), shared, n, c_dims, c_w, c_b, c_off,
-                              _ptr(seeds), pop, batch, float(sigma), _ACTS[activation],
-                              _ptr(out), _stream(x))
-    check(st, "vn_perturbed_mlp")
+    st = lib.vn_perturbed_mlp_ex(_ptr(x), _dt(x, "x"), shared, n, c_dims, c_w, c_b, c_off,
+                                 _ptr(seeds), pop, batch, float(sigma), _ACTS[activation],
+                                 _NOISE[noise], _ptr(out), _stream(x))
+    check(st, "vn_perturbed_mlp_ex")
     return out
 
 

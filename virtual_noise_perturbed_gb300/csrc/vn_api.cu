@@ -312,6 +312,16 @@ vn_status vn_perturbed_mlp(const void* x, vn_dtype x_dt, int x_shared, int64_t n
                            const int64_t* dims, const float* const* w, const float* const* b,
                            const uint64_t* offsets, const int64_t* seeds, int64_t pop,
                            int64_t batch, double sigma, vn_act act, float* y, void* stream) {
+  return vn_perturbed_mlp_ex(x, x_dt, x_shared, n_layers, dims, w, b, offsets, seeds, pop, batch,
+                             sigma, act, VN_NOISE_UNIFORM, y, stream);
+}
+
+vn_status vn_perturbed_mlp_ex(const void* x, vn_dtype x_dt, int x_shared, int64_t n_layers,
+                              const int64_t* dims, const float* const* w, const float* const* b,
+                              const uint64_t* offsets, const int64_t* seeds, int64_t pop,
+                              int64_t batch, double sigma, vn_act act, vn_noise kind, float* y,
+                              void* stream) {
+  if (kind != VN_NOISE_UNIFORM && kind != VN_NOISE_GAUSSIAN) return VN_ERR_VALUE;
   if (!dtype_ok(x_dt)) return VN_ERR_DTYPE;
   if (act != VN_ACT_NONE && act != VN_ACT_TANH) return VN_ERR_VALUE;
   if (n_layers < 1 || n_layers > vn::kMlpMaxLayers) return VN_ERR_SHAPE;
@@ -350,6 +360,7 @@ vn_status vn_perturbed_mlp(const void* x, vn_dtype x_dt, int x_shared, int64_t n
   m.n_layers = static_cast<int>(n_layers);
   m.dims = dims; m.w = w; m.b = b != nullptr ? b : kNoBias; m.offsets = offsets;
   m.seeds = seeds; m.pop = pop; m.batch = batch; m.sigma = sig; m.act = act; m.y = y;
+  m.kind = kind;
   return launched(vn::launch_mlp(m, static_cast<cudaStream_t>(stream)));
 }
 

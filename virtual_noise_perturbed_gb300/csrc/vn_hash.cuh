@@ -165,6 +165,15 @@ __device__ __forceinline__ float noise_value(uint32_t lo, uint32_t hi) {
   }
 }
 
+// The noise value of element idx of individual seed for either kind, the
+// Gaussian one with kGaussScale applied (used where the cost does not matter).
+template <int kKind>
+__device__ __forceinline__ float noise_at_kind(uint64_t seed, uint64_t idx) {
+  const uint64_t s = seed + (idx + 1ull) * kGamma;
+  const float v = noise_value<kKind>(static_cast<uint32_t>(s), static_cast<uint32_t>(s >> 32));
+  return kKind == kGaussian ? kGaussScale * v : v;
+}
+
 // PRNG(seed, idx) in one call (used where the cost does not matter).
 __device__ __forceinline__ float noise_at(uint64_t seed, uint64_t idx) {
   const uint64_t s = seed + (idx + 1ull) * kGamma;

@@ -86,6 +86,7 @@ struct MlpArgs {
   vn_act act;        // between layers
   float* y;
   vn_act act_last = VN_ACT_NONE;  // after the last layer (a single perturbed linear's own)
+  int kind = 0;                   // noise kind: 0 the centered uniform, 1 the Gaussian variant
 };
 // Floats per (individual, batch row) of one activation buffer for these dims.
 size_t mlp_buffer_floats(int n_layers, const int64_t* dims);

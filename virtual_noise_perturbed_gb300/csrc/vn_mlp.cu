@@ -108,7 +108,7 @@ __device__ __forceinline__ void load_w8(const float* w, int in, int out, bool ve
 // population with fewer individuals hashes its last one again in the empty
 // slots (the same wall time: the other CTAs have a full group) and stores
 // nothing for them.
-template <int NB, int kP>
+template <int NB, int kP, int kKind>
 __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant__ MlpDev a) {
   extern __shared__ float4 smem4[];
   float* smem = reinterpret_cast<float*>(smem4);
@@ -121,7 +121,10 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant_
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const float sigma = a.sigma;
-  const float shift = -1.5f * sigma;
+  // Uniform kind: W' = fma(sigma, 1 + u, W - 1.5*sigma). Gaussian kind: W' =
+  // fma(sigma * kGaussScale, unit, W), unit = gaussian_unit of the finalizer's halves.
+  const float shift = kKind == kGaussian ? 0.f : -1.5f * sigma;
+  const float sigma_unit = kKind == kGaussian ? sigma * kGaussScale : sigma;
   const int64_t ib = static_cast<int64_t>(blockIdx.x) * kP;
   const int np = static_cast<int>(min(static_cast<int64_t>(kP), a.pop - ib));
 
@@ -211,7 +214,13 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant_
         float wp[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          wp[e] = fmaf(sigma, __uint_as_float(mix_to_one_plus_u(slo, shi)), wm[e]);
+          if constexpr (kKind == kGaussian) {
+            uint32_t zlo, zhi;
+            mix64_halves(slo, shi, zlo, zhi);
+            wp[e] = fmaf(sigma_unit, gaussian_unit(zlo, zhi), wm[e]);
+          } else {
+            wp[e] = fmaf(sigma_unit, __uint_as_float(mix_to_one_plus_u(slo, shi)), wm[e]);
+          }
           add64_madc(slo, shi, a.g_lo, a.g_hi, a.one);
         }
 #pragma unroll
@@ -254,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1) mlp_kernel(const __grid_constant_
               if (Lb != nullptr) {
                 const uint2 sd = s_seed[pr / NB];
                 const uint64_t seed = (static_cast<uint64_t>(sd.y) << 32) | sd.x;
-                v += fmaf(sigma, noise_at(seed, bias_base + static_cast<uint64_t>(j)), bj);
+                v += fmaf(sigma, noise_at_kind<kKind>(seed, bias_base + static_cast<uint64_t>(j)), bj);
               }
               if (tanh_act) v = tanhf(v);
               dst[pr * blen + j] = v;
@@ -310,9 +319,9 @@ LayerShape layer_shape(int64_t in, int64_t out) {
   return sh;
 }
 
-template <int NB, int kP>
+template <int NB, int kP, int kKind>
 cudaError_t launch_p(MlpDev& d, cudaStream_t stream, size_t smem) {
-  auto fn = mlp_kernel<NB, kP>;
+  auto fn = mlp_kernel<NB, kP, kKind>;
   if (smem > 48 * 1024) {
     static size_t configured = 0;
     if (configured < smem) {
@@ -330,7 +339,7 @@ cudaError_t launch_p(MlpDev& d, cudaStream_t stream, size_t smem) {
 // Group size: enough individuals per CTA that one CTA per SM covers the
 // population (ceil(pop / SMs)), at most kAcc / NB, and no more than the shared
 // memory holds.
-template <int NB>
+template <int NB, int kKind>
 cudaError_t launch_nb(MlpDev& d, cudaStream_t stream, const DeviceInfo& dev) {
   constexpr int kMaxP = kAcc / NB;
   const size_t per_ind = 2ull * NB * static_cast<size_t>(d.buf_len) * sizeof(float);
@@ -343,26 +352,26 @@ cudaError_t launch_nb(MlpDev& d, cudaStream_t stream, const DeviceInfo& dev) {
   const size_t smem = base + static_cast<size_t>(p) * per_ind;
   if constexpr (NB == 1) {
     switch (p) {
-      case 1: return launch_p<1, 1>(d, stream, smem);
-      case 2: return launch_p<1, 2>(d, stream, smem);
-      case 3: return launch_p<1, 3>(d, stream, smem);
-      case 4: return launch_p<1, 4>(d, stream, smem);
-      case 5: return launch_p<1, 5>(d, stream, smem);
-      case 6: return launch_p<1, 6>(d, stream, smem);
-      case 7: return launch_p<1, 7>(d, stream, smem);
-      default: return launch_p<1, 8>(d, stream, smem);
+      case 1: return launch_p<1, 1, kKind>(d, stream, smem);
+      case 2: return launch_p<1, 2, kKind>(d, stream, smem);
+      case 3: return launch_p<1, 3, kKind>(d, stream, smem);
+      case 4: return launch_p<1, 4, kKind>(d, stream, smem);
+      case 5: return launch_p<1, 5, kKind>(d, stream, smem);
+      case 6: return launch_p<1, 6, kKind>(d, stream, smem);
+      case 7: return launch_p<1, 7, kKind>(d, stream, smem);
+      default: return launch_p<1, 8, kKind>(d, stream, smem);
     }
   } else if constexpr (NB == 2) {
     switch (p) {
-      case 1: return launch_p<2, 1>(d, stream, smem);
-      case 2: return launch_p<2, 2>(d, stream, smem);
-      case 3: return launch_p<2, 3>(d, stream, smem);
-      default: return launch_p<2, 4>(d, stream, smem);
+      case 1: return launch_p<2, 1, kKind>(d, stream, smem);
+      case 2: return launch_p<2, 2, kKind>(d, stream, smem);
+      case 3: return launch_p<2, 3, kKind>(d, stream, smem);
+      default: return launch_p<2, 4, kKind>(d, stream, smem);
     }
   } else if constexpr (NB == 4) {
-    return p == 1 ? launch_p<4, 1>(d, stream, smem) : launch_p<4, 2>(d, stream, smem);
+    return p == 1 ? launch_p<4, 1, kKind>(d, stream, smem) : launch_p<4, 2, kKind>(d, stream, smem);
   } else {
-    return launch_p<8, 1>(d, stream, smem);
+    return launch_p<8, 1, kKind>(d, stream, smem);
   }
 }
 
@@ -410,10 +419,16 @@ cudaError_t launch_mlp(const MlpArgs& m, cudaStream_t stream) {
   d.g_hi = kGammaHi;
   d.one = 1u;
   d.x_bf16 = m.x_dt == VN_BF16 ? 1 : 0;
-  if (m.batch <= 1) return launch_nb<1>(d, stream, dev);
-  if (m.batch <= 2) return launch_nb<2>(d, stream, dev);
-  if (m.batch <= 4) return launch_nb<4>(d, stream, dev);
-  return launch_nb<8>(d, stream, dev);
+  if (m.kind == kGaussian) {
+    if (m.batch <= 1) return launch_nb<1, kGaussian>(d, stream, dev);
+    if (m.batch <= 2) return launch_nb<2, kGaussian>(d, stream, dev);
+    if (m.batch <= 4) return launch_nb<4, kGaussian>(d, stream, dev);
+    return launch_nb<8, kGaussian>(d, stream, dev);
+  }
+  if (m.batch <= 1) return launch_nb<1, kUniform>(d, stream, dev);
+  if (m.batch <= 2) return launch_nb<2, kUniform>(d, stream, dev);
+  if (m.batch <= 4) return launch_nb<4, kUniform>(d, stream, dev);
+  return launch_nb<8, kUniform>(d, stream, dev);
 }
 
 }  // namespace vn
