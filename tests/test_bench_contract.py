@@ -42,3 +42,9 @@ def test_reference_arm_prints_one_json_line():
     assert d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
+
+
+def test_bench_refuses_gaussian_on_other_workloads():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--workload", "mid",
+                          "--noise", "gaussian"], capture_output=True, text=True, timeout=120, cwd=ROOT)
+    assert out.returncode != 0 and "gaussian" in out.stderr

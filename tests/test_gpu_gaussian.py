@@ -138,3 +138,25 @@ def test_gaussian_forward_uniform_kind_is_the_plain_chain():
     assert not torch.equal(a, g)
     with pytest.raises(ValueError):
         virtual_perturbed_mlp(*args, noise="cauchy")
+
+
+def test_gaussian_policy_workload_full_size_sampled():
+    """The ES policy workload at full size (pop 1024) in its one-launch Gaussian forward,
+    against the oracle's Gaussian chain on individuals anchored at both ends plus a
+    seeded sample."""
+    from virtual_noise_perturbed_gb300 import workloads
+    w = workloads.make(2)
+    ws = [l.weight for l in w.layers]
+    bs = [l.bias for l in w.layers]
+    offs = [l.offset for l in w.layers]
+    y = virtual_perturbed_mlp(w.x.to(DEV), [t.to(DEV) for t in ws], [t.to(DEV) for t in bs],
+                              w.seeds.to(DEV), w.sigma, offs, activation="tanh", noise="gaussian")
+    rng = np.random.default_rng(2)
+    inds = sorted({0, 1, w.pop - 2, w.pop - 1} | set(rng.choice(w.pop, 8, replace=False).tolist()))
+    h = w.x.numpy()[inds].astype(np.float64)
+    seeds = w.seeds.numpy()[inds]
+    for l, (wt, bt) in enumerate(zip(ws, bs)):
+        h = es.perturbed_linear(h, wt.numpy(), bt.numpy(), seeds, w.sigma, offs[l], noise="gaussian")
+        if l + 1 < len(ws):
+            h = np.tanh(h)
+    assert_close(to_np(y)[inds], h, TOL_FP32, "gaussian policy workload")
