@@ -704,12 +704,14 @@ def run_e2e(wl, dev, stream, steps, world, el_step, noise):
     """The same step through the C ABI with inputs in pinned host memory: each step
     copies its inputs host -> device, runs, and copies every result back.
 
-    Two sets of device buffers alternate between steps, and the results are copied
-    back on a second stream, so step k's device->host copy overlaps step k+1's
-    host->device copy and kernels (the two copy directions use separate engines);
-    a set is reused only after its previous results have reached the host."""
+    Two sets of device buffers alternate between steps, and the copies run on
+    streams of their own, so that step k+1's host->device copy and step k-1's
+    device->host copy overlap step k's kernels (the two copy directions use
+    separate engines). A set's inputs are rewritten only after the kernels that
+    read them have finished, and its outputs only after they have reached the host."""
     import torch
-    copy_stream = torch.cuda.Stream(dev)
+    copy_stream = torch.cuda.Stream(dev)   # device -> host
+    load_stream = torch.cuda.Stream(dev)   # host -> device
     sets = []
     for _ in range(2):
         launches, bufs, outputs = build_step(wl, dev, stream.cuda_stream, noise)
@@ -719,15 +721,21 @@ def run_e2e(wl, dev, stream, steps, world, el_step, noise):
     host_out = [[o.detach().cpu().pin_memory() for o in st[2]] for st in sets]
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
     d2h = sum(v.numel() * v.element_size() for v in host_out[0])
+    loaded = [torch.cuda.Event() for _ in sets]
     computed = [torch.cuda.Event() for _ in sets]
     copied = [torch.cuda.Event() for _ in sets]
 
     def one(k):
         launches, bufs, outputs = sets[k % 2]
-        with torch.cuda.stream(stream):
-            stream.wait_event(copied[k % 2])          # this set's last results are on the host
+        with torch.cuda.stream(load_stream):
+            load_stream.wait_event(computed[k % 2])   # the kernels that read this set are done
+            load_stream.wait_event(copied[k % 2])     # and its results (theta is both) are out
             for name, v in host_in.items():
                 bufs[name].copy_(v, non_blocking=True)
+            loaded[k % 2].record(load_stream)
+        with torch.cuda.stream(stream):
+            stream.wait_event(loaded[k % 2])
+            stream.wait_event(copied[k % 2])          # this set's last results are on the host
             for l in launches:
                 l()
             computed[k % 2].record(stream)
@@ -737,6 +745,8 @@ def run_e2e(wl, dev, stream, steps, world, el_step, noise):
                 h.copy_(o, non_blocking=True)
             copied[k % 2].record(copy_stream)
 
+    for e in computed:
+        e.record(stream)
     for c in copied:
         c.record(copy_stream)
     one(0)
@@ -746,15 +756,19 @@ def run_e2e(wl, dev, stream, steps, world, el_step, noise):
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     a.record(stream)
+    load_stream.wait_stream(stream)
+    copy_stream.wait_stream(stream)
     for k in range(steps):
         one(k)
     stream.wait_stream(copy_stream)
+    stream.wait_stream(load_stream)
     b.record(stream)
     torch.cuda.synchronize(dev)
     ms = max_over_ranks(a.elapsed_time(b), world, dev)
     return {"value": el_step * steps * world / (ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": ms / steps,
-            "copies": "results of step k copied back on a second stream while step k+1 runs"}
+            "copies": "step k+1's inputs copied in and step k-1's results copied back on streams "
+                      "of their own while step k runs"}
 
 
 if __name__ == "__main__":
