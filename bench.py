@@ -15,8 +15,8 @@ whole hot path over one population:
   * noise dump: the centered-uniform noise of the whole flat parameter vector
     (84,488 elements) for every individual,
 so each step regenerates the population's parameter noise three times.
-`--noise gaussian` runs the same step (or the gradient-only workload) with the
-Box-Muller variant of the noise throughout.
+`--noise gaussian` runs the same step (or the step of another workload but the
+tiny one) with the Box-Muller variant of the noise throughout.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl vn|reference]
                        [--workload es_mlp|tiny|mid|grad_only|large_tc]
@@ -196,14 +196,15 @@ def build_step(wl, dev, stream_ptr, noise="uniform"):
             bufs[f"w{li}"], bufs[f"b{li}"] = l.weight, l.bias
             path = lib.vn_perturbed_linear_path(P(h.data_ptr()), dt[h.dtype], 0, P(l.weight.data_ptr()),
                                                 dt[l.weight.dtype], batch, l.in_f, l.out_f)
-            kernel = "linear_tc" if path == _lib.VN_PATH_TC else "linear_ffma"
+            kernel = ("linear_tc" if path == _lib.VN_PATH_TC else "linear_ffma") + suffix
             args = (P(h.data_ptr()), dt[h.dtype], 0, P(l.weight.data_ptr()), dt[l.weight.dtype],
                     P(l.bias.data_ptr()), dt[l.bias.dtype], P(d.seeds.data_ptr()), pop, batch,
                     l.in_f, l.out_f, float(wl.sigma), l.offset, P(y.data_ptr()), dt[ydt],
-                    _lib.VN_PATH_AUTO, act, s)
+                    _lib.VN_PATH_AUTO, act,
+                    _lib.VN_NOISE_GAUSSIAN if noise == "gaussian" else _lib.VN_NOISE_UNIFORM, s)
             el = pop * l.out_f * l.in_f
             hbm = h.numel() * h.element_size() + y.numel() * y.element_size() + l.weight.numel() * l.weight.element_size()
-            launches.append(Launch(kernel, lib.vn_perturbed_linear_ex, args, el,
+            launches.append(Launch(kernel, lib.vn_perturbed_linear_kind, args, el,
                                    flops=2.0 * el * batch, hbm_bytes=hbm))
             h = y
         outputs.append(h)
@@ -507,14 +508,14 @@ def main(argv=None) -> int:
     ap.add_argument("--pop", type=int, default=None,
                     help="run only the workload's first POP individuals (smaller profiling cases)")
     ap.add_argument("--noise", choices=["uniform", "gaussian"], default="uniform",
-                    help="gaussian: the Box-Muller noise variant (gradient-only and ES policy workloads)")
+                    help="gaussian: the Box-Muller noise variant throughout (not on the tiny workload)")
     ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.noise == "gaussian" and args.workload not in ("grad_only", "es_mlp"):
-        ap.error("--noise gaussian applies to the gradient-only and ES policy workloads")
+    if args.noise == "gaussian" and args.workload == "tiny":
+        ap.error("--noise gaussian applies to the es_mlp, mid, grad_only and large_tc workloads")
 
     from virtual_noise_perturbed_gb300 import workloads
     number = {v: k for k, v in workloads.NAMES.items()}[args.workload]

@@ -126,6 +126,24 @@ vn_status vn_perturbed_linear_ex(const void* x, vn_dtype x_dt, int x_shared,
                                  void* stream);
 
 /*
+ * vn_perturbed_linear_kind -- vn_perturbed_linear_ex with a choice of noise
+ * distribution: N_i and nb_i are noise_kind(seed_i, index) at the same indices
+ * (VN_NOISE_UNIFORM: vn_perturbed_linear_ex exactly). VN_NOISE_GAUSSIAN (the
+ * Box-Muller variant of vn_noise, within its stated error) runs on the
+ * tensor-core kernel (VN_PATH_TC, or VN_PATH_AUTO with its conditions and batch
+ * >= 16) or on the chain kernel of vn_perturbed_mlp with one layer (fp32 W and b,
+ * batch <= 8, a layer that fits its shared memory; VN_PATH_AUTO or VN_PATH_FFMA);
+ * other Gaussian calls return VN_ERR_PATH. An unknown kind returns VN_ERR_VALUE.
+ */
+vn_status vn_perturbed_linear_kind(const void* x, vn_dtype x_dt, int x_shared,
+                                   const void* w, vn_dtype w_dt,
+                                   const void* b, vn_dtype b_dt,
+                                   const int64_t* seeds, int64_t pop, int64_t batch,
+                                   int64_t in, int64_t out, double sigma, uint64_t offset,
+                                   void* y, vn_dtype y_dt, vn_path path, vn_act act,
+                                   vn_noise kind, void* stream);
+
+/*
  * vn_weight_gradient -- "virtual_weight_gradient" (API entry of the page):
  *     grad_w[j, k] = sum_i fitness[i] * N_i[j, k] / (pop * sigma)
  * fitness [pop] fp32, seeds [pop] int64, grad_w [out, in] fp32 (written, not

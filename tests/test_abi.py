@@ -177,3 +177,11 @@ def test_mlp_ex_refuses_unknown_noise_kind(lib):
     f = lib.vn_perturbed_mlp_ex
     assert f(P(fake), 0, 0, 1, dims, ptrs, None, offs, P(fake), 4, 1, 0.1, 1, 2, P(fake), P(0)) == 4
     assert f(P(fake), 0, 0, 1, dims, ptrs, None, offs, P(fake), 4, 9, 0.1, 1, 1, P(fake), P(0)) == 2
+
+
+def test_linear_kind_refuses_unknown_noise_kind(lib):
+    fake = 0x1000
+    f = lib.vn_perturbed_linear_kind
+    # (x, x_dt, shared, w, w_dt, b, b_dt, seeds, pop, batch, in, out, sigma, offset, y, y_dt, path, act, kind, s)
+    assert f(P(fake), 0, 0, P(fake), 0, P(0), 0, P(fake), 4, 1, 8, 8, 0.1, 0, P(fake), 0, 0, 0, 5, P(0)) == 4
+    assert f(P(fake), 0, 0, P(fake), 0, P(0), 0, P(fake), -1, 1, 8, 8, 0.1, 0, P(fake), 0, 0, 0, 1, P(0)) == 2

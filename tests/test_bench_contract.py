@@ -45,6 +45,6 @@ def test_reference_arm_prints_one_json_line():
 
 
 def test_bench_refuses_gaussian_on_other_workloads():
-    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--workload", "mid",
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--workload", "tiny",
                           "--noise", "gaussian"], capture_output=True, text=True, timeout=120, cwd=ROOT)
     assert out.returncode != 0 and "gaussian" in out.stderr

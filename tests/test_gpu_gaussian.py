@@ -160,3 +160,57 @@ def test_gaussian_policy_workload_full_size_sampled():
         if l + 1 < len(ws):
             h = np.tanh(h)
     assert_close(to_np(y)[inds], h, TOL_FP32, "gaussian policy workload")
+
+
+def _linear_case(pop, batch, in_f, out_f, xdt, wdt, seed):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn((pop, batch, in_f), generator=g).to(xdt)
+    w = (torch.randn((out_f, in_f), generator=g) / in_f ** 0.5).to(wdt)
+    b = (torch.randn(out_f, generator=g) * 0.1).to(wdt)
+    seeds = torch.arange(pop, dtype=torch.int64) * 5 + 2
+    return x, w, b, seeds
+
+
+@pytest.mark.parametrize("pop,batch,in_f,out_f,wdt", [(3, 40, 128, 200, torch.bfloat16),
+                                                      (2, 256, 512, 130, torch.bfloat16),
+                                                      (5, 32, 64, 128, torch.float32)])
+def test_gaussian_tensor_core_forward_matches_oracle(pop, batch, in_f, out_f, wdt):
+    """The tensor-core forward with the Gaussian kind against the oracle's float64
+    forward with the same noise, within the bf16 path's 2e-2 of the output RMS."""
+    from virtual_noise_perturbed_gb300 import virtual_perturbed_linear
+    from tests.parity import TOL_BF16
+    x, w, b, seeds = _linear_case(pop, batch, in_f, out_f, torch.bfloat16, wdt, in_f + pop)
+    y = virtual_perturbed_linear(x.to(DEV), w.to(DEV), b.to(DEV), seeds.to(DEV), 0.05, 321, path="tc",
+                                 noise="gaussian")
+    want = es.perturbed_linear(x.float().numpy(), w.float().numpy(), b.float().numpy(), seeds.numpy(),
+                               0.05, 321, noise="gaussian")
+    assert_close(to_np(y), want, TOL_BF16, "gaussian tc forward")
+
+
+def test_gaussian_tensor_core_one_hot_reads_the_bf16_dump():
+    """X rows e_k (bf16), W = 0, sigma = 1, no bias: Y[i, k, j] = bf16 of the GPU's Gaussian
+    dump at offset + j*in + k, bit for bit (pins the Gaussian unit inside the swizzled tile)."""
+    from virtual_noise_perturbed_gb300 import virtual_perturbed_linear
+    pop, in_f, out_f, off = 2, 32, 136, 77
+    x = torch.eye(in_f, dtype=torch.bfloat16).repeat(pop, 1, 1)
+    seeds = torch.tensor([9, -9], dtype=torch.int64)
+    y = virtual_perturbed_linear(x.to(DEV), torch.zeros(out_f, in_f, dtype=torch.bfloat16, device=DEV),
+                                 None, seeds.to(DEV), 1.0, off, path="tc", noise="gaussian").cpu()
+    d = noise_dump(seeds.to(DEV), out_f * in_f, off, noise="gaussian").cpu().view(pop, out_f, in_f)
+    assert torch.equal(y, d.transpose(1, 2).to(torch.bfloat16))
+
+
+def test_gaussian_single_layer_cuda_core_forward():
+    """fp32 W, batch <= 8: the Gaussian single layer runs on the chain kernel whatever
+    the population (here 6 individuals, forced "ffma" and automatic), against the
+    oracle; a Gaussian call only the single-layer kernel could run is refused."""
+    from virtual_noise_perturbed_gb300 import virtual_perturbed_linear
+    x, w, b, seeds = _linear_case(6, 3, 70, 33, torch.float32, torch.float32, 4)
+    want = es.perturbed_linear(x.numpy(), w.numpy(), b.numpy(), seeds.numpy(), 0.1, 55, noise="gaussian")
+    for path in ("auto", "ffma"):
+        y = virtual_perturbed_linear(x.to(DEV), w.to(DEV), b.to(DEV), seeds.to(DEV), 0.1, 55, path=path,
+                                     noise="gaussian")
+        assert_close(to_np(y), want, TOL_FP32, f"gaussian single layer {path}")
+    with pytest.raises(VNError):
+        virtual_perturbed_linear(x.to(DEV), w.to(DEV).to(torch.bfloat16), b.to(DEV), seeds.to(DEV), 0.1, 55,
+                                 noise="gaussian")

@@ -36,6 +36,8 @@ SIGNATURES = {
                                  _P, _I, _P]),
     "vn_perturbed_linear_ex": (_I, [_P, _I, _I, _P, _I, _P, _I, _P, _I64, _I64, _I64, _I64, _D,
                                     _U64, _P, _I, _I, _I, _P]),
+    "vn_perturbed_linear_kind": (_I, [_P, _I, _I, _P, _I, _P, _I, _P, _I64, _I64, _I64, _I64, _D,
+                                      _U64, _P, _I, _I, _I, _I, _P]),
     "vn_weight_gradient": (_I, [_P, _P, _I64, _I64, _I64, _D, _U64, _P, _P]),
     "vn_bias_gradient": (_I, [_P, _P, _I64, _I64, _D, _U64, _P, _P]),
     "vn_noise_dump": (_I, [_P, _I64, _I64, _U64, _P, _P]),

@@ -62,12 +62,13 @@ def _ptr(t: Optional[torch.Tensor]) -> ctypes.c_void_p:
 def virtual_perturbed_linear(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Tensor],
                              seeds: torch.Tensor, sigma: float, offset: int, *,
                              activation: Optional[str] = None, path: str = "auto",
-                             out: Optional[torch.Tensor] = None) -> torch.Tensor:
+                             out: Optional[torch.Tensor] = None, noise: str = "uniform") -> torch.Tensor:
     """Y[i] = X[i] @ (W + sigma*N_i)^T + (b + sigma*nb_i), shape (pop, batch, out).
 
     x is (batch, in) (shared by every individual) or (pop, batch, in). The
     result dtype is torch.result_type(x, weight). ``activation="tanh"`` applies
-    tanh to Y in the kernel's epilogue; ``path`` forces "ffma" or "tc"."""
+    tanh to Y in the kernel's epilogue; ``path`` forces "ffma" or "tc"; ``noise="gaussian"``
+    perturbs with the Box-Muller variant (``vn_perturbed_linear_kind``)."""
     lib = load()
     x = _cuda(x, "x")
     weight = _cuda(weight, "weight")
@@ -97,11 +98,13 @@ def virtual_perturbed_linear(x: torch.Tensor, weight: torch.Tensor, bias: Option
         raise ValueError("out has the wrong shape, dtype or layout")
     if activation not in _ACTS or path not in _PATHS:
         raise ValueError("activation must be None/'tanh'; path 'auto'/'ffma'/'tc'")
-    st = lib.vn_perturbed_linear_ex(
+    if noise not in _NOISE:
+        raise ValueError("noise must be 'uniform' or 'gaussian'")
+    st = lib.vn_perturbed_linear_kind(
         _ptr(x), _dt(x, "x"), shared, _ptr(weight), _dt(weight, "weight"),
         _ptr(bias), _dt(bias, "bias") if bias is not None else 0,
         _ptr(seeds), pop, batch, in_f, out_f, float(sigma), int(offset) & _M64,
-        _ptr(out), _DT[ydt], _PATHS[path], _ACTS[activation], _stream(x))
+        _ptr(out), _DT[ydt], _PATHS[path], _ACTS[activation], _NOISE[noise], _stream(x))
     check(st, "vn_perturbed_linear")
     return out
 

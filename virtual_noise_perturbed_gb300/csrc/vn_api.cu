@@ -202,6 +202,17 @@ vn_status vn_perturbed_linear_ex(const void* x, vn_dtype x_dt, int x_shared, con
                                  const int64_t* seeds, int64_t pop, int64_t batch, int64_t in,
                                  int64_t out, double sigma, uint64_t offset, void* y,
                                  vn_dtype y_dt, vn_path path, vn_act act, void* stream) {
+  return vn_perturbed_linear_kind(x, x_dt, x_shared, w, w_dt, b, b_dt, seeds, pop, batch, in, out,
+                                  sigma, offset, y, y_dt, path, act, VN_NOISE_UNIFORM, stream);
+}
+
+vn_status vn_perturbed_linear_kind(const void* x, vn_dtype x_dt, int x_shared, const void* w,
+                                   vn_dtype w_dt, const void* b, vn_dtype b_dt,
+                                   const int64_t* seeds, int64_t pop, int64_t batch, int64_t in,
+                                   int64_t out, double sigma, uint64_t offset, void* y,
+                                   vn_dtype y_dt, vn_path path, vn_act act, vn_noise kind,
+                                   void* stream) {
+  if (kind != VN_NOISE_UNIFORM && kind != VN_NOISE_GAUSSIAN) return VN_ERR_VALUE;
   if (!dtype_ok(x_dt) || !dtype_ok(w_dt) || (b != nullptr && !dtype_ok(b_dt)) || !dtype_ok(y_dt))
     return VN_ERR_DTYPE;
   const vn_dtype want_y = (x_dt == VN_BF16 && w_dt == VN_BF16) ? VN_BF16 : VN_F32;
@@ -227,10 +238,11 @@ vn_status vn_perturbed_linear_ex(const void* x, vn_dtype x_dt, int x_shared, con
   a.x = x; a.x_dt = x_dt; a.x_shared = x_shared ? 1 : 0;
   a.w = w; a.w_dt = w_dt; a.b = b; a.b_dt = b_dt;
   a.seeds = seeds; a.pop = pop; a.batch = batch; a.in = in; a.out = out;
-  a.sigma = sig; a.offset = offset; a.y = y; a.y_dt = y_dt; a.act = act;
+  a.sigma = sig; a.offset = offset; a.y = y; a.y_dt = y_dt; a.act = act; a.kind = kind;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool gaussian = kind == VN_NOISE_GAUSSIAN;
 
-  if (path == VN_PATH_FFMA) return launched(vn::launch_linear_ffma(a, s));
+  if (path == VN_PATH_FFMA && !gaussian) return launched(vn::launch_linear_ffma(a, s));
   vn::DeviceInfo dev;
   cudaError_t err = vn::device_info(&dev);
   if (err != cudaSuccess) return cuda_failure(err);
@@ -240,14 +252,15 @@ vn_status vn_perturbed_linear_ex(const void* x, vn_dtype x_dt, int x_shared, con
     if (!tc_ok) return VN_ERR_PATH;
     return launched(vn::launch_linear_tc(a, s));
   }
-  if (tc_ok && batch >= kAutoTcMinBatch && device_is_cc10(dev))
+  if (path == VN_PATH_AUTO && tc_ok && batch >= kAutoTcMinBatch && device_is_cc10(dev))
     return launched(vn::launch_linear_tc(a, s));
   // fp32 W (and bias), a policy-sized batch and enough individuals to give every
   // SM a group of them: the one-launch chain kernel with one layer (its
   // individuals share each loaded W chunk, which the single-layer CUDA-core
-  // kernel does not), when the layer fits its shared memory.
+  // kernel does not), when the layer fits its shared memory. It is also the
+  // CUDA-core kernel of the Gaussian kind, for any population.
   if (w_dt == VN_F32 && (b == nullptr || b_dt == VN_F32) && batch >= 1 &&
-      batch <= vn::kMlpMaxBatch && pop >= dev.sm_count && in < (int64_t{1} << 31) &&
+      batch <= vn::kMlpMaxBatch && (pop >= dev.sm_count || gaussian) && in < (int64_t{1} << 31) &&
       out < (int64_t{1} << 31)) {
     const int64_t dims[2] = {in, out};
     const size_t buf = vn::mlp_buffer_floats(1, dims);
@@ -262,9 +275,12 @@ vn_status vn_perturbed_linear_ex(const void* x, vn_dtype x_dt, int x_shared, con
       m.seeds = seeds; m.pop = pop; m.batch = batch; m.sigma = sig; m.act = VN_ACT_NONE;
       m.y = static_cast<float*>(y);
       m.act_last = act;
+      m.kind = kind;
       return launched(vn::launch_mlp(m, s));
     }
   }
+  // The single-layer CUDA-core kernel has the uniform kind only.
+  if (gaussian) return VN_ERR_PATH;
   return launched(vn::launch_linear_ffma(a, s));
 }
 

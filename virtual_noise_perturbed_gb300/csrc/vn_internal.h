@@ -52,6 +52,7 @@ struct LinearArgs {
   void* y;
   vn_dtype y_dt;
   vn_act act;
+  int kind = 0;  // noise kind: 0 the centered uniform, 1 the Gaussian variant
 };
 
 // CUDA-core forward: any dtypes, any batch.

@@ -333,7 +333,7 @@ __device__ __forceinline__ Unit decode(const TcParams& p, int64_t u, int mh) {
 // ---------------------------------------------------------------- the kernel
 // kHook: the test-hook instance (one hashing thread may withhold an arrive);
 // the ordinary instances carry no trace of it.
-template <int MH, bool kWBf16, bool kYBf16, bool kHook>
+template <int MH, bool kWBf16, bool kYBf16, bool kHook, int kKind>
 __global__ void __launch_bounds__(kThreads, 1)
 linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
                  const TcParams p) {
@@ -509,7 +509,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
             const uint64_t bidx =
                 p.offset + static_cast<uint64_t>(p.out) * static_cast<uint64_t>(p.in) +
                 static_cast<uint64_t>(j);
-            bias = fmaf(p.sigma, noise_at(seed, bidx), bj);
+            bias = fmaf(p.sigma, noise_at_kind<kKind>(seed, bidx), bj);
           }
           // Y[i, n, j] for the unit's batch rows n = n0 + c0 + q: one row pointer
           // per 16 columns, batch rows `out` elements apart.
@@ -562,7 +562,10 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
     auto soff = [&](int q) { return soff0 + q * (kRowsPerPass * 128u); };
     auto rowq = [&](int q) { return row0 + q * kRowsPerPass; };
     const float sigma = p.sigma;
-    const float shift = -1.5f * sigma;
+    // Uniform kind: W + sigma*n = fma(sigma, 1 + u, W - 1.5*sigma). Gaussian kind:
+    // W + sigma*G = fma(sigma * kGaussScale, unit, W), unit from the finalizer's halves.
+    const float shift = kKind == kGaussian ? 0.f : -1.5f * sigma;
+    const float sigma_unit = kKind == kGaussian ? sigma * kGaussScale : sigma;
     const uint32_t g_lo = p.g_lo, g_hi = p.g_hi, one = p.one;
 
     // This thread's chunk q inside a staged W tile (rows of 64 k, 256 bytes in
@@ -650,14 +653,24 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
             float pv[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
+              // The element's noise term: the uniform kind as 1 + u (its -1.5 rides on
+              // the shift), the Gaussian kind as the unit Box-Muller value.
+              float unit;
+              if constexpr (kKind == kGaussian) {
+                uint32_t zlo, zhi;
+                mix64_halves(slo, shi, zlo, zhi);
+                unit = gaussian_unit(zlo, zhi);
+              } else {
+                unit = __uint_as_float(mix_to_one_plus_u(slo, shi));
+              }
               if constexpr (kWBf16) {
                 // sigma*n = fma(sigma, 1 + u, -1.5*sigma), then + W straight from its bf16 bits.
-                const float tt = fmaf(sigma, __uint_as_float(mix_to_one_plus_u(slo, shi)), shift);
+                const float tt = fmaf(sigma_unit, unit, shift);
                 const uint32_t wv = (e & 4) ? ((e & 2) ? wraw[q].a.w : wraw[q].a.z)
                                             : ((e & 2) ? wraw[q].a.y : wraw[q].a.x);
                 pv[e] = (e & 1) ? add_bf16_f32<true>(wv, tt) : add_bf16_f32<false>(wv, tt);
               } else {
-                pv[e] = fmaf(sigma, __uint_as_float(mix_to_one_plus_u(slo, shi)), wm[q][e]);
+                pv[e] = fmaf(sigma_unit, unit, wm[q][e]);
               }
               add64_madc(slo, shi, g_lo, g_hi, one);
             }
@@ -704,10 +717,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-template <int MH, bool kW, bool kY, bool kHook>
+template <int MH, bool kW, bool kY, bool kHook, int kKind = kUniform>
 cudaError_t launch_typed(const CUtensorMap& xmap, const CUtensorMap& wmap, const TcParams& p,
                          int grid, size_t smem, cudaStream_t stream) {
-  auto fn = linear_tc_kernel<MH, kW, kY, kHook>;
+  auto fn = linear_tc_kernel<MH, kW, kY, kHook, kKind>;
   static size_t configured = 0;
   if (configured < smem) {
     cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -826,6 +839,13 @@ cudaError_t launch_linear_tc_hook(const LinearArgs& a, cudaStream_t stream, long
     // The test hook has one instance: bf16 W and Y.
     if (!(wbf && ybf)) return cudaErrorInvalidValue;
     return launch_typed<1, true, true, true>(xmap, wmap, p, grid, smem, stream);
+  }
+  if (a.kind == kGaussian) {
+    if (wbf) {
+      return ybf ? launch_typed<1, true, true, false, kGaussian>(xmap, wmap, p, grid, smem, stream)
+                 : launch_typed<1, true, false, false, kGaussian>(xmap, wmap, p, grid, smem, stream);
+    }
+    return launch_typed<1, false, false, false, kGaussian>(xmap, wmap, p, grid, smem, stream);
   }
   if (wbf) {
     return ybf ? launch_typed<1, true, true, false>(xmap, wmap, p, grid, smem, stream)
