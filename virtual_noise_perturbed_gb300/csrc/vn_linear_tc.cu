@@ -333,7 +333,7 @@ __device__ __forceinline__ Unit decode(const TcParams& p, int64_t u, int mh) {
 // ---------------------------------------------------------------- the kernel
 // kHook: the test-hook instance (one hashing thread may withhold an arrive);
 // the ordinary instances carry no trace of it.
-template <int MH, bool kWBf16, bool kYBf16, bool kHook, int kKind>
+template <int MH, bool kWBf16, bool kYBf16, bool kHook, int kKind, bool kG1>
 __global__ void __launch_bounds__(kThreads, 1)
 linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
                  const TcParams p) {
@@ -408,7 +408,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
           tma_load_2d(wslot0 + wr.s * p.w_bytes, &wmap, full_w(wr.s), kc * kKC, un.m0);
           ++wit;
           wr.next(2);
-          for (int ii = 0; ii < un.gcount; ++ii, ++it, rg.next(S)) {
+          for (int ii = 0; ii < (kG1 ? 1 : un.gcount); ++ii, ++it, rg.next(S)) {
             const int s = rg.s;
             if (!(ok = mbar_wait(empty(s), rg.ph ^ 1u, s_abort, kProducerSleepNs))) break;
             mbar_expect_tx(full_x(s), x_bytes);
@@ -449,7 +449,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
         tc_fence_after();
         const uint32_t dcol = tmem + b * cols_per_buf;
         for (int kc = 0; ok && kc < p.k_chunks; ++kc) {
-          for (int ii = 0; ii < un.gcount; ++ii, rg.next(S)) {
+          for (int ii = 0; ii < (kG1 ? 1 : un.gcount); ++ii, rg.next(S)) {
             const int s = rg.s;
             if (!(ok = mbar_wait(full_x(s), rg.ph, s_abort, kMmaSleepNs))) break;
             if (!(ok = mbar_wait(full_a(s), rg.ph, s_abort, kMmaSleepNs))) break;
@@ -494,7 +494,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
       if (s_abort->abort) break;
       tc_fence_after();
       const uint32_t dcol = tmem + b * cols_per_buf + (static_cast<uint32_t>(quarter * 32) << 16);
-      for (int ii = 0; ii < un.gcount; ++ii) {
+      for (int ii = 0; ii < (kG1 ? 1 : un.gcount); ++ii) {
         const int64_t i = un.i0 + ii;
         const uint64_t seed = static_cast<uint64_t>(__ldg(p.seeds + i));
 #pragma unroll
@@ -642,7 +642,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
         fence_proxy_async_smem();
         mbar_arrive(ew0 + 8u * ws);
         if (++ws == 2) { ws = 0; wph ^= 1u; }
-        for (int ii = 0; ii < un.gcount; ++ii) {
+        for (int ii = 0; ii < (kG1 ? 1 : un.gcount); ++ii) {
           const uint64_t seed = static_cast<uint64_t>(__ldg(seedp + ii));
           if (!mbar_wait(em0 + 8u * s, ph ^ 1u, s_abort)) goto hashing_done;
           const uint32_t a0 = a_this + s * stage_bytes;
@@ -717,10 +717,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-template <int MH, bool kW, bool kY, bool kHook, int kKind = kUniform>
-cudaError_t launch_typed(const CUtensorMap& xmap, const CUtensorMap& wmap, const TcParams& p,
-                         int grid, size_t smem, cudaStream_t stream) {
-  auto fn = linear_tc_kernel<MH, kW, kY, kHook, kKind>;
+template <int MH, bool kW, bool kY, bool kHook, int kKind, bool kG1>
+cudaError_t launch_kernel(const CUtensorMap& xmap, const CUtensorMap& wmap, const TcParams& p,
+                          int grid, size_t smem, cudaStream_t stream) {
+  auto fn = linear_tc_kernel<MH, kW, kY, kHook, kKind, kG1>;
   static size_t configured = 0;
   if (configured < smem) {
     cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -730,6 +730,16 @@ cudaError_t launch_typed(const CUtensorMap& xmap, const CUtensorMap& wmap, const
   }
   fn<<<grid, kThreads, smem, stream>>>(xmap, wmap, p);
   return cudaGetLastError();
+}
+
+// One individual per unit (the whole TMEM buffer for one batch tile): the
+// individual loops of every role have a single, compile-time iteration.
+template <int MH, bool kW, bool kY, bool kHook, int kKind = kUniform>
+cudaError_t launch_typed(const CUtensorMap& xmap, const CUtensorMap& wmap, const TcParams& p,
+                         int grid, size_t smem, cudaStream_t stream) {
+  if (p.g == 1 && !kHook)
+    return launch_kernel<MH, kW, kY, kHook, kKind, true>(xmap, wmap, p, grid, smem, stream);
+  return launch_kernel<MH, kW, kY, kHook, kKind, false>(xmap, wmap, p, grid, smem, stream);
 }
 
 }  // namespace
