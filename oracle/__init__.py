@@ -15,9 +15,12 @@ Modules
               numpy ``uint64`` arrays (bulk work; wraps mod 2**64 and shifts
               logically, as the page requires).
 ``es``        the method itself: the noise dump, ``compute_offsets``, the
-              perturbed linear forward, the weight / bias gradient estimates
-              and the mean-abs reduction metric, all in float64 with the
-              noise materialised explicitly.
+              perturbed linear forward, the weight / bias gradient estimates,
+              the mean-abs reduction metric, the centered ranks and the
+              parameter update, all in float64 with the noise materialised
+              explicitly; the dump, the gradient and the forward also with the
+              Gaussian variant of the noise (Box-Muller on the finalizer's
+              two halves, ``splitmix.gaussian_*``).
 
 Readings of the page (where it is silent or ambiguous) are stated in the
 docstring of the function that takes them. Parity status: every function here
