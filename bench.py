@@ -766,10 +766,49 @@ def run_e2e(wl, dev, stream, steps, world, el_step, noise):
     b.record(stream)
     torch.cuda.synchronize(dev)
     ms = max_over_ranks(a.elapsed_time(b), world, dev)
+    link = host_link(sets[0], host_in, host_out[0], load_stream, copy_stream, dev)
+    link["frac"] = link["bound_ms_per_step"] / (ms / steps)
     return {"value": el_step * steps * world / (ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": ms / steps,
             "copies": "step k+1's inputs copied in and step k-1's results copied back on streams "
-                      "of their own while step k runs"}
+                      "of their own while step k runs", "host_link": link}
+
+
+def host_link(step_set, host_in, host_out, load_stream, copy_stream, dev, reps=5):
+    """The host link's own floor for one e2e step: the step's input copies alone and its
+    result copies alone, each timed with events on its own stream (the two directions
+    run on separate copy engines, so a pipelined step can take no less than the slower)."""
+    import torch
+    _, bufs, outputs = step_set
+
+    def timed(stream, body):
+        body()
+        torch.cuda.synchronize(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            body()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / reps
+
+    def load():
+        with torch.cuda.stream(load_stream):
+            for name, v in host_in.items():
+                bufs[name].copy_(v, non_blocking=True)
+
+    def back():
+        with torch.cuda.stream(copy_stream):
+            for o, h in zip(outputs, host_out):
+                h.copy_(o, non_blocking=True)
+
+    h2d_ms = timed(load_stream, load)
+    d2h_ms = timed(copy_stream, back)
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out)
+    return {"h2d_ms": h2d_ms, "d2h_ms": d2h_ms, "h2d_gbs": h2d / (h2d_ms * 1e-3) / 1e9,
+            "d2h_gbs": d2h / (d2h_ms * 1e-3) / 1e9, "bound_ms_per_step": max(h2d_ms, d2h_ms)}
 
 
 if __name__ == "__main__":
