@@ -33,6 +33,9 @@
  *     valid and the kernel was launched, not that it has finished.
  *   - Arguments are validated on the host before anything is launched. A call
  *     that fails validation returns its status and launches nothing.
+ *   - An output array may not share memory with an input array of the same
+ *     call, nor with another output: a call whose arrays overlap that way
+ *     returns VN_ERR_VALUE and launches nothing.
  *   - A size of 0 in an output dimension is valid and launches nothing (the
  *     pointers of empty arrays may then be NULL).
  *   - Kernels that wait on on-chip barriers bound every wait. A wait that runs
@@ -54,7 +57,8 @@ typedef enum vn_status {
   VN_ERR_NULL = 1,     /* a required pointer is NULL                                */
   VN_ERR_SHAPE = 2,    /* a size is negative, or pop < 1 where an estimate needs it   */
   VN_ERR_DTYPE = 3,    /* unsupported dtype or dtype combination                    */
-  VN_ERR_VALUE = 4,    /* sigma not finite, or sigma == 0 for a gradient            */
+  VN_ERR_VALUE = 4,    /* sigma not finite, sigma == 0 for a gradient, an unknown    */
+                       /* enum, or an output overlapping an input of the call       */
   VN_ERR_ALIGN = 5,    /* a pointer is not aligned to its element size              */
   VN_ERR_OVERFLOW = 6, /* a size product does not fit in int64                      */
   VN_ERR_TIMEOUT = 7,  /* a device-side bounded wait ran out (vn_device_status)     */
@@ -290,7 +294,8 @@ vn_status vn_centered_ranks(const float* fitness, int64_t pop, float* out, void*
  *     theta[k] = fma(lr, grad[k], theta[k]),  k < n   (fp32, in place)
  * With grad from vn_weight_gradient / vn_bias_gradient over the blocks laid out
  * by compute_offsets, lr > 0 ascends the fitness. lr finite; theta and grad
- * fp32, 4-byte aligned (16-byte alignment of both takes a vector path).
+ * fp32, 4-byte aligned (16-byte alignment of both takes a vector path), and
+ * must not overlap.
  */
 vn_status vn_es_update(float* theta, const float* grad, int64_t n, double lr, void* stream);
 

@@ -185,3 +185,58 @@ def test_linear_kind_refuses_unknown_noise_kind(lib):
     # (x, x_dt, shared, w, w_dt, b, b_dt, seeds, pop, batch, in, out, sigma, offset, y, y_dt, path, act, kind, s)
     assert f(P(fake), 0, 0, P(fake), 0, P(0), 0, P(fake), 4, 1, 8, 8, 0.1, 0, P(fake), 0, 0, 0, 5, P(0)) == 4
     assert f(P(fake), 0, 0, P(fake), 0, P(0), 0, P(fake), -1, 1, 8, 8, 0.1, 0, P(fake), 0, 0, 0, 1, P(0)) == 2
+
+
+def test_outputs_overlapping_inputs_are_refused(lib):
+    """Every call refuses an output that shares bytes with one of its inputs (or
+    with its other output) before anything is launched: VN_ERR_VALUE."""
+    fake = 0x10000
+    f_, s_, g_ = fake, fake + 0x100, fake + 0x200            # fitness, seeds, a free area
+    # dump: 4 x 4 floats over the 4 seeds
+    assert lib.vn_noise_dump(P(s_), 4, 4, 0, P(s_ + 16), P(0)) == 4
+    # gradients: grad over fitness, grad over seeds
+    assert lib.vn_weight_gradient(P(f_), P(s_), 4, 2, 2, 0.1, 0, P(f_ + 12), P(0)) == 4
+    assert lib.vn_bias_gradient(P(f_), P(s_), 4, 4, 0.1, 0, P(s_ + 28), P(0)) == 4
+    assert lib.vn_gradient_ex(P(f_), P(s_), 4, 4, 0.1, 0, 1, P(s_ - 12), P(0)) == 4
+    # gradient + update: theta over fitness, over seeds, over grad
+    gu = lib.vn_gradient_update
+    assert gu(P(f_), P(s_), 4, 4, 0.1, 0, 0, 0.1, P(g_), P(f_ + 4), P(0)) == 4
+    assert gu(P(f_), P(s_), 4, 4, 0.1, 0, 0, 0.1, P(g_), P(s_ + 16), P(0)) == 4
+    assert gu(P(f_), P(s_), 4, 4, 0.1, 0, 0, 0.1, P(g_), P(g_ + 12), P(0)) == 4
+    # metric: fitness over center (8 floats), over seeds
+    assert lib.vn_reduce_metric(P(g_), P(s_), 4, 8, 0.1, 0, P(g_ + 28), P(0)) == 4
+    assert lib.vn_reduce_metric(P(g_), P(s_), 4, 8, 0.1, 0, P(s_ + 24), P(0)) == 4
+    # forward: y (2 x 2 x 4 floats) over x, w, b and seeds
+    x, w, b, s = fake + 0x1000, fake + 0x2000, fake + 0x3000, fake + 0x4000
+
+    def lin(y, bias=b):
+        return lib.vn_perturbed_linear(P(x), 0, 0, P(w), 0, P(bias), 0, P(s), 2, 2, 4, 4, 0.1, 0,
+                                       P(y), 0, P(0))
+    assert lin(x + 60) == 4          # the last float of x
+    assert lin(w - 60) == 4          # y's last float is w's first
+    assert lin(b + 8) == 4
+    assert lin(s + 12) == 4
+    # chain forward: y over a layer's weights, its bias, x
+    dims = (ctypes.c_int64 * 3)(4, 4, 4)
+    ws = (ctypes.c_void_p * 2)(w, w + 0x100)
+    bs = (ctypes.c_void_p * 2)(b, b + 0x100)
+    offs = (ctypes.c_uint64 * 2)(0, 20)
+
+    def mlp(y, bias=None):
+        return lib.vn_perturbed_mlp(P(x), 0, 0, 2, dims, ws, bias, offs, P(s), 2, 1, 0.1, 1, P(y), P(0))
+    assert mlp(w + 0x100 + 60) == 4  # the second layer's last weight
+    assert mlp(b + 0x100, bs) == 4   # the second layer's bias
+    assert mlp(x + 4) == 4
+    # parameter step and ranks
+    assert lib.vn_es_update(P(g_), P(g_ + 8), 4, 0.1, P(0)) == 4
+    assert lib.vn_centered_ranks(P(g_), 4, P(g_ + 12), P(0)) == 4
+
+
+def test_binding_requires_one_device_per_call():
+    """The binding runs each call with its tensors' device made current, and refuses
+    a call whose tensors sit on different devices."""
+    import torch
+    from virtual_noise_perturbed_gb300 import api
+    with pytest.raises(ValueError, match="share a device"):
+        api._device(torch.empty(1), torch.empty(1, device="meta"))
+    assert api._device(torch.empty(1), None, torch.empty(2)) == torch.device("cpu")

@@ -134,3 +134,32 @@ def test_gradient_update_refusals():
         gradient_update(torch.ones(4, device=DEV), torch.arange(4, device=DEV), theta.double(), 0.1, 4, 0.1)
     with pytest.raises(VNError):
         gradient_update(torch.ones(4, device=DEV), torch.arange(4, device=DEV), theta, 0.1, 4, float("inf"))
+
+
+def test_adjacent_slices_of_one_buffer():
+    """Fitness and theta carved from one allocation back to back (no shared byte), and
+    theta and grad likewise: validation accepts them, and the results are the bits that
+    separate buffers give. Slices that share bytes are refused before any launch."""
+    pop, n, sigma, lr, off = 300, 4099, 0.02, 0.05, 777
+    g = torch.Generator().manual_seed(11)
+    fit = torch.randn(pop, generator=g)
+    theta0 = torch.randn(n, generator=g)
+    seeds = torch.arange(pop, dtype=torch.int64).to(DEV)
+
+    buf = torch.cat([fit, theta0]).to(DEV)               # [fitness | theta]
+    grad_a = gradient_update(buf[:pop], seeds, buf[pop:], sigma, pop, lr, off)
+    theta_b = theta0.to(DEV)
+    grad_b = gradient_update(fit.to(DEV), seeds, theta_b, sigma, pop, lr, off)
+    assert torch.equal(grad_a, grad_b) and torch.equal(buf[pop:], theta_b)
+    assert torch.equal(buf[:pop].cpu(), fit)             # the input is untouched
+
+    buf2 = torch.cat([theta0, grad_b.cpu()]).to(DEV)     # [theta | grad]
+    es_update(buf2[:n], buf2[n:], lr)
+    theta_c = theta0.to(DEV)
+    es_update(theta_c, grad_b, lr)
+    assert torch.equal(buf2[:n], theta_c)
+
+    with pytest.raises(VNError, match="VALUE"):
+        es_update(buf2[:n], buf2[n - 4:2 * n - 4], lr)   # grad's first 4 floats are theta's last
+    with pytest.raises(VNError, match="VALUE"):
+        gradient_update(buf[:pop], seeds, buf[pop - 1:pop - 1 + n], sigma, pop, lr, off)

@@ -59,6 +59,15 @@ def _ptr(t: Optional[torch.Tensor]) -> ctypes.c_void_p:
     return ctypes.c_void_p(0 if t is None or t.numel() == 0 else t.data_ptr())
 
 
+def _device(*tensors: Optional[torch.Tensor]) -> torch.device:
+    """The one device every tensor of a call is on. The library launches on the
+    current CUDA device, so each call runs with this device made current."""
+    devices = {t.device for t in tensors if t is not None}
+    if len(devices) != 1:
+        raise ValueError(f"the tensors of one call must share a device, got {sorted(map(str, devices))}")
+    return devices.pop()
+
+
 def virtual_perturbed_linear(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Tensor],
                              seeds: torch.Tensor, sigma: float, offset: int, *,
                              activation: Optional[str] = None, path: str = "auto",
@@ -100,11 +109,12 @@ def virtual_perturbed_linear(x: torch.Tensor, weight: torch.Tensor, bias: Option
         raise ValueError("activation must be None/'tanh'; path 'auto'/'ffma'/'tc'")
     if noise not in _NOISE:
         raise ValueError("noise must be 'uniform' or 'gaussian'")
-    st = lib.vn_perturbed_linear_kind(
-        _ptr(x), _dt(x, "x"), shared, _ptr(weight), _dt(weight, "weight"),
-        _ptr(bias), _dt(bias, "bias") if bias is not None else 0,
-        _ptr(seeds), pop, batch, in_f, out_f, float(sigma), int(offset) & _M64,
-        _ptr(out), _DT[ydt], _PATHS[path], _ACTS[activation], _NOISE[noise], _stream(x))
+    with torch.cuda.device(_device(x, weight, bias, seeds, out)):
+        st = lib.vn_perturbed_linear_kind(
+            _ptr(x), _dt(x, "x"), shared, _ptr(weight), _dt(weight, "weight"),
+            _ptr(bias), _dt(bias, "bias") if bias is not None else 0,
+            _ptr(seeds), pop, batch, in_f, out_f, float(sigma), int(offset) & _M64,
+            _ptr(out), _DT[ydt], _PATHS[path], _ACTS[activation], _NOISE[noise], _stream(x))
     check(st, "vn_perturbed_linear")
     return out
 
@@ -173,9 +183,10 @@ def virtual_perturbed_mlp(x: torch.Tensor, weights: Sequence[torch.Tensor],
     c_w = (ctypes.c_void_p * n)(*[_ptr(w).value for w in weights])
     c_b = (ctypes.c_void_p * n)(*[_ptr(b).value for b in biases])
     c_off = (ctypes.c_uint64 * n)(*[int(o) & _M64 for o in offsets])
-    st = lib.vn_perturbed_mlp_ex(_ptr(x), _dt(x, "x"), shared, n, c_dims, c_w, c_b, c_off,
-                                 _ptr(seeds), pop, batch, float(sigma), _ACTS[activation],
-                                 _NOISE[noise], _ptr(out), _stream(x))
+    with torch.cuda.device(_device(x, seeds, out, *weights, *biases)):
+        st = lib.vn_perturbed_mlp_ex(_ptr(x), _dt(x, "x"), shared, n, c_dims, c_w, c_b, c_off,
+                                     _ptr(seeds), pop, batch, float(sigma), _ACTS[activation],
+                                     _NOISE[noise], _ptr(out), _stream(x))
     check(st, "vn_perturbed_mlp_ex")
     return out
 
@@ -195,9 +206,11 @@ def virtual_weight_gradient(fitness: torch.Tensor, seeds: torch.Tensor, weight_s
     seeds = _seeds(seeds)
     fitness = _fitness(fitness, pop_size, seeds)
     out_f, in_f = (int(d) for d in weight_shape)
-    g = torch.empty((out_f, in_f), dtype=torch.float32, device=fitness.device)
-    st = lib.vn_weight_gradient(_ptr(fitness), _ptr(seeds), pop_size, out_f, in_f, float(sigma),
-                                int(offset) & _M64, _ptr(g), _stream(g))
+    dev = _device(fitness, seeds)
+    g = torch.empty((out_f, in_f), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        st = lib.vn_weight_gradient(_ptr(fitness), _ptr(seeds), pop_size, out_f, in_f, float(sigma),
+                                    int(offset) & _M64, _ptr(g), _stream(g))
     check(st, "vn_weight_gradient")
     return g
 
@@ -209,9 +222,11 @@ def virtual_bias_gradient(fitness: torch.Tensor, seeds: torch.Tensor, bias_shape
     seeds = _seeds(seeds)
     fitness = _fitness(fitness, pop_size, seeds)
     (out_f,) = (int(d) for d in bias_shape)
-    g = torch.empty((out_f,), dtype=torch.float32, device=fitness.device)
-    st = lib.vn_bias_gradient(_ptr(fitness), _ptr(seeds), pop_size, out_f, float(sigma),
-                              int(offset) & _M64, _ptr(g), _stream(g))
+    dev = _device(fitness, seeds)
+    g = torch.empty((out_f,), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        st = lib.vn_bias_gradient(_ptr(fitness), _ptr(seeds), pop_size, out_f, float(sigma),
+                                  int(offset) & _M64, _ptr(g), _stream(g))
     check(st, "vn_bias_gradient")
     return g
 
@@ -231,9 +246,11 @@ def virtual_flat_gradient(fitness: torch.Tensor, seeds: torch.Tensor, n_params: 
         raise ValueError("noise must be 'uniform' or 'gaussian'")
     seeds = _seeds(seeds)
     fitness = _fitness(fitness, pop_size, seeds)
-    g = torch.empty((int(n_params),), dtype=torch.float32, device=fitness.device)
-    st = lib.vn_gradient_ex(_ptr(fitness), _ptr(seeds), pop_size, int(n_params), float(sigma),
-                            int(offset) & _M64, _NOISE[noise], _ptr(g), _stream(g))
+    dev = _device(fitness, seeds)
+    g = torch.empty((int(n_params),), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        st = lib.vn_gradient_ex(_ptr(fitness), _ptr(seeds), pop_size, int(n_params), float(sigma),
+                                int(offset) & _M64, _NOISE[noise], _ptr(g), _stream(g))
     check(st, "vn_gradient_ex")
     return g
 
@@ -252,10 +269,12 @@ def gradient_update(fitness: torch.Tensor, seeds: torch.Tensor, theta: torch.Ten
         raise ValueError("theta must be a contiguous float32 CUDA tensor (updated in place)")
     seeds = _seeds(seeds)
     fitness = _fitness(fitness, pop_size, seeds)
-    g = torch.empty((theta.numel(),), dtype=torch.float32, device=theta.device)
-    st = lib.vn_gradient_update(_ptr(fitness), _ptr(seeds), pop_size, theta.numel(), float(sigma),
-                                int(offset) & _M64, _NOISE[noise], float(lr), _ptr(g), _ptr(theta),
-                                _stream(g))
+    dev = _device(fitness, seeds, theta)
+    g = torch.empty((theta.numel(),), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        st = lib.vn_gradient_update(_ptr(fitness), _ptr(seeds), pop_size, theta.numel(), float(sigma),
+                                    int(offset) & _M64, _NOISE[noise], float(lr), _ptr(g), _ptr(theta),
+                                    _stream(g))
     check(st, "vn_gradient_update")
     return g
 
@@ -269,8 +288,9 @@ def noise_dump(seeds: torch.Tensor, n_elements: int, offset: int, *,
         raise ValueError("noise must be 'uniform' or 'gaussian'")
     seeds = _seeds(seeds)
     d = torch.empty((seeds.numel(), int(n_elements)), dtype=torch.float32, device=seeds.device)
-    st = lib.vn_noise_dump_ex(_ptr(seeds), seeds.numel(), int(n_elements), int(offset) & _M64,
-                              _NOISE[noise], _ptr(d), _stream(d))
+    with torch.cuda.device(seeds.device):
+        st = lib.vn_noise_dump_ex(_ptr(seeds), seeds.numel(), int(n_elements), int(offset) & _M64,
+                                  _NOISE[noise], _ptr(d), _stream(d))
     check(st, "vn_noise_dump")
     return d
 
@@ -283,9 +303,11 @@ def virtual_reduce_metric(center: torch.Tensor, seeds: torch.Tensor, sigma: floa
     if center.numel() != n_params:
         raise ValueError(f"center has {center.numel()} elements, n_params={n_params}")
     seeds = _seeds(seeds)
-    f = torch.empty((seeds.numel(),), dtype=torch.float32, device=center.device)
-    st = lib.vn_reduce_metric(_ptr(center), _ptr(seeds), seeds.numel(), int(n_params), float(sigma),
-                              int(offset) & _M64, _ptr(f), _stream(f))
+    dev = _device(center, seeds)
+    f = torch.empty((seeds.numel(),), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        st = lib.vn_reduce_metric(_ptr(center), _ptr(seeds), seeds.numel(), int(n_params),
+                                  float(sigma), int(offset) & _M64, _ptr(f), _stream(f))
     check(st, "vn_reduce_metric")
     return f
 
@@ -299,7 +321,9 @@ def centered_ranks(fitness: torch.Tensor, *, out: Optional[torch.Tensor] = None)
         out = torch.empty(pop, dtype=torch.float32, device=fitness.device)
     elif out.shape != (pop,) or out.dtype != torch.float32 or not out.is_contiguous():
         raise ValueError("out must be a contiguous float32 tensor of shape (pop,)")
-    check(lib.vn_centered_ranks(_ptr(fitness), pop, _ptr(out), _stream(fitness)), "vn_centered_ranks")
+    with torch.cuda.device(_device(fitness, out)):
+        st = lib.vn_centered_ranks(_ptr(fitness), pop, _ptr(out), _stream(fitness))
+    check(st, "vn_centered_ranks")
     return out
 
 
@@ -312,8 +336,9 @@ def es_update(theta: torch.Tensor, grad: torch.Tensor, lr: float) -> torch.Tenso
     grad = _cuda(grad, "grad").to(torch.float32)
     if grad.numel() != theta.numel():
         raise ValueError("grad and theta differ in size")
-    check(lib.vn_es_update(_ptr(theta), _ptr(grad), theta.numel(), float(lr), _stream(theta)),
-          "vn_es_update")
+    with torch.cuda.device(_device(theta, grad)):
+        st = lib.vn_es_update(_ptr(theta), _ptr(grad), theta.numel(), float(lr), _stream(theta))
+    check(st, "vn_es_update")
     return theta
 
 
@@ -329,9 +354,14 @@ def compute_offsets(param_shapes: Sequence[Sequence[int]]) -> list:
 def perturbed_linear_path(x: torch.Tensor, weight: torch.Tensor) -> str:
     """"tc" or "ffma": the kernel ``virtual_perturbed_linear`` would use (no launch)."""
     lib = load()
+    for t, name in ((x, "x"), (weight, "weight")):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
     batch = x.shape[-2]
-    p = lib.vn_perturbed_linear_path(_ptr(x), _dt(x, "x"), int(x.dim() == 2), _ptr(weight),
-                                     _dt(weight, "weight"), batch, weight.shape[1], weight.shape[0])
+    with torch.cuda.device(_device(x, weight)):
+        p = lib.vn_perturbed_linear_path(_ptr(x), _dt(x, "x"), int(x.dim() == 2), _ptr(weight),
+                                         _dt(weight, "weight"), batch, weight.shape[1],
+                                         weight.shape[0])
     return "tc" if p == _lib.VN_PATH_TC else "ffma"
 
 

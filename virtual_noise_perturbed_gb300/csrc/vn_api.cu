@@ -5,7 +5,6 @@
 
 #include <cmath>
 #include <cstdio>
-#include <cstring>
 #include <mutex>
 
 #include "vn.h"
@@ -57,6 +56,13 @@ bool aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % 
 
 // r = a * b, false when it does not fit in int64 (inputs are >= 0).
 bool mul(int64_t a, int64_t b, int64_t* r) { return !__builtin_mul_overflow(a, b, r); }
+
+// The byte ranges [p, p + pb) and [q, q + qb) share a byte (an empty range shares none).
+bool overlap(const void* p, int64_t pb, const void* q, int64_t qb) {
+  if (p == nullptr || q == nullptr || pb <= 0 || qb <= 0) return false;
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(q);
+  return a < b + static_cast<uintptr_t>(qb) && b < a + static_cast<uintptr_t>(pb);
+}
 
 bool float_sigma(double sigma, float* out) {
   if (!std::isfinite(sigma)) return false;
@@ -111,6 +117,9 @@ vn_status vn_noise_dump_ex(const int64_t* seeds, int64_t pop, int64_t n, uint64_
   if (total == 0) return VN_OK;
   if (seeds == nullptr || out == nullptr) return VN_ERR_NULL;
   if (!aligned(seeds, 8) || !aligned(out, 4)) return VN_ERR_ALIGN;
+  int64_t out_bytes, seed_bytes;
+  if (!mul(total, 4, &out_bytes) || !mul(pop, 8, &seed_bytes)) return VN_ERR_OVERFLOW;
+  if (overlap(out, out_bytes, seeds, seed_bytes)) return VN_ERR_VALUE;
   return launched(vn::launch_noise_dump(seeds, pop, n, offset, kind, out,
                                         static_cast<cudaStream_t>(stream)));
 }
@@ -132,12 +141,17 @@ static vn_status gradient(const float* fitness, const int64_t* seeds, int64_t po
   if (m == 0) return VN_OK;
   if (fitness == nullptr || seeds == nullptr || grad == nullptr) return VN_ERR_NULL;
   if (!aligned(fitness, 4) || !aligned(seeds, 8) || !aligned(grad, 4)) return VN_ERR_ALIGN;
-  if (theta != nullptr) {
-    if (!aligned(theta, 4)) return VN_ERR_ALIGN;
-    const uintptr_t t0 = reinterpret_cast<uintptr_t>(theta), g0 = reinterpret_cast<uintptr_t>(grad);
-    const uintptr_t bytes = static_cast<uintptr_t>(m) * 4;
-    if (t0 < g0 + bytes && g0 < t0 + bytes) return VN_ERR_VALUE;  // theta and grad overlap
-  }
+  if (theta != nullptr && !aligned(theta, 4)) return VN_ERR_ALIGN;
+  int64_t m_bytes, seed_bytes;
+  if (!mul(m, 4, &m_bytes) || !mul(pop, 8, &seed_bytes)) return VN_ERR_OVERFLOW;
+  const int64_t fit_bytes = pop * 4;
+  // The outputs (grad, and theta when given) may not share memory with an input or each other.
+  if (overlap(grad, m_bytes, fitness, fit_bytes) || overlap(grad, m_bytes, seeds, seed_bytes))
+    return VN_ERR_VALUE;
+  if (theta != nullptr &&
+      (overlap(theta, m_bytes, grad, m_bytes) || overlap(theta, m_bytes, fitness, fit_bytes) ||
+       overlap(theta, m_bytes, seeds, seed_bytes)))
+    return VN_ERR_VALUE;
   return launched(vn::launch_grad(fitness, seeds, pop, m, offset, scale, kind, grad,
                                   static_cast<cudaStream_t>(stream), theta, lr_f));
 }
@@ -182,6 +196,11 @@ vn_status vn_reduce_metric(const float* center, const int64_t* seeds, int64_t po
   if (pop == 0) return VN_OK;
   if (center == nullptr || seeds == nullptr || fitness == nullptr) return VN_ERR_NULL;
   if (!aligned(center, 4) || !aligned(seeds, 8) || !aligned(fitness, 4)) return VN_ERR_ALIGN;
+  int64_t center_bytes, seed_bytes;
+  if (!mul(n_params, 4, &center_bytes) || !mul(pop, 8, &seed_bytes)) return VN_ERR_OVERFLOW;
+  const int64_t fit_bytes = pop * 4;  // fits: pop * 8 does
+  if (overlap(fitness, fit_bytes, center, center_bytes) || overlap(fitness, fit_bytes, seeds, seed_bytes))
+    return VN_ERR_VALUE;
   const float inv_n = static_cast<float>(1.0 / static_cast<double>(n_params));
   return launched(vn::launch_reduce_metric(center, seeds, pop, n_params, sig, inv_n, offset,
                                            fitness, static_cast<cudaStream_t>(stream)));
@@ -233,6 +252,16 @@ vn_status vn_perturbed_linear_kind(const void* x, vn_dtype x_dt, int x_shared, c
   if (!aligned(seeds, 8) || !aligned(y, dtype_size(y_dt)) || !aligned(x, dtype_size(x_dt)) ||
       !aligned(w, dtype_size(w_dt)) || (b != nullptr && !aligned(b, dtype_size(b_dt))))
     return VN_ERR_ALIGN;
+  {
+    int64_t yb, xb, wb, bb, sb;
+    if (!mul(y_elems, dtype_size(y_dt), &yb) || !mul(x_elems, dtype_size(x_dt), &xb) ||
+        !mul(w_elems, dtype_size(w_dt), &wb) || !mul(out, dtype_size(b_dt), &bb) ||
+        !mul(pop, 8, &sb))
+      return VN_ERR_OVERFLOW;
+    if (overlap(y, yb, x, xb) || overlap(y, yb, w, wb) || overlap(y, yb, b, bb) ||
+        overlap(y, yb, seeds, sb))
+      return VN_ERR_VALUE;
+  }
 
   vn::LinearArgs a;
   a.x = x; a.x_dt = x_dt; a.x_shared = x_shared ? 1 : 0;
@@ -361,6 +390,18 @@ vn_status vn_perturbed_mlp_ex(const void* x, vn_dtype x_dt, int x_shared, int64_
   if (y_elems == 0) return VN_OK;
   if (seeds == nullptr || y == nullptr || (x_elems > 0 && x == nullptr)) return VN_ERR_NULL;
   if (!aligned(seeds, 8) || !aligned(y, 4) || !aligned(x, dtype_size(x_dt))) return VN_ERR_ALIGN;
+  {
+    int64_t yb, xb, sb;
+    if (!mul(y_elems, 4, &yb) || !mul(x_elems, dtype_size(x_dt), &xb) || !mul(pop, 8, &sb))
+      return VN_ERR_OVERFLOW;
+    if (overlap(y, yb, x, xb) || overlap(y, yb, seeds, sb)) return VN_ERR_VALUE;
+    for (int64_t l = 0; l < n_layers; ++l) {
+      int64_t wb;
+      if (!mul(dims[l] * dims[l + 1], 4, &wb)) return VN_ERR_OVERFLOW;  // the product fits: checked above
+      if (overlap(y, yb, w[l], wb) || (b != nullptr && overlap(y, yb, b[l], dims[l + 1] * 4)))
+        return VN_ERR_VALUE;
+    }
+  }
   // The one device-dependent check: both activation buffers of one individual
   // must fit in the device's shared memory.
   const size_t buf = vn::mlp_buffer_floats(static_cast<int>(n_layers), dims);
@@ -385,9 +426,7 @@ vn_status vn_centered_ranks(const float* fitness, int64_t pop, float* out, void*
   if (pop == 0) return VN_OK;
   if (fitness == nullptr || out == nullptr) return VN_ERR_NULL;
   if (!aligned(fitness, 4) || !aligned(out, 4)) return VN_ERR_ALIGN;
-  const uintptr_t f0 = reinterpret_cast<uintptr_t>(fitness), o0 = reinterpret_cast<uintptr_t>(out);
-  const uintptr_t bytes = static_cast<uintptr_t>(pop) * 4;
-  if (f0 < o0 + bytes && o0 < f0 + bytes) return VN_ERR_VALUE;  // in and out overlap
+  if (overlap(out, pop * 4, fitness, pop * 4)) return VN_ERR_VALUE;  // pop < 2^31: no overflow
   return launched(vn::launch_centered_ranks(fitness, pop, out, static_cast<cudaStream_t>(stream)));
 }
 
@@ -398,6 +437,9 @@ vn_status vn_es_update(float* theta, const float* grad, int64_t n, double lr, vo
   if (n == 0) return VN_OK;
   if (theta == nullptr || grad == nullptr) return VN_ERR_NULL;
   if (!aligned(theta, 4) || !aligned(grad, 4)) return VN_ERR_ALIGN;
+  int64_t bytes;
+  if (!mul(n, 4, &bytes)) return VN_ERR_OVERFLOW;
+  if (overlap(theta, bytes, grad, bytes)) return VN_ERR_VALUE;
   return launched(vn::launch_es_update(theta, grad, n, lr_f, static_cast<cudaStream_t>(stream)));
 }
 
