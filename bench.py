@@ -464,6 +464,14 @@ def step_elements(wl) -> int:
     return el
 
 
+def compute_dtype(wl) -> str:
+    """The arithmetic type of the step's contraction: bf16 where the forward runs on
+    the tensor cores (bf16 activations), f32 otherwise (the policy chain, the CUDA-core
+    forward, and the gradient-only step, which has no forward)."""
+    import torch
+    return "bf16" if wl.forward and wl.x.dtype == torch.bfloat16 else "f32"
+
+
 def config_for(wl, world, noise="uniform"):
     return {"workload": wl.name, "description": wl.description, "noise": noise, "pop": wl.pop, "batch": wl.batch,
             "layers": [[l.in_f, l.out_f] for l in wl.layers], "sigma": wl.sigma,
@@ -690,7 +698,7 @@ def main(argv=None) -> int:
                                                             if graph_error else ""))
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": total_ms_max / args.steps, "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "f32" if wl.number in (1, 2) else "bf16",
+                "scaling": "weak", "vs_baseline": None, "dtype": compute_dtype(wl),
                 "data": "synthetic", "config": cfg, "roofline": roofline, "cpu_baseline": cpu,
                 "e2e": e2e, "gpu_launches": n_launches * (k_steps + k_kern), "clocks": clocks,
                 "kernels": kernels, **extra, "wall_s_timed_region": wall}

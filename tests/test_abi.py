@@ -240,3 +240,45 @@ def test_binding_requires_one_device_per_call():
     with pytest.raises(ValueError, match="share a device"):
         api._device(torch.empty(1), torch.empty(1, device="meta"))
     assert api._device(torch.empty(1), None, torch.empty(2)) == torch.device("cpu")
+
+
+def test_concurrent_builds_take_turns_and_build_once(monkeypatch, tmp_path):
+    """build() holds a file lock around compile and link: callers that start together
+    (the ranks of one job) build one at a time, and one that finds the library current
+    after waiting does not build again. The compile step is a stand-in here."""
+    import threading
+    import time
+
+    from virtual_noise_perturbed_gb300 import build as b
+    monkeypatch.setattr(b, "BUILD", str(tmp_path))
+    state = {"current": False, "spans": []}
+    monkeypatch.setattr(b, "up_to_date", lambda: state["current"])
+
+    def compile_step(verbose, extra_flags):
+        t0 = time.monotonic()
+        time.sleep(0.2)
+        state["spans"].append((t0, time.monotonic()))
+
+    monkeypatch.setattr(b, "_compile_and_link", compile_step)
+    threads = [threading.Thread(target=b.build, kwargs={"force": True}) for _ in range(3)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    spans = sorted(state["spans"])
+    assert len(spans) == 3                                    # forced: each builds, in turn
+    assert all(a[1] <= c[0] for a, c in zip(spans, spans[1:]))
+
+    state["spans"].clear()
+
+    def compile_once(verbose, extra_flags):
+        compile_step(verbose, extra_flags)
+        state["current"] = True
+
+    monkeypatch.setattr(b, "_compile_and_link", compile_once)
+    threads = [threading.Thread(target=b.build) for _ in range(3)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert len(state["spans"]) == 1                           # the others found it current

@@ -1,7 +1,7 @@
 """The bench's JSON contract on the CPU: the reference arm (the oracle timed on the
 host) prints one line with the keys the driver reads, and the per-step element
 count it reports is the workload's definition (pop x weights for the forward, pop x
-parameters for the gradients and the dump)."""
+parameters for the gradients and the dump), as is the dtype it names."""
 
 import json
 import os
@@ -25,6 +25,8 @@ def test_step_elements(number):
     want = {1: wl.pop * (weights + 2 * params), 2: wl.pop * (weights + 2 * params),
             3: wl.pop * (weights + params), 4: wl.pop * params, 5: wl.pop * weights}[number]
     assert bench.step_elements(wl) == want
+    # the JSON line's dtype: bf16 only where the forward runs on the tensor cores
+    assert bench.compute_dtype(wl) == {1: "f32", 2: "f32", 3: "bf16", 4: "f32", 5: "bf16"}[number]
 
 
 def test_reference_arm_prints_one_json_line():

@@ -6,13 +6,16 @@ Each ``csrc/*.cu`` file is compiled in parallel to ``_build/*.o`` and the
 objects are linked into ``virtual_noise_perturbed_gb300/libvn.so`` (CUDA
 runtime linked statically; the driver API is reached through the runtime's
 entry-point query, so no link against libcuda is needed). A rebuild happens
-only when a source or header is newer than the library.
+only when a source or header is newer than the library. Builds take a file lock,
+so processes that start together (the ranks of one job, test workers) build
+once: the others wait, then find the library current.
 """
 
 from __future__ import annotations
 
 import argparse
 import concurrent.futures as cf
+import fcntl
 import glob
 import os
 import shutil
@@ -67,10 +70,22 @@ def _run(cmd, verbose):
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    """Compile and link libvn.so; returns its path."""
+    """Compile and link libvn.so unless it is current; returns its path."""
     if not force and up_to_date():
         return LIB
     os.makedirs(BUILD, exist_ok=True)
+    with open(os.path.join(BUILD, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            if not force and up_to_date():  # another process built it while this one waited
+                return LIB
+            _compile_and_link(verbose, extra_flags)
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
+    return LIB
+
+
+def _compile_and_link(verbose: bool, extra_flags) -> None:
     cc = nvcc()
     flags = CFLAGS + list(extra_flags or [])
     objs, cmds = [], []
@@ -83,7 +98,6 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
     tmp = LIB + ".tmp"
     _run([cc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"], verbose)
     os.replace(tmp, LIB)
-    return LIB
 
 
 def main(argv=None) -> int:
