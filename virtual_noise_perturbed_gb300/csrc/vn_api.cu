@@ -13,7 +13,6 @@
 namespace vn {
 
 cudaError_t device_info(DeviceInfo* info) {
-  constexpr int kMaxDevices = 64;
   static DeviceInfo cache[kMaxDevices];
   static std::mutex mu;
   int dev = 0;

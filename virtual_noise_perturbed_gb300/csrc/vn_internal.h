@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 
 #include "vn.h"
+#include "vn_smem.h"
 
 namespace vn {
 

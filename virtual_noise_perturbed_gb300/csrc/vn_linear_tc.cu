@@ -721,13 +721,9 @@ template <int MH, bool kW, bool kY, bool kHook, int kKind, bool kG1>
 cudaError_t launch_kernel(const CUtensorMap& xmap, const CUtensorMap& wmap, const TcParams& p,
                           int grid, size_t smem, cudaStream_t stream) {
   auto fn = linear_tc_kernel<MH, kW, kY, kHook, kKind, kG1>;
-  static size_t configured = 0;
-  if (configured < smem) {
-    cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(smem));
-    if (err != cudaSuccess) return err;
-    configured = smem;
-  }
+  static SmemRecord configured;
+  const cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), smem, configured);
+  if (err != cudaSuccess) return err;
   fn<<<grid, kThreads, smem, stream>>>(xmap, wmap, p);
   return cudaGetLastError();
 }

@@ -323,13 +323,9 @@ template <int NB, int kP, int kKind>
 cudaError_t launch_p(MlpDev& d, cudaStream_t stream, size_t smem) {
   auto fn = mlp_kernel<NB, kP, kKind>;
   if (smem > 48 * 1024) {
-    static size_t configured = 0;
-    if (configured < smem) {
-      cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
-      if (err != cudaSuccess) return err;
-      configured = smem;
-    }
+    static SmemRecord configured;
+    const cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), smem, configured);
+    if (err != cudaSuccess) return err;
   }
   const int64_t grid = (d.pop + kP - 1) / kP;
   fn<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(d);
