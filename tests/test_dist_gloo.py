@@ -61,3 +61,22 @@ def test_single_rank_defaults():
         os.environ.pop(v, None)
     assert bench.dist_env() == (1, 0, 0)
     assert bench.max_over_ranks(3.5, 1) == 3.5
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    """The reference arm launched as the multi-GPU bench is: rank 0 alone times the
+    oracle and prints the one JSON line; the other rank exits 0 without work."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()),
+           os.path.join(root, "bench.py"), "--impl", "reference", "--workload", "tiny",
+           "--gpus", "2", "--steps", "1", "--warmup", "3"]
+    out = subprocess.run(cmd, capture_output=True, text=True, timeout=300, cwd=root)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
