@@ -815,8 +815,11 @@ def host_link(step_set, host_in, host_out, load_stream, copy_stream, dev, reps=5
     d2h_ms = timed(copy_stream, back)
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
     d2h = sum(v.numel() * v.element_size() for v in host_out)
-    return {"h2d_ms": h2d_ms, "d2h_ms": d2h_ms, "h2d_gbs": h2d / (h2d_ms * 1e-3) / 1e9,
-            "d2h_gbs": d2h / (d2h_ms * 1e-3) / 1e9, "bound_ms_per_step": max(h2d_ms, d2h_ms)}
+    def gbs(nbytes, ms):
+        return nbytes / (ms * 1e-3) / 1e9 if ms > 0 else None
+
+    return {"h2d_ms": h2d_ms, "d2h_ms": d2h_ms, "h2d_gbs": gbs(h2d, h2d_ms), "d2h_gbs": gbs(d2h, d2h_ms),
+            "bound_ms_per_step": max(h2d_ms, d2h_ms)}
 
 
 if __name__ == "__main__":
