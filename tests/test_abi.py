@@ -282,3 +282,17 @@ def test_concurrent_builds_take_turns_and_build_once(monkeypatch, tmp_path):
     for t in threads:
         t.join()
     assert len(state["spans"]) == 1                           # the others found it current
+
+
+def test_binding_output_buffers_are_checked():
+    """``out=`` buffers must be contiguous float32 of the result's shape on the call's device."""
+    import torch
+    from virtual_noise_perturbed_gb300 import api
+    cpu = torch.device("cpu")
+    buf = torch.zeros(3, 4)
+    assert api._out(buf, (3, 4), cpu) is buf
+    assert api._out(None, (2,), cpu).shape == (2,)
+    for bad in (torch.zeros(4, 3), torch.zeros(3, 4, dtype=torch.float64), torch.zeros(4, 3).t(),
+                torch.zeros(3, 4, device="meta")):
+        with pytest.raises(ValueError):
+            api._out(bad, (3, 4), cpu)

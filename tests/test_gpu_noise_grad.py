@@ -7,9 +7,9 @@ import torch
 
 from oracle import es
 from tests.parity import TOL_FP32, assert_close, to_np
-from virtual_noise_perturbed_gb300 import (VNError, compute_offsets, noise_dump, virtual_bias_gradient,
-                                           virtual_flat_gradient, virtual_reduce_metric,
-                                           virtual_weight_gradient, workloads)
+from virtual_noise_perturbed_gb300 import (VNError, compute_offsets, gradient_update, noise_dump,
+                                           virtual_bias_gradient, virtual_flat_gradient,
+                                           virtual_reduce_metric, virtual_weight_gradient, workloads)
 from virtual_noise_perturbed_gb300.build import build
 
 pytestmark = pytest.mark.gpu
@@ -225,3 +225,38 @@ def test_invalid_calls_raise():
         virtual_weight_gradient(torch.ones(3, device=DEV), s, (2, 2), 0.1, 4, 0)
     with pytest.raises(ValueError):
         noise_dump(torch.arange(4), 3, 0)  # CPU tensor: no CPU path exists
+
+
+def test_output_buffers_are_written_in_place():
+    """``out=``: the result lands in the caller's buffer (NaN-filled first), which is
+    returned, with the bits a fresh call gives; a buffer of the wrong shape is refused."""
+    g = torch.Generator().manual_seed(21)
+    pop, n, sigma, off = 37, 1003, 0.03, 12345
+    seeds = (torch.arange(pop, dtype=torch.int64) * 7 - 3).to(DEV)
+    fit = torch.randn(pop, generator=g).to(DEV)
+    center = torch.randn(n, generator=g).to(DEV)
+
+    def into(fn, shape, *args, **kw):
+        want = fn(*args, **kw)
+        buf = torch.full(shape, float("nan"), device=DEV)
+        got = fn(*args, out=buf, **kw)
+        assert got is buf and torch.equal(got, want), fn.__name__
+
+    into(noise_dump, (pop, n), seeds, n, off)
+    into(noise_dump, (pop, n), seeds, n, off, noise="gaussian")
+    into(virtual_weight_gradient, (17, 59), fit, seeds, (17, 59), sigma, pop, off)
+    into(virtual_bias_gradient, (17,), fit, seeds, (17,), sigma, pop, off)
+    into(virtual_flat_gradient, (n,), fit, seeds, n, sigma, pop, off)
+    into(virtual_reduce_metric, (pop,), center, seeds, sigma, n, off)
+
+    theta0 = torch.randn(n, generator=g).to(DEV)
+    theta_a, theta_b = theta0.clone(), theta0.clone()
+    grad_a = gradient_update(fit, seeds, theta_a, sigma, pop, 0.1, off)
+    buf = torch.full((n,), float("nan"), device=DEV)
+    grad_b = gradient_update(fit, seeds, theta_b, sigma, pop, 0.1, off, out=buf)
+    assert grad_b is buf and torch.equal(grad_a, grad_b) and torch.equal(theta_a, theta_b)
+
+    with pytest.raises(ValueError):
+        noise_dump(seeds, n, off, out=torch.empty(pop, n + 1, device=DEV))
+    with pytest.raises(ValueError):
+        virtual_flat_gradient(fit, seeds, n, sigma, pop, off, out=torch.empty(n, dtype=torch.float64, device=DEV))

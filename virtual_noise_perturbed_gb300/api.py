@@ -59,6 +59,17 @@ def _ptr(t: Optional[torch.Tensor]) -> ctypes.c_void_p:
     return ctypes.c_void_p(0 if t is None or t.numel() == 0 else t.data_ptr())
 
 
+def _out(out: Optional[torch.Tensor], shape, device: torch.device) -> torch.Tensor:
+    """The caller's float32 output buffer, checked (shape, dtype, layout, device), or a new one."""
+    shape = tuple(int(d) for d in shape)
+    if out is None:
+        return torch.empty(shape, dtype=torch.float32, device=device)
+    if not isinstance(out, torch.Tensor) or tuple(out.shape) != shape or out.dtype != torch.float32 \
+            or not out.is_contiguous() or out.device != device:
+        raise ValueError(f"out must be a contiguous float32 tensor of shape {shape} on {device}")
+    return out
+
+
 def _device(*tensors: Optional[torch.Tensor]) -> torch.device:
     """The one device every tensor of a call is on. The library launches on the
     current CUDA device, so each call runs with this device made current."""
@@ -200,14 +211,16 @@ def _fitness(fitness: torch.Tensor, pop_size: int, seeds: torch.Tensor) -> torch
 
 
 def virtual_weight_gradient(fitness: torch.Tensor, seeds: torch.Tensor, weight_shape: Sequence[int],
-                            sigma: float, pop_size: int, offset: int) -> torch.Tensor:
-    """grad[j, k] = sum_i fitness_i * N_i[j, k] / (pop_size * sigma), fp32, weight_shape."""
+                            sigma: float, pop_size: int, offset: int, *,
+                            out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """grad[j, k] = sum_i fitness_i * N_i[j, k] / (pop_size * sigma), fp32, weight_shape
+    (written into ``out`` when given)."""
     lib = load()
     seeds = _seeds(seeds)
     fitness = _fitness(fitness, pop_size, seeds)
     out_f, in_f = (int(d) for d in weight_shape)
     dev = _device(fitness, seeds)
-    g = torch.empty((out_f, in_f), dtype=torch.float32, device=dev)
+    g = _out(out, (out_f, in_f), dev)
     with torch.cuda.device(dev):
         st = lib.vn_weight_gradient(_ptr(fitness), _ptr(seeds), pop_size, out_f, in_f, float(sigma),
                                     int(offset) & _M64, _ptr(g), _stream(g))
@@ -216,14 +229,16 @@ def virtual_weight_gradient(fitness: torch.Tensor, seeds: torch.Tensor, weight_s
 
 
 def virtual_bias_gradient(fitness: torch.Tensor, seeds: torch.Tensor, bias_shape: Sequence[int],
-                          sigma: float, pop_size: int, offset: int) -> torch.Tensor:
-    """grad[j] = sum_i fitness_i * nb_i[j] / (pop_size * sigma); ``offset`` points at the bias region."""
+                          sigma: float, pop_size: int, offset: int, *,
+                          out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """grad[j] = sum_i fitness_i * nb_i[j] / (pop_size * sigma); ``offset`` points at the bias
+    region (written into ``out`` when given)."""
     lib = load()
     seeds = _seeds(seeds)
     fitness = _fitness(fitness, pop_size, seeds)
     (out_f,) = (int(d) for d in bias_shape)
     dev = _device(fitness, seeds)
-    g = torch.empty((out_f,), dtype=torch.float32, device=dev)
+    g = _out(out, (out_f,), dev)
     with torch.cuda.device(dev):
         st = lib.vn_bias_gradient(_ptr(fitness), _ptr(seeds), pop_size, out_f, float(sigma),
                                   int(offset) & _M64, _ptr(g), _stream(g))
@@ -232,7 +247,8 @@ def virtual_bias_gradient(fitness: torch.Tensor, seeds: torch.Tensor, bias_shape
 
 
 def virtual_flat_gradient(fitness: torch.Tensor, seeds: torch.Tensor, n_params: int, sigma: float,
-                          pop_size: int, offset: int = 0, *, noise: str = "uniform") -> torch.Tensor:
+                          pop_size: int, offset: int = 0, *, noise: str = "uniform",
+                          out: Optional[torch.Tensor] = None) -> torch.Tensor:
     """grad[t] = sum_i fitness_i * PRNG(seed_i, offset + t) / (pop_size * sigma), t < n_params.
 
     With parameter blocks laid out by ``compute_offsets`` (weights then bias, one
@@ -240,14 +256,15 @@ def virtual_flat_gradient(fitness: torch.Tensor, seeds: torch.Tensor, n_params: 
     block b's gradient is ``grad[offsets[b] : offsets[b] + numel_b]`` reshaped to the
     block's shape, equal (up to the order of the fp32 sums) to
     ``virtual_weight_gradient`` / ``virtual_bias_gradient`` on that block.
-    ``noise="gaussian"`` uses the Box-Muller variant of the noise instead."""
+    ``noise="gaussian"`` uses the Box-Muller variant of the noise instead; ``out`` receives
+    the result when given."""
     lib = load()
     if noise not in _NOISE:
         raise ValueError("noise must be 'uniform' or 'gaussian'")
     seeds = _seeds(seeds)
     fitness = _fitness(fitness, pop_size, seeds)
     dev = _device(fitness, seeds)
-    g = torch.empty((int(n_params),), dtype=torch.float32, device=dev)
+    g = _out(out, (int(n_params),), dev)
     with torch.cuda.device(dev):
         st = lib.vn_gradient_ex(_ptr(fitness), _ptr(seeds), pop_size, int(n_params), float(sigma),
                                 int(offset) & _M64, _NOISE[noise], _ptr(g), _stream(g))
@@ -256,11 +273,12 @@ def virtual_flat_gradient(fitness: torch.Tensor, seeds: torch.Tensor, n_params: 
 
 
 def gradient_update(fitness: torch.Tensor, seeds: torch.Tensor, theta: torch.Tensor, sigma: float,
-                    pop_size: int, lr: float, offset: int = 0, *, noise: str = "uniform") -> torch.Tensor:
+                    pop_size: int, lr: float, offset: int = 0, *, noise: str = "uniform",
+                    out: Optional[torch.Tensor] = None) -> torch.Tensor:
     """The flat gradient estimate and the ES step in one launch (``vn_gradient_update``):
     grad = virtual_flat_gradient(fitness, seeds, theta.numel(), sigma, pop_size, offset),
-    then theta += lr * grad in place (fp32 fma). Returns grad; both are bit-identical
-    to the two separate calls."""
+    then theta += lr * grad in place (fp32 fma). Returns grad (in ``out`` when given); both
+    are bit-identical to the two separate calls."""
     lib = load()
     if noise not in _NOISE:
         raise ValueError("noise must be 'uniform' or 'gaussian'")
@@ -270,7 +288,7 @@ def gradient_update(fitness: torch.Tensor, seeds: torch.Tensor, theta: torch.Ten
     seeds = _seeds(seeds)
     fitness = _fitness(fitness, pop_size, seeds)
     dev = _device(fitness, seeds, theta)
-    g = torch.empty((theta.numel(),), dtype=torch.float32, device=dev)
+    g = _out(out, (theta.numel(),), dev)
     with torch.cuda.device(dev):
         st = lib.vn_gradient_update(_ptr(fitness), _ptr(seeds), pop_size, theta.numel(), float(sigma),
                                     int(offset) & _M64, _NOISE[noise], float(lr), _ptr(g), _ptr(theta),
@@ -280,14 +298,15 @@ def gradient_update(fitness: torch.Tensor, seeds: torch.Tensor, theta: torch.Ten
 
 
 def noise_dump(seeds: torch.Tensor, n_elements: int, offset: int, *,
-               noise: str = "uniform") -> torch.Tensor:
+               noise: str = "uniform", out: Optional[torch.Tensor] = None) -> torch.Tensor:
     """(pop, n) fp32 noise, D[i, t] = PRNG(seed_i, offset + t): the centered uniform
-    (bit-exact), or with ``noise="gaussian"`` the Box-Muller variant."""
+    (bit-exact), or with ``noise="gaussian"`` the Box-Muller variant; written into ``out``
+    when given."""
     lib = load()
     if noise not in _NOISE:
         raise ValueError("noise must be 'uniform' or 'gaussian'")
     seeds = _seeds(seeds)
-    d = torch.empty((seeds.numel(), int(n_elements)), dtype=torch.float32, device=seeds.device)
+    d = _out(out, (seeds.numel(), int(n_elements)), seeds.device)
     with torch.cuda.device(seeds.device):
         st = lib.vn_noise_dump_ex(_ptr(seeds), seeds.numel(), int(n_elements), int(offset) & _M64,
                                   _NOISE[noise], _ptr(d), _stream(d))
@@ -296,15 +315,15 @@ def noise_dump(seeds: torch.Tensor, n_elements: int, offset: int, *,
 
 
 def virtual_reduce_metric(center: torch.Tensor, seeds: torch.Tensor, sigma: float, n_params: int,
-                          offset: int = 0) -> torch.Tensor:
-    """fitness[i] = mean_k |center[k] + sigma * noise[i, k]|, (pop,) fp32."""
+                          offset: int = 0, *, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """fitness[i] = mean_k |center[k] + sigma * noise[i, k]|, (pop,) fp32 (in ``out`` when given)."""
     lib = load()
     center = _cuda(center, "center").reshape(-1).to(torch.float32)
     if center.numel() != n_params:
         raise ValueError(f"center has {center.numel()} elements, n_params={n_params}")
     seeds = _seeds(seeds)
     dev = _device(center, seeds)
-    f = torch.empty((seeds.numel(),), dtype=torch.float32, device=dev)
+    f = _out(out, (seeds.numel(),), dev)
     with torch.cuda.device(dev):
         st = lib.vn_reduce_metric(_ptr(center), _ptr(seeds), seeds.numel(), int(n_params),
                                   float(sigma), int(offset) & _M64, _ptr(f), _stream(f))
