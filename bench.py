@@ -366,6 +366,43 @@ def barrier(world: int):
         dist.barrier()
 
 
+def roofline_of(per_kernel, pk, workload):
+    """The roofline object of the dominant kernel (the one with the most time) from the
+    kernel pass's per-kernel sums {"ms", "launches", "elements", "flops", "hbm_bytes"}:
+    achieved = algorithmic work of its launches / their event time, against each bound
+    that applies -- the integer ALU pipe (12 operations per noise element; 13 for the
+    Gaussian kind, which also has the MUFU and issue bounds), HBM when the launch has
+    algorithmic bytes, the tensor pipe when it has flops -- and the tightest one reported."""
+    dom = max(per_kernel, key=lambda n: per_kernel[n]["ms"])
+    r = per_kernel[dom]
+    secs = r["ms"] * 1e-3
+    gaussian = dom.endswith("_gaussian")
+    alu_ops = ALU_OPS_GAUSSIAN if gaussian else ALU_OPS_PER_ELEMENT
+    cands = {"alu": (r["elements"] * alu_ops / secs / 1e12, pk["alu_ops"] / 1e12, "Tops/s")}
+    if gaussian:
+        cands["mufu"] = (r["elements"] * MUFU_OPS_GAUSSIAN / secs / 1e12,
+                         SMS_NOMINAL * MUFU_LANES_PER_SM * SM_CLOCK_MAX_HZ / 1e12, "Tops/s")
+        cands["issue"] = (r["elements"] * OPS_GAUSSIAN / secs / 1e12, pk["issue_ops"] / 1e12, "Tops/s")
+    if r["hbm_bytes"]:
+        cands["hbm"] = (r["hbm_bytes"] / secs / 1e9, pk["hbm_gbs"], "GB/s")
+    if r["flops"]:
+        cands["tensor"] = (r["flops"] / secs / 1e12, pk["bf16_tflops"], "TFLOP/s")
+    bound = max(cands, key=lambda b: cands[b][0] / cands[b][1])
+    ach, peak, unit = cands[bound]
+    return {"bound": bound, "kernel": dom, "achieved": ach, "peak": peak, "unit": unit,
+            "frac": ach / peak, "traffic": traffic_for(dom, workload),
+            "peak_source": ("derived: 152 SMs x 64 integer-ALU lanes x 2.07 GHz" if bound == "alu"
+                            else "derived: 152 SMs x 32 MUFU lanes x 2.07 GHz" if bound == "mufu"
+                            else "derived: 152 SMs x 128 issue lanes x 2.07 GHz" if bound == "issue"
+                            else pk["source"]),
+            "ops_per_element": {"alu": alu_ops, "mufu": MUFU_OPS_GAUSSIAN, "issue": OPS_GAUSSIAN}.get(bound),
+            # every operation of the element (21, or 32 for the Gaussian variant)
+            # through the issue port (152 SMs x 128 lanes x 2.07 GHz)
+            "issue_frac": r["elements"] * (OPS_GAUSSIAN if gaussian else OPS_PER_ELEMENT) / secs
+                          / pk["issue_ops"],
+            "launches": r["launches"], "avg_launch_us": 1e3 * r["ms"] / r["launches"]}
+
+
 def traffic_for(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary of this kernel on this
     workload, if the kernel's source is unchanged since the capture (else None)."""
@@ -633,35 +670,7 @@ def main(argv=None) -> int:
     value = el_step * args.steps * world / (total_ms_max * 1e-3)
 
     # --- roofline of the dominant kernel
-    pk = peaks()
-    dom = max(per_kernel, key=lambda n: per_kernel[n]["ms"])
-    r = per_kernel[dom]
-    secs = r["ms"] * 1e-3
-    gaussian = dom.endswith("_gaussian")
-    alu_ops = ALU_OPS_GAUSSIAN if gaussian else ALU_OPS_PER_ELEMENT
-    cands = {"alu": (r["elements"] * alu_ops / secs / 1e12, pk["alu_ops"] / 1e12, "Tops/s")}
-    if gaussian:
-        cands["mufu"] = (r["elements"] * MUFU_OPS_GAUSSIAN / secs / 1e12,
-                         SMS_NOMINAL * MUFU_LANES_PER_SM * SM_CLOCK_MAX_HZ / 1e12, "Tops/s")
-        cands["issue"] = (r["elements"] * OPS_GAUSSIAN / secs / 1e12, pk["issue_ops"] / 1e12, "Tops/s")
-    if r["hbm_bytes"]:
-        cands["hbm"] = (r["hbm_bytes"] / secs / 1e9, pk["hbm_gbs"], "GB/s")
-    if r["flops"]:
-        cands["tensor"] = (r["flops"] / secs / 1e12, pk["bf16_tflops"], "TFLOP/s")
-    bound = max(cands, key=lambda b: cands[b][0] / cands[b][1])
-    ach, peak, unit = cands[bound]
-    roofline = {"bound": bound, "kernel": dom, "achieved": ach, "peak": peak, "unit": unit,
-                "frac": ach / peak, "traffic": traffic_for(dom, wl.name),
-                "peak_source": ("derived: 152 SMs x 64 integer-ALU lanes x 2.07 GHz" if bound == "alu"
-                                else "derived: 152 SMs x 32 MUFU lanes x 2.07 GHz" if bound == "mufu"
-                                else "derived: 152 SMs x 128 issue lanes x 2.07 GHz" if bound == "issue"
-                                else pk["source"]),
-                "ops_per_element": {"alu": alu_ops, "mufu": MUFU_OPS_GAUSSIAN, "issue": OPS_GAUSSIAN}.get(bound),
-                # every operation of the element (21, or 32 for the Gaussian variant)
-                # through the issue port (152 SMs x 128 lanes x 2.07 GHz)
-                "issue_frac": r["elements"] * (OPS_GAUSSIAN if gaussian else OPS_PER_ELEMENT) / secs
-                              / pk["issue_ops"],
-                "launches": r["launches"], "avg_launch_us": 1e3 * r["ms"] / r["launches"]}
+    roofline = roofline_of(per_kernel, peaks(), wl.name)
     kernels = {n: {"launches": v["launches"], "share": v["ms"] / sum(x["ms"] for x in per_kernel.values()),
                    "avg_us": 1e3 * v["ms"] / v["launches"],
                    "noise_elem_per_s": v["elements"] / (v["ms"] * 1e-3)} for n, v in per_kernel.items()}

@@ -50,3 +50,47 @@ def test_bench_refuses_gaussian_on_other_workloads():
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--workload", "tiny",
                           "--noise", "gaussian"], capture_output=True, text=True, timeout=120, cwd=ROOT)
     assert out.returncode != 0 and "gaussian" in out.stderr
+
+
+PK = {"alu_ops": 152 * 64 * 2.07e9, "issue_ops": 152 * 128 * 2.07e9, "hbm_gbs": 6687.8,
+      "bf16_tflops": 1945.4, "source": "measured"}
+
+
+def _k(ms, launches, elements, flops=0.0, hbm_bytes=0.0):
+    return {"ms": ms, "launches": launches, "elements": elements, "flops": flops, "hbm_bytes": hbm_bytes}
+
+
+def test_roofline_reproduces_a_measured_bench_line():
+    """The default step's kernel-pass figures of a GB300 run (the policy forward took
+    85.2325 us per launch over 1000 launches; the others less): the dominant kernel is the
+    forward, bound by the integer ALU pipe at 12 operations per element."""
+    el = 1024 * (64 * 256 + 256 * 256 + 256 * 8)             # 85,983,232 per launch
+    per_kernel = {
+        "linear_mlp": _k(85.23251131176949, 1000, el * 1000, 2.0 * el * 1000, 632864 * 1000),
+        "grad": _k(80.3, 1000, 1024 * 84488 * 1000),
+        "noise_dump": _k(80.2, 1000, 1024 * 84488 * 1000, hbm_bytes=4 * 1024 * 84488 * 1000),
+        "es_ranks": _k(6.3, 1000, 0),
+    }
+    r = bench.roofline_of(per_kernel, PK, "no-such-workload")
+    assert r["kernel"] == "linear_mlp" and r["bound"] == "alu" and r["unit"] == "Tops/s"
+    assert abs(r["achieved"] - 12.105694976249307) < 1e-9
+    assert abs(r["frac"] - 0.6011679506861666) < 1e-12
+    assert abs(r["issue_frac"] - 0.5260219568503957) < 1e-12
+    assert r["peak"] == PK["alu_ops"] / 1e12 and r["ops_per_element"] == 12
+    assert r["traffic"] is None and r["launches"] == 1000 and abs(r["avg_launch_us"] - 85.2325113) < 1e-6
+
+
+def test_roofline_picks_the_tightest_bound():
+    n = 10 ** 9
+    # a dump whose stores outrun its hashing: HBM binds (4 B per element at 6.6 TB/s
+    # against 12 ALU operations per element at 20.1 Tops/s)
+    r = bench.roofline_of({"noise_dump": _k(1.0, 1, n, hbm_bytes=4 * n)}, PK, "x")
+    assert r["bound"] == "hbm" and abs(r["achieved"] - 4000.0) < 1e-9 and r["unit"] == "GB/s"
+    # the Gaussian kind: 32 instructions through a 128-lane issue port bind before 13 ALU
+    # operations on the 64-lane pipe or 3 MUFU operations on the 32-lane one
+    r = bench.roofline_of({"grad_gaussian": _k(1.0, 1, n)}, PK, "x")
+    assert r["bound"] == "issue" and r["ops_per_element"] == 32
+    assert abs(r["frac"] - n * 32 / 1e-3 / PK["issue_ops"]) < 1e-12
+    # a contraction with few elements and many flops: the tensor pipe binds
+    r = bench.roofline_of({"linear_tc": _k(1.0, 1, 10 ** 6, flops=1.5e12)}, PK, "x")
+    assert r["bound"] == "tensor" and abs(r["achieved"] - 1500.0) < 1e-9
