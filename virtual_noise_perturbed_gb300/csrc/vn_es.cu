@@ -99,8 +99,9 @@ cudaError_t launch_ranks(const float* fitness, int64_t pop, float* out, cudaStre
   return cudaGetLastError();
 }
 
-// Threads per i: the most that still leaves every thread at least 64 keys to scan
-// (32 for a full warp per i: at 1,024 individuals it cuts the launch from 8.1 to 6.2 µs).
+// Threads per i: the most that still leaves every thread at least 64 keys to scan,
+// except a full warp per i from 1,024 individuals on (32 keys or more per thread; at
+// 1,024 individuals it cuts the launch from 8.1 to 6.2 µs).
 cudaError_t launch_centered_ranks(const float* fitness, int64_t pop, float* out,
                                   cudaStream_t stream) {
   if (pop >= 32 * 32) return launch_ranks<32>(fitness, pop, out, stream);
