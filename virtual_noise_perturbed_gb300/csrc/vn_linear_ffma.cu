@@ -4,8 +4,8 @@
 // "virtual_perturbed_linear" and the module description:
 //   Y[i] = X[i] @ (W + sigma*N_i)^T + (b + sigma*nb_i)
 // with N_i[j,k] at offset + j*in + k and nb_i[j] at offset + out*in + j.
-// The noise is "generated on-the-fly ... and added to the weight tile in
-// registers" (module description): no noise tensor exists in memory.
+// As the module description has it, the noise is made where it is used and
+// added to the weights in registers: no noise tensor exists in memory.
 //
 // This path serves small per-individual batches with bf16 W (or bias), batches
 // of 9 to 15, populations smaller than the SM count, and every call that forces

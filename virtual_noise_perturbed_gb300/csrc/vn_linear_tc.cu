@@ -6,7 +6,7 @@
 //   Y[i] = X[i] @ (W + sigma*N_i)^T + (b + sigma*nb_i)
 // N_i[j,k] at offset + j*in + k, nb_i[j] at offset + out*in + j. The noise is
 // generated on the fly and added to the weight tile before the contraction
-// (the page's "added to the weight tile in registers"); no noise tensor exists.
+// (the module description adds it to the tile in registers); no noise tensor exists.
 //
 // Per individual the product is D = W'_i X_i^T with D[j, n] = Y_i[n, j]:
 //   A = W'_i tile, 128 output rows x 64 k (bf16, K-major), written into shared
