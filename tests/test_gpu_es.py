@@ -83,7 +83,8 @@ def test_one_es_generation_of_the_policy():
     shapes = []
     for a, c in zip(dims[:-1], dims[1:]):
         shapes += [(c, a), (c,)]
-    offs = compute_offsets(shapes)
+    offs = es.compute_offsets(shapes)
+    assert compute_offsets(shapes) == offs
     n = offs[-1] + shapes[-1][0]
     theta0 = torch.cat([t.reshape(-1) for l in w.layers for t in (l.weight, l.bias)])
     theta = theta0.to(DEV)

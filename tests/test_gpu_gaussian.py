@@ -13,7 +13,7 @@ import torch
 
 from oracle import es
 from tests.parity import TOL_FP32, assert_close, to_np
-from virtual_noise_perturbed_gb300 import (VNError, compute_offsets, noise_dump,
+from virtual_noise_perturbed_gb300 import (VNError, noise_dump,
                                            virtual_bias_gradient, virtual_flat_gradient,
                                            virtual_perturbed_mlp)
 from virtual_noise_perturbed_gb300.build import build
@@ -97,7 +97,7 @@ def _chain_case(dims, pop, batch, seed):
     shapes = []
     for a, c in zip(dims[:-1], dims[1:]):
         shapes += [(c, a), (c,)]
-    return x, ws, bs, seeds, compute_offsets(shapes)[0::2]
+    return x, ws, bs, seeds, es.compute_offsets(shapes)[0::2]
 
 
 @pytest.mark.parametrize("dims,pop,batch", [([64, 256, 256, 8], 5, 1), ([13, 37, 5], 11, 3),

@@ -35,10 +35,11 @@ def _layers(dims, seed, bias_mask=None):
 
 
 def _offsets(dims):
+    """The weight blocks' offsets by the oracle's compute_offsets over (W_0, b_0, W_1, ...)."""
     shapes = []
     for a, c in zip(dims[:-1], dims[1:]):
         shapes += [(c, a), (c,)]
-    return compute_offsets(shapes)[0::2]
+    return es.compute_offsets(shapes)[0::2]
 
 
 def _oracle_chain(x, ws, bs, seeds, sigma, offsets, act, individuals=None):
@@ -63,9 +64,11 @@ def _check(dims, pop, batch, *, shared=False, xdt=torch.float32, act="tanh", bia
     x = torch.randn((batch, dims[0]) if shared else (pop, batch, dims[0]), generator=g).to(xdt)
     seeds = torch.arange(pop, dtype=torch.int64) * 3 + 11
     offs = [o + base_offset for o in _offsets(dims)]
+    # With no base offset the library lays the blocks out itself (its own
+    # compute_offsets, offsets=None); the oracle side uses the oracle's.
     y = virtual_perturbed_mlp(x.to(DEV), [w.to(DEV) for w in ws],
                               [None if b is None else b.to(DEV) for b in bs], seeds.to(DEV), sigma,
-                              offs, activation=act)
+                              offs if base_offset else None, activation=act)
     want = _oracle_chain(x, ws, bs, seeds, sigma, offs, act)
     if shared:
         assert want.shape == (pop, batch, dims[-1])

@@ -157,7 +157,8 @@ def test_flat_gradient_covers_every_block():
     shapes = []
     for l in w.layers:
         shapes += [(l.out_f, l.in_f), (l.out_f,)]
-    offs = compute_offsets(shapes)
+    offs = es.compute_offsets(shapes)
+    assert compute_offsets(shapes) == offs
     n = offs[-1] + shapes[-1][0]
     flat = to_np(virtual_flat_gradient(w.fitness.to(DEV), w.seeds.to(DEV), n, w.sigma, w.pop, 0))
     f, s = w.fitness.numpy(), w.seeds.numpy()
