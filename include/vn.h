@@ -283,9 +283,11 @@ vn_status vn_perturbed_mlp_ex(const void* x, vn_dtype x_dt, int x_shared,
  * rank_i = number of j with fitness[j] < fitness[i], plus the number of j < i
  * with an equal value: ascending order, ties by index. The comparison is a
  * total order on the float bit patterns (-0 below +0; NaNs beyond the
- * infinities on their sign's side), so out is always a permutation of
- * {r / (pop - 1) - 0.5}. fitness and out are fp32 [pop], 4-byte aligned, and
- * must not overlap. 0 <= pop < 2^31. The work is pop^2 comparisons.
+ * infinities on their sign's side), so the ranks are a permutation of
+ * 0..pop-1 and out a permutation of {r / (pop - 1) - 0.5}. rank_i is converted
+ * to fp32 with round-to-nearest-even before the division: exact up to 2^24
+ * individuals, rounded above. fitness and out are fp32 [pop], 4-byte aligned,
+ * and must not overlap. 0 <= pop < 2^31. The work is pop^2 comparisons.
  */
 vn_status vn_centered_ranks(const float* fitness, int64_t pop, float* out, void* stream);
 
@@ -306,7 +308,7 @@ vn_status vn_device_status(void* stream);
 
 /* Test hook for the bounded-wait machinery of the tensor-core kernel; not part
  * of the method. Runs the tensor-core forward with the arguments of
- * vn_perturbed_linear (validated the same way, VN_PATH_TC) but with every
+ * vn_perturbed_linear (the same checks, with the real pop; VN_PATH_TC) but with every
  * barrier wait limited to `timeout_ms` (0 < timeout_ms <= 60000) and one
  * hashing thread of the first CTA skipping its arrive at stage
  * `withhold_stage` (>= 0), so that the MMA thread's wait on that stage can
@@ -316,7 +318,7 @@ vn_status vn_device_status(void* stream);
  * the context stays usable. y is left partly unwritten. No GPU fault, trap or
  * hang is involved. If the CTA has fewer stages than withhold_stage, nothing is
  * withheld and the call completes normally. The hook exists for bf16 W and Y
- * only (VN_ERR_DTYPE otherwise). */
+ * only (VN_ERR_DTYPE otherwise) and needs a nonempty output (VN_ERR_SHAPE). */
 vn_status vn_testhook_linear_tc_withhold(const void* x, vn_dtype x_dt, int x_shared,
                                          const void* w, vn_dtype w_dt,
                                          const void* b, vn_dtype b_dt,

@@ -187,6 +187,29 @@ def test_linear_kind_refuses_unknown_noise_kind(lib):
     assert f(P(fake), 0, 0, P(fake), 0, P(0), 0, P(fake), -1, 1, 8, 8, 0.1, 0, P(fake), 0, 0, 0, 1, P(0)) == 2
 
 
+def test_testhook_checks_like_the_tensor_core_call(lib):
+    """The bounded-wait test hook runs the same checks as vn_perturbed_linear_kind,
+    with its real population: a misaligned or overlapping output is refused before
+    any device query or launch."""
+    fake = 0x10000
+    x, w, b, s = fake + 0x1000, fake + 0x2000, fake + 0x3000, fake + 0x4000
+    hook = lib.vn_testhook_linear_tc_withhold
+
+    def call(y, pop=2, bias=b, stage=0, ms=50.0, seeds=s):
+        # bf16 x, w, b and y: (x, 1, 0, w, 1, b, 1, seeds, pop, batch 2, in 8, out 4, sigma, offset, y, 1, ...)
+        return hook(P(x), 1, 0, P(w), 1, P(bias), 1, P(seeds), pop, 2, 8, 4, 0.1, 0, P(y), 1, stage, ms, P(0))
+    assert call(fake + 0x5001) == 5          # y misaligned for bf16: VN_ERR_ALIGN
+    assert call(x + 16) == 4                 # y over x: VN_ERR_VALUE
+    assert call(w + 2) == 4                  # y over w
+    assert call(s + 8) == 4                  # y over the seeds
+    assert call(fake + 0x5000, seeds=s + 4) == 5   # seeds misaligned
+    assert call(fake + 0x5000, pop=0) == 2   # nothing to withhold an arrive in: VN_ERR_SHAPE
+    assert call(fake + 0x5000, stage=-1) == 4
+    assert call(fake + 0x5000, ms=0.0) == 4
+    assert hook(P(x), 1, 0, P(w), 0, P(b), 1, P(s), 2, 2, 8, 4, 0.1, 0, P(fake + 0x5000), 0, 0, 50.0,
+                P(0)) == 3                   # fp32 W: the hook has bf16 W and Y only
+
+
 def test_outputs_overlapping_inputs_are_refused(lib):
     """Every call refuses an output that shares bytes with one of its inputs (or
     with its other output) before anything is launched: VN_ERR_VALUE."""

@@ -82,13 +82,20 @@ def _device(*tensors: Optional[torch.Tensor]) -> torch.device:
 def virtual_perturbed_linear(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Tensor],
                              seeds: torch.Tensor, sigma: float, offset: int, *,
                              activation: Optional[str] = None, path: str = "auto",
-                             out: Optional[torch.Tensor] = None, noise: str = "uniform") -> torch.Tensor:
+                             out: Optional[torch.Tensor] = None, noise: str = "uniform",
+                             check_status: bool = False) -> torch.Tensor:
     """Y[i] = X[i] @ (W + sigma*N_i)^T + (b + sigma*nb_i), shape (pop, batch, out).
 
     x is (batch, in) (shared by every individual) or (pop, batch, in). The
     result dtype is torch.result_type(x, weight). ``activation="tanh"`` applies
     tanh to Y in the kernel's epilogue; ``path`` forces "ffma" or "tc"; ``noise="gaussian"``
-    perturbs with the Box-Muller variant (``vn_perturbed_linear_kind``)."""
+    perturbs with the Box-Muller variant (``vn_perturbed_linear_kind``).
+
+    The launch is asynchronous. On the tensor-core path every on-chip barrier wait
+    is bounded (4 s); a wait that runs out stops the kernel with part of Y unwritten
+    and records VN_ERR_TIMEOUT on the device, which only ``device_status()`` reports.
+    So Y from that path is valid once ``device_status()`` has returned without
+    raising; ``check_status=True`` makes that call here (it synchronises the stream)."""
     lib = load()
     x = _cuda(x, "x")
     weight = _cuda(weight, "weight")
@@ -126,7 +133,9 @@ def virtual_perturbed_linear(x: torch.Tensor, weight: torch.Tensor, bias: Option
             _ptr(bias), _dt(bias, "bias") if bias is not None else 0,
             _ptr(seeds), pop, batch, in_f, out_f, float(sigma), int(offset) & _M64,
             _ptr(out), _DT[ydt], _PATHS[path], _ACTS[activation], _NOISE[noise], _stream(x))
-    check(st, "vn_perturbed_linear")
+        check(st, "vn_perturbed_linear")
+        if check_status:
+            device_status(x.device)
     return out
 
 
@@ -385,7 +394,9 @@ def perturbed_linear_path(x: torch.Tensor, weight: torch.Tensor) -> str:
 
 
 def device_status(device=None) -> None:
-    """Synchronise the current stream and raise VNError if a kernel recorded an expired wait."""
+    """Synchronise the current stream and raise VNError if a kernel recorded an expired wait
+    since the last call (the status word is then cleared). Results written by the
+    tensor-core forward since the last call are valid only if this returns normally."""
     lib = load()
     s = torch.cuda.current_stream(device)
     check(lib.vn_device_status(ctypes.c_void_p(s.cuda_stream)), "vn_device_status")

@@ -77,6 +77,51 @@ bool device_is_cc10(const vn::DeviceInfo& d) { return d.cc_major == 10; }
 // below it the MMA's N of 16 would be mostly padding.
 constexpr int64_t kAutoTcMinBatch = 16;
 
+// The checks of a perturbed linear call (vn_perturbed_linear_kind and the test
+// hook share them): dtypes, enums, sizes, sigma, size products, nulls,
+// alignment and overlaps, in that order. On VN_OK, *empty tells whether the
+// output has no elements (nothing to launch) and *a holds the arguments.
+vn_status check_linear(const void* x, vn_dtype x_dt, int x_shared, const void* w, vn_dtype w_dt,
+                       const void* b, vn_dtype b_dt, const int64_t* seeds, int64_t pop,
+                       int64_t batch, int64_t in, int64_t out, double sigma, uint64_t offset,
+                       void* y, vn_dtype y_dt, vn_act act, vn_noise kind, vn::LinearArgs* a,
+                       bool* empty) {
+  if (kind != VN_NOISE_UNIFORM && kind != VN_NOISE_GAUSSIAN) return VN_ERR_VALUE;
+  if (!dtype_ok(x_dt) || !dtype_ok(w_dt) || (b != nullptr && !dtype_ok(b_dt)) || !dtype_ok(y_dt))
+    return VN_ERR_DTYPE;
+  const vn_dtype want_y = (x_dt == VN_BF16 && w_dt == VN_BF16) ? VN_BF16 : VN_F32;
+  if (y_dt != want_y) return VN_ERR_DTYPE;
+  if (act != VN_ACT_NONE && act != VN_ACT_TANH) return VN_ERR_VALUE;
+  if (pop < 0 || batch < 0 || in < 0 || out < 0) return VN_ERR_SHAPE;
+  float sig;
+  if (!float_sigma(sigma, &sig)) return VN_ERR_VALUE;
+  int64_t x_elems, y_elems, w_elems, t;
+  if (!mul(batch, in, &x_elems) || (!x_shared && !mul(x_elems, pop, &x_elems)) ||
+      !mul(pop, batch, &t) || !mul(t, out, &y_elems) || !mul(out, in, &w_elems))
+    return VN_ERR_OVERFLOW;
+  *empty = y_elems == 0;
+  if (*empty) return VN_OK;
+  if (seeds == nullptr || y == nullptr || (x_elems > 0 && x == nullptr) ||
+      (w_elems > 0 && w == nullptr))
+    return VN_ERR_NULL;
+  if (!aligned(seeds, 8) || !aligned(y, dtype_size(y_dt)) || !aligned(x, dtype_size(x_dt)) ||
+      !aligned(w, dtype_size(w_dt)) || (b != nullptr && !aligned(b, dtype_size(b_dt))))
+    return VN_ERR_ALIGN;
+  int64_t yb, xb, wb, bb, sb;
+  if (!mul(y_elems, dtype_size(y_dt), &yb) || !mul(x_elems, dtype_size(x_dt), &xb) ||
+      !mul(w_elems, dtype_size(w_dt), &wb) || !mul(out, dtype_size(b_dt), &bb) ||
+      !mul(pop, 8, &sb))
+    return VN_ERR_OVERFLOW;
+  if (overlap(y, yb, x, xb) || overlap(y, yb, w, wb) || overlap(y, yb, b, bb) ||
+      overlap(y, yb, seeds, sb))
+    return VN_ERR_VALUE;
+  a->x = x; a->x_dt = x_dt; a->x_shared = x_shared ? 1 : 0;
+  a->w = w; a->w_dt = w_dt; a->b = b; a->b_dt = b_dt;
+  a->seeds = seeds; a->pop = pop; a->batch = batch; a->in = in; a->out = out;
+  a->sigma = sig; a->offset = offset; a->y = y; a->y_dt = y_dt; a->act = act; a->kind = kind;
+  return VN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -230,43 +275,12 @@ vn_status vn_perturbed_linear_kind(const void* x, vn_dtype x_dt, int x_shared, c
                                    int64_t out, double sigma, uint64_t offset, void* y,
                                    vn_dtype y_dt, vn_path path, vn_act act, vn_noise kind,
                                    void* stream) {
-  if (kind != VN_NOISE_UNIFORM && kind != VN_NOISE_GAUSSIAN) return VN_ERR_VALUE;
-  if (!dtype_ok(x_dt) || !dtype_ok(w_dt) || (b != nullptr && !dtype_ok(b_dt)) || !dtype_ok(y_dt))
-    return VN_ERR_DTYPE;
-  const vn_dtype want_y = (x_dt == VN_BF16 && w_dt == VN_BF16) ? VN_BF16 : VN_F32;
-  if (y_dt != want_y) return VN_ERR_DTYPE;
   if (path != VN_PATH_AUTO && path != VN_PATH_FFMA && path != VN_PATH_TC) return VN_ERR_PATH;
-  if (act != VN_ACT_NONE && act != VN_ACT_TANH) return VN_ERR_VALUE;
-  if (pop < 0 || batch < 0 || in < 0 || out < 0) return VN_ERR_SHAPE;
-  float sig;
-  if (!float_sigma(sigma, &sig)) return VN_ERR_VALUE;
-  int64_t x_elems, y_elems, w_elems, t;
-  if (!mul(batch, in, &x_elems) || (!x_shared && !mul(x_elems, pop, &x_elems)) ||
-      !mul(pop, batch, &t) || !mul(t, out, &y_elems) || !mul(out, in, &w_elems))
-    return VN_ERR_OVERFLOW;
-  if (y_elems == 0) return VN_OK;
-  if (seeds == nullptr || y == nullptr || (x_elems > 0 && x == nullptr) ||
-      (w_elems > 0 && w == nullptr))
-    return VN_ERR_NULL;
-  if (!aligned(seeds, 8) || !aligned(y, dtype_size(y_dt)) || !aligned(x, dtype_size(x_dt)) ||
-      !aligned(w, dtype_size(w_dt)) || (b != nullptr && !aligned(b, dtype_size(b_dt))))
-    return VN_ERR_ALIGN;
-  {
-    int64_t yb, xb, wb, bb, sb;
-    if (!mul(y_elems, dtype_size(y_dt), &yb) || !mul(x_elems, dtype_size(x_dt), &xb) ||
-        !mul(w_elems, dtype_size(w_dt), &wb) || !mul(out, dtype_size(b_dt), &bb) ||
-        !mul(pop, 8, &sb))
-      return VN_ERR_OVERFLOW;
-    if (overlap(y, yb, x, xb) || overlap(y, yb, w, wb) || overlap(y, yb, b, bb) ||
-        overlap(y, yb, seeds, sb))
-      return VN_ERR_VALUE;
-  }
-
   vn::LinearArgs a;
-  a.x = x; a.x_dt = x_dt; a.x_shared = x_shared ? 1 : 0;
-  a.w = w; a.w_dt = w_dt; a.b = b; a.b_dt = b_dt;
-  a.seeds = seeds; a.pop = pop; a.batch = batch; a.in = in; a.out = out;
-  a.sigma = sig; a.offset = offset; a.y = y; a.y_dt = y_dt; a.act = act; a.kind = kind;
+  bool empty = false;
+  const vn_status st = check_linear(x, x_dt, x_shared, w, w_dt, b, b_dt, seeds, pop, batch, in,
+                                    out, sigma, offset, y, y_dt, act, kind, &a, &empty);
+  if (st != VN_OK || empty) return st;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   const bool gaussian = kind == VN_NOISE_GAUSSIAN;
 
@@ -300,7 +314,7 @@ vn_status vn_perturbed_linear_kind(const void* x, vn_dtype x_dt, int x_shared, c
       m.x = x; m.x_dt = x_dt; m.x_shared = x_shared ? 1 : 0;
       m.n_layers = 1;
       m.dims = dims; m.w = wl; m.b = bl; m.offsets = offs;
-      m.seeds = seeds; m.pop = pop; m.batch = batch; m.sigma = sig; m.act = VN_ACT_NONE;
+      m.seeds = seeds; m.pop = pop; m.batch = batch; m.sigma = a.sigma; m.act = VN_ACT_NONE;
       m.y = static_cast<float*>(y);
       m.act_last = act;
       m.kind = kind;
@@ -328,26 +342,20 @@ vn_status vn_testhook_linear_tc_withhold(const void* x, vn_dtype x_dt, int x_sha
                                          double timeout_ms, void* stream) {
   if (!(timeout_ms > 0.0) || !(timeout_ms <= 60000.0) || withhold_stage < 0) return VN_ERR_VALUE;
   if (w_dt != VN_BF16 || y_dt != VN_BF16) return VN_ERR_DTYPE;  // the hook's one instance
-  // Validate exactly as a forced tensor-core call would (this launches nothing:
-  // pop = 0 makes the output empty).
-  vn_status st = vn_perturbed_linear_ex(x, x_dt, x_shared, w, w_dt, b, b_dt, seeds, 0, batch, in,
-                                        out, sigma, offset, y, y_dt, VN_PATH_TC, VN_ACT_NONE,
-                                        stream);
+  // The same checks as a forced tensor-core call, with the real population.
+  vn::LinearArgs a;
+  bool empty = false;
+  const vn_status st = check_linear(x, x_dt, x_shared, w, w_dt, b, b_dt, seeds, pop, batch, in,
+                                    out, sigma, offset, y, y_dt, VN_ACT_NONE, VN_NOISE_UNIFORM,
+                                    &a, &empty);
   if (st != VN_OK) return st;
-  if (pop < 1 || batch < 1 || out < 1) return VN_ERR_SHAPE;
-  if (seeds == nullptr || y == nullptr || x == nullptr || w == nullptr) return VN_ERR_NULL;
+  if (empty) return VN_ERR_SHAPE;  // the hook needs a kernel to withhold an arrive in
   vn::DeviceInfo dev;
   cudaError_t err = vn::device_info(&dev);
   if (err != cudaSuccess) return cuda_failure(err);
   if (!device_is_cc10(dev)) return VN_ERR_DEVICE;
   if (!vn::linear_tc_applies(x, x_dt, w, w_dt, batch, in, out) || pop > (int64_t{1} << 31) - 1)
     return VN_ERR_PATH;
-  vn::LinearArgs a;
-  a.x = x; a.x_dt = x_dt; a.x_shared = x_shared ? 1 : 0;
-  a.w = w; a.w_dt = w_dt; a.b = b; a.b_dt = b_dt;
-  a.seeds = seeds; a.pop = pop; a.batch = batch; a.in = in; a.out = out;
-  a.sigma = static_cast<float>(sigma); a.offset = offset; a.y = y; a.y_dt = y_dt;
-  a.act = VN_ACT_NONE;
   return launched(vn::launch_linear_tc_hook(a, static_cast<cudaStream_t>(stream), withhold_stage,
                                             static_cast<unsigned long long>(timeout_ms * 1e6)));
 }

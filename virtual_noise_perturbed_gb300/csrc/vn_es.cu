@@ -6,8 +6,10 @@
 // rank_i the position of fitness[i] in ascending order, equal values ordered by
 // index. The order is a total order on float bit patterns (negative values
 // below positive ones, -0 below +0, NaNs at the ends by sign), so every input
-// gives a permutation of 0..pop-1. rank_i is an exact integer; the division and
-// the subtraction are single fp32 operations, so the result is fully determined.
+// gives a permutation of 0..pop-1. rank_i is counted exactly as an integer and
+// converted to fp32 by round-to-nearest-even (exact up to 2^24 individuals, rounded
+// above); the conversion, the division and the subtraction are single fp32
+// operations, so the result is fully determined.
 //
 // Update: theta[k] += lr * grad[k] (one fp32 fma per element), the ascent step
 // on the estimate of the page's module description.
@@ -43,7 +45,8 @@ centered_ranks_kernel(const float* __restrict__ fitness, int pop, float* __restr
   __shared__ uint32_t s_key[kRankTile];
   constexpr int kPerCta = kRankThreads / kTpi;
   const int sub = threadIdx.x % kTpi;
-  const int i = blockIdx.x * kPerCta + threadIdx.x / kTpi;
+  // 64-bit: the last CTA's first index may pass 2^31 - 1 when pop is close to it.
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * kPerCta + threadIdx.x / kTpi;
   const uint32_t ki = i < pop ? order_key(fitness[i]) : 0u;
   uint32_t rank = 0;
   for (int j0 = 0; j0 < pop; j0 += kRankTile) {
@@ -52,7 +55,7 @@ centered_ranks_kernel(const float* __restrict__ fitness, int pop, float* __restr
     for (int t = threadIdx.x; t < jn; t += kRankThreads) s_key[t] = order_key(fitness[j0 + t]);
     __syncthreads();
     // Keys below ki, and equal keys at a lower index (j < i <=> t < i - j0).
-    const int before = i - j0;
+    const int64_t before = i - j0;
 #pragma unroll 8
     for (int t = sub; t < jn; t += kTpi) {
       const uint32_t kj = s_key[t];

@@ -28,6 +28,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "vn_hash.cuh"
 #include "vn_internal.h"
@@ -137,11 +138,17 @@ grad_kernel(const float* __restrict__ fitness, const int64_t* __restrict__ seeds
   }
 }
 
-int occupancy(const void* fn) {
+// Resident CTAs of `fn` per SM on device `dev`, queried once per (kernel,
+// device) and kept in `cache` (0 = not yet queried): devices of different
+// models in one process get their own figure.
+int occupancy(const void* fn, int dev, std::atomic<int> (&cache)[kMaxDevices]) {
+  const int known = cache[dev].load(std::memory_order_relaxed);
+  if (known > 0) return known;
   int blocks = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, fn, kThreads, 0) != cudaSuccess ||
       blocks < 1)
     blocks = 1;
+  cache[dev].store(blocks, std::memory_order_relaxed);
   return blocks;
 }
 
@@ -153,8 +160,9 @@ cudaError_t launch_grad_kind(const float* fitness, const int64_t* seeds, int64_t
   cudaError_t err = device_info(&dev);
   if (err != cudaSuccess) return err;
   const int64_t tiles = (m + kTile - 1) / kTile;
-  static const int occ =
-      occupancy(reinterpret_cast<const void*>(&grad_kernel<false, kKind, kUpdate>));
+  static std::atomic<int> occ_cache[kMaxDevices];
+  const int occ = occupancy(reinterpret_cast<const void*>(&grad_kernel<false, kKind, kUpdate>),
+                            dev.device, occ_cache);
   const int64_t resident = static_cast<int64_t>(dev.sm_count) * occ;
 
   // Split the population across a cluster while the tiles alone leave the GPU
