@@ -1,25 +1,29 @@
 #!/usr/bin/env python
 """Benchmark of the virtual-noise ES step on one node.
 
-Default workload: the ES MLP policy step (pop 1024, batch 1, 64 -> 256 -> 256 -> 8
-with tanh, fp32, sigma 0.02, centered-rank fitness). One step is one pass of the
-whole hot path over one population:
-  * forward: the three perturbed linears in one launch (vn_perturbed_mlp: the
-    activations stay on chip, tanh between layers),
-  * fitness shaping: the centered ranks of the population's returns,
-  * gradients: grad_W and grad_b of all three layers; the six blocks are laid
-    out by compute_offsets one after another, so they are one flat range of
-    element indices and one reduction over the population computes them all,
-  * update: the flat parameter vector (the layers are views of it) += lr * grad,
-    applied by the gradient launch as it stores each element (vn_gradient_update),
-  * noise dump: the centered-uniform noise of the whole flat parameter vector
-    (84,488 elements) for every individual,
-so each step regenerates the population's parameter noise three times.
-`--noise gaussian` runs the same step (or the step of another workload but the
-tiny one) with the Box-Muller variant of the noise throughout.
+Default workload (the headline): the large tensor-core forward, pop 256 x batch 256,
+4096 -> 4096, X / W / Y bf16, sigma 0.01 -- one launch of the fused perturbed
+linear (tcgen05 + TMEM) per step, 4.3e9 noise elements regenerated per step.
+The same JSON line carries, under "configs", the other workloads measured the same
+way with their own roofline objects:
+  * mid:       pop 4096, batch 32, 1024 -> 1024 (X bf16, W fp32): the tensor-core
+               forward plus grad_W and grad_b,
+  * grad_only: grad_W and grad_b of a 4096 x 4096 block over pop 16384, fitness the
+               centered ranks of the returns (the ranks computed on the device),
+  * es_mlp:    one ES generation of the MLP policy (pop 1024, batch 1, 64 -> 256 ->
+               256 -> 8 with tanh, fp32): the three layers in one launch, centered
+               ranks, the flat gradient of all six blocks with the parameter step
+               fused, and the noise dump of the whole parameter vector; its e2e is
+               reported with and without the dump,
+  * tiny:      pop 8, batch 4, 32 -> 16, fp32: forward, gradients and dump,
+and "alu_peak_measured": the hash-only kernel (vn_hash_probe), whose element rate is
+the measured ceiling of the integer ALU pipe beside the derived one.
+`--workload NAME` makes another workload the headline (then no extras unless
+`--extras` names them); `--noise gaussian` runs the Box-Muller variant of the noise
+throughout.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl vn|reference]
-                       [--workload es_mlp|tiny|mid|grad_only|large_tc]
+                       [--workload large_tc|mid|grad_only|es_mlp|tiny] [--extras auto|none|a,b]
 For N > 1 launch with torch.distributed.run: every rank runs its own population
 (seeds offset by rank * pop), no data-path collective (weak scaling).
 
@@ -33,6 +37,11 @@ the events) so that every step starts with a cold L2:
     launch bracketed by its own pair of events -> per-kernel durations, shares
     and the dominant kernel's roofline. (An event pair around each launch adds
     its own gap between launches, so it is kept out of the step pass.)
+The headline times exactly K steps; an extra workload times min(K, the steps that
+fit --extra-seconds, at least 3) and says how many in its entry.
+The oracle legs (cpu_baseline, --impl reference) run the oracle as it stands on
+the host's cores: each individual's pass is independent, so the sampled
+individuals are split over one spawned process per core.
 Rank 0 prints one JSON line.
 """
 
@@ -129,9 +138,10 @@ def contiguous_blocks(wl) -> bool:
     return True
 
 
-def build_step(wl, dev, stream_ptr, noise="uniform"):
+def build_step(wl, dev, stream_ptr, noise="uniform", include_dump=True):
     """Device buffers and the launches of one step of workload ``wl`` (on ``dev``);
-    ``noise="gaussian"`` runs the gradient-only workload with the Box-Muller variant."""
+    ``noise="gaussian"`` runs the step with the Box-Muller variant of the noise;
+    ``include_dump=False`` leaves the noise dump of the tiny and policy workloads out."""
     import torch
     from virtual_noise_perturbed_gb300 import _lib
 
@@ -269,7 +279,7 @@ def build_step(wl, dev, stream_ptr, noise="uniform"):
                                pop * l.out_f, hbm_bytes=gb.numel() * 4))
         outputs += [gw, gb]
 
-    if wl.number in (1, 2):
+    if wl.number in (1, 2) and include_dump:
         dump = torch.empty((pop, n_params), dtype=torch.float32, device=dev)
         launches.append(Launch("noise_dump" + suffix, lib.vn_noise_dump_ex,
                                (P(d.seeds.data_ptr()), pop, n_params, wl.layers[0].offset,
@@ -421,74 +431,155 @@ def traffic_for(kernel: str, workload: str):
 
 
 # ---------------------------------------------------------------------------
-# The oracle leg (cpu_baseline and --impl reference)
+# The oracle leg (cpu_baseline and --impl reference): the oracle as it stands.
+# Each individual's pass is independent of the others', so a sample of
+# individuals is split over one spawned process per host core (spawned, not
+# forked: the parent has used CUDA). Only the split is parallel; every worker runs
+# the oracle's own functions, unchanged, on its individuals.
 # ---------------------------------------------------------------------------
 
-def oracle_step(wl, individuals: int, noise: str = "uniform") -> int:
-    """The oracle's pass over the first ``individuals`` of the population: forward,
-    the centered ranks of the returns (over the whole population: a rank is global),
-    the gradients' sums over those individuals, the parameter update and their noise
-    dump. Returns the noise elements regenerated."""
+def oracle_cores() -> int:
+    """The host cores this process may run on."""
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:  # pragma: no cover -- not Linux
+        return max(1, os.cpu_count() or 1)
+
+
+_ORACLE_STATIC = None
+
+
+def _oracle_init(static):
+    """Worker start-up: keep the workload's shared arrays and import the oracle once."""
+    global _ORACLE_STATIC
+    _ORACLE_STATIC = static
+    import oracle.es  # noqa: F401
+
+
+def _oracle_ready(_):
+    return os.getpid()
+
+
+def _oracle_job(job) -> int:
+    """One worker's share of an oracle pass: forward, gradient sums, parameter update
+    and noise dump over the individuals whose X rows, seeds and fitness ``job``
+    carries. Returns the noise elements regenerated."""
     import numpy as np
     from oracle import es
 
-    s = slice(0, individuals)
-    seeds = wl.seeds[s].numpy()
-    if wl.grads and wl.returns is not None:
-        fit = es.centered_ranks(wl.returns.numpy())[s]
-    else:
-        fit = wl.fitness[s].numpy()
+    st = _ORACLE_STATIC
+    x, seeds, fit = job
+    k = int(seeds.shape[0])
+    if k == 0:
+        return 0
+    noise, sigma, layers = st["noise"], st["sigma"], st["layers"]
     n = 0
-    if wl.forward:
-        h = wl.x[s].float().numpy().astype(np.float64)
-        for li, l in enumerate(wl.layers):
-            h = es.perturbed_linear(h, l.weight.float().numpy(), l.bias.float().numpy(), seeds, wl.sigma,
-                                    l.offset, noise=noise)
-            if wl.activation == "tanh" and li < len(wl.layers) - 1:
+    if st["forward"]:
+        h = x.astype(np.float64)
+        for li, (w, b, off, in_f, out_f) in enumerate(layers):
+            h = es.perturbed_linear(h, w, b, seeds, sigma, off, noise=noise)
+            if st["activation"] == "tanh" and li < len(layers) - 1:
                 h = np.tanh(h)
-            n += individuals * l.out_f * l.in_f
-    for l in (wl.layers if wl.grads else []):
-        if noise == "gaussian":
-            es.gaussian_flat_gradient(fit, seeds, l.out_f * l.in_f, wl.sigma, individuals, l.offset)
-            es.gaussian_flat_gradient(fit, seeds, l.out_f, wl.sigma, individuals, l.offset + l.out_f * l.in_f)
-            n += individuals * (l.out_f * l.in_f + l.out_f)
-            continue
-        gw = es.weight_gradient(fit, seeds, (l.out_f, l.in_f), wl.sigma, individuals, l.offset)
-        gb = es.bias_gradient(fit, seeds, (l.out_f,), wl.sigma, individuals, l.offset + l.out_f * l.in_f)
-        if wl.forward and len(wl.layers) > 1:
-            es.es_update(l.weight.float().numpy(), gw, ES_LR)
-            es.es_update(l.bias.float().numpy(), gb, ES_LR)
-        n += individuals * (l.out_f * l.in_f + l.out_f)
-    if wl.number in (1, 2):
-        n_params = sum(l.out_f * l.in_f + l.out_f for l in wl.layers)
-        (es.gaussian_dump if noise == "gaussian" else es.noise_dump)(seeds, n_params, wl.layers[0].offset)
-        n += individuals * n_params
+            n += k * out_f * in_f
+    if st["grads"]:
+        for (w, b, off, in_f, out_f) in layers:
+            if noise == "gaussian":
+                es.gaussian_flat_gradient(fit, seeds, out_f * in_f, sigma, k, off)
+                es.gaussian_flat_gradient(fit, seeds, out_f, sigma, k, off + out_f * in_f)
+            else:
+                gw = es.weight_gradient(fit, seeds, (out_f, in_f), sigma, k, off)
+                gb = es.bias_gradient(fit, seeds, (out_f,), sigma, k, off + out_f * in_f)
+                if st["update"]:
+                    es.es_update(w, gw, ES_LR)
+                    es.es_update(b, gb, ES_LR)
+            n += k * (out_f * in_f + out_f)
+    if st["dump_n"]:
+        (es.gaussian_dump if noise == "gaussian" else es.noise_dump)(seeds, st["dump_n"], st["dump_offset"])
+        n += k * st["dump_n"]
     return n
 
 
-def cpu_cores_used() -> int:
-    # numpy element-wise work is single-threaded and the BLAS pools are pinned to
-    # one thread at the top of this file.
-    return 1
+class OraclePool:
+    """The oracle's pass over sampled individuals of ``wl``, on ``cores`` spawned workers."""
+
+    def __init__(self, wl, noise: str = "uniform", cores: int = None):
+        import multiprocessing as mp
+
+        self.wl, self.noise = wl, noise
+        self.cores = cores or oracle_cores()
+        n_params = sum(l.out_f * l.in_f + l.out_f for l in wl.layers)
+        static = {
+            "noise": noise, "sigma": wl.sigma, "activation": wl.activation,
+            "forward": wl.forward, "grads": wl.grads,
+            "update": wl.forward and wl.grads and len(wl.layers) > 1,
+            "dump_n": n_params if wl.number in (1, 2) else 0,
+            "dump_offset": wl.layers[0].offset,
+            "layers": [(l.weight.float().numpy(), None if l.bias is None else l.bias.float().numpy(),
+                        l.offset, l.in_f, l.out_f) for l in wl.layers],
+        }
+        self.x = wl.x.float().numpy() if wl.forward else None
+        self.seeds = wl.seeds.numpy()
+        ctx = mp.get_context("spawn")
+        self.pool = ctx.Pool(self.cores, initializer=_oracle_init, initargs=(static,))
+        self.pool.map(_oracle_ready, range(self.cores), chunksize=1)  # every worker up and importing
+
+    def run(self, individuals: int):
+        """One pass over the first ``individuals`` individuals: the fitness (the centered
+        ranks of the whole population's returns, where the workload shapes them; a
+        rank is global), then the individuals split evenly over the workers.
+        Returns (noise elements, seconds)."""
+        import numpy as np
+        from oracle import es
+
+        t0 = time.monotonic()
+        wl = self.wl
+        if wl.grads and wl.returns is not None:
+            fit = es.centered_ranks(wl.returns.numpy())
+        else:
+            fit = wl.fitness.numpy()
+        parts = [p for p in np.array_split(np.arange(individuals), self.cores) if p.size]
+        jobs = [(None if self.x is None else self.x[p], self.seeds[p], fit[p]) for p in parts]
+        n = sum(self.pool.map(_oracle_job, jobs, chunksize=1))
+        return n, time.monotonic() - t0
+
+    def calibrate(self, budget_s: float) -> int:
+        """Individuals of one pass that take about ``budget_s`` (one per core first)."""
+        one = min(self.wl.pop, self.cores)
+        _, t = self.run(one)
+        per_round = max(t, 1e-3)
+        rounds = max(1, int(budget_s / per_round))
+        return int(min(self.wl.pop, one * rounds))
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
 
 
-def time_oracle(wl, budget_s: float, steps: int = 1, noise: str = "uniform"):
-    """Run ``steps`` oracle passes, each on as many individuals as fit ``budget_s``."""
-    t = time.perf_counter()
-    oracle_step(wl, 1, noise)
-    per_ind = max(time.perf_counter() - t, 1e-4)
-    inds = int(max(1, min(wl.pop, budget_s / per_ind)))
-    total_el, total_t = 0, 0.0
-    for _ in range(steps):
-        t = time.perf_counter()
-        total_el += oracle_step(wl, inds, noise)
-        total_t += time.perf_counter() - t
-    return total_el / total_t, inds, total_t
+def sample_text(wl, inds: int, cores: int) -> str:
+    parts = ["forward"] if wl.forward else []
+    if wl.grads:
+        parts.append("gradient sums")
+    if wl.number in (1, 2):
+        parts.append("noise dump")
+    return (f"the oracle's pass ({', '.join(parts)}) over the first {inds} of {wl.pop} individuals, "
+            f"split over {cores} spawned processes (one per host core)")
+
+
+def time_oracle(wl, budget_s: float, noise: str = "uniform"):
+    """The cpu_baseline: one oracle pass on all host cores over as many individuals as
+    fit about ``budget_s``. Returns (elements/s, individuals, seconds, cores)."""
+    pool = OraclePool(wl, noise)
+    try:
+        inds = pool.calibrate(budget_s)
+        n, t = pool.run(inds)
+    finally:
+        pool.close()
+    return n / t, inds, t, pool.cores
 
 
 # ---------------------------------------------------------------------------
 
-def step_elements(wl) -> int:
+def step_elements(wl, include_dump: bool = True) -> int:
     """Noise elements one step of ``wl`` regenerates (forward, gradients, dump), as
     ``build_step`` counts them: pop x weights for the forward, pop x parameters for
     the gradients and for the dump of the ES workloads."""
@@ -496,7 +587,7 @@ def step_elements(wl) -> int:
     el = wl.pop * sum(l.out_f * l.in_f for l in wl.layers) if wl.forward else 0
     if wl.grads:
         el += wl.pop * n_params
-    if wl.number in (1, 2):
+    if wl.number in (1, 2) and include_dump:
         el += wl.pop * n_params
     return el
 
@@ -517,45 +608,226 @@ def config_for(wl, world, noise="uniform"):
 
 
 def run_reference(args, wl, world, rank):
+    """The oracle alone, as it stands, on the host's cores: W warm-up passes, then K
+    timed passes, each over a bounded sample of the workload's individuals."""
     if rank != 0:
         return 0
-    from virtual_noise_perturbed_gb300 import workloads  # noqa: F401
-    budget = min(2.0, 150.0 / max(1, args.steps + args.warmup))
-    for _ in range(args.warmup):
-        time_oracle(wl, budget / 4, noise=args.noise)
-    rate, inds, total_t = time_oracle(wl, budget, steps=args.steps, noise=args.noise)
+    budget = min(4.0, 100.0 / max(1, args.steps))
+    pool = OraclePool(wl, args.noise)
+    try:
+        one = min(wl.pop, pool.cores)
+        for _ in range(args.warmup):
+            _, t_one = pool.run(one)
+        inds = int(min(wl.pop, one * max(1, int(budget / max(t_one, 1e-3)))))
+        total_el, total_t = 0, 0.0
+        for _ in range(args.steps):
+            n, t = pool.run(inds)
+            total_el += n
+            total_t += t
+    finally:
+        pool.close()
+    rate = total_el / total_t
     cfg = config_for(wl, 1, args.noise)
     line = {"metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
             "impl": "reference",
-            "cpu_baseline": {"value": rate, "unit": UNIT, "cores": cpu_cores_used(), "kind": "oracle",
-                             "sample": f"each step: the oracle's pass over the first {inds} of {wl.pop} "
-                                       f"individuals (forward, gradient sums, noise dump)"},
+            "cpu_baseline": {"value": rate, "unit": UNIT, "cores": pool.cores, "kind": "oracle",
+                             "sample": "each step: " + sample_text(wl, inds, pool.cores)},
             "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
 
 
+# ---------------------------------------------------------------------------
+# GPU measurement of one workload
+# ---------------------------------------------------------------------------
+
+def measure(wl, dev, stream, flush, args, world, noise, steps=None, include_dump=True):
+    """Warm-up, the step pass and the kernel pass of one workload on this rank.
+
+    ``steps`` None: exactly --steps steps (the headline); else at most that many,
+    as many as fit --extra-seconds by the last warm-up step's time (at least 3)."""
+    import torch
+
+    launches, bufs, outputs = build_step(wl, dev, stream.cuda_stream, noise, include_dump)
+    res = {"n_launches": len(launches), "el_step": sum(l.elements for l in launches)}
+    with torch.cuda.stream(stream):
+        wa, wb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for w in range(args.warmup):
+            if w == args.warmup - 1:
+                wa.record(stream)
+            for l in launches:
+                l()
+            if w == args.warmup - 1:
+                wb.record(stream)
+            flush.zero_()
+        torch.cuda.synchronize(dev)
+        est_ms = max(wa.elapsed_time(wb), 1e-3)
+        if steps is None:
+            k_steps = args.steps
+            k_kern = args.kernel_steps if args.kernel_steps is not None else args.steps
+        else:
+            k_steps = k_kern = int(min(args.steps, max(3, args.extra_seconds * 1e3 / est_ms)))
+        # The step pass replays the step's C-ABI calls captured once as a CUDA graph
+        # (the same kernels and arguments; the graph only removes the host launch
+        # latency between them). If capture is refused, the calls are made directly.
+        graph, graph_error = None, None
+        if not args.no_graph:
+            try:
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph, stream=stream):
+                    for l in launches:
+                        l()
+                graph.replay()
+                torch.cuda.synchronize(dev)
+            except Exception as exc:  # noqa: BLE001 -- reported in the JSON line
+                graph = None
+                graph_error = f"{type(exc).__name__}: {exc}"[:200]
+                torch.cuda.synchronize(dev)
+        ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(k_steps)]
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(launches))]
+              for _ in range(k_kern)]
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        wall0 = time.perf_counter()
+        for k in range(k_steps):
+            ev_step[k][0].record(stream)
+            if graph is not None:
+                graph.replay()
+            else:
+                for l in launches:
+                    l()
+            ev_step[k][1].record(stream)
+            flush.zero_()
+        torch.cuda.synchronize(dev)
+        res["wall_s"] = time.perf_counter() - wall0
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        for k in range(k_kern):
+            for j, l in enumerate(launches):
+                ev[k][2 * j].record(stream)
+                l()
+                ev[k][2 * j + 1].record(stream)
+            flush.zero_()
+        torch.cuda.synchronize(dev)
+        barrier(world)
+    per_kernel = {}
+    for k in range(k_kern):
+        for j, l in enumerate(launches):
+            ms = ev[k][2 * j].elapsed_time(ev[k][2 * j + 1])
+            rec = per_kernel.setdefault(l.kernel, {"ms": 0.0, "launches": 0, "elements": 0, "flops": 0.0,
+                                                   "hbm_bytes": 0.0, "grad_w_elems": 0})
+            rec["ms"] += ms
+            rec["launches"] += 1
+            rec["elements"] += l.elements
+            rec["flops"] += l.flops
+            rec["hbm_bytes"] += l.hbm_bytes
+            rec["grad_w_elems"] += l.grad_w_elems
+    total_ms = sum(a.elapsed_time(b) for a, b in ev_step)
+    res.update({"steps": k_steps, "kernel_steps": k_kern, "total_ms_max": max_over_ranks(total_ms, world, dev),
+                "per_kernel": per_kernel, "graph": graph is not None, "graph_error": graph_error,
+                "gpu_launches": len(launches) * (k_steps + k_kern)})
+    return res
+
+
+def summarise(wl, res, world, pk):
+    """value, ms per step, the dominant kernel's roofline, per-kernel shares and the
+    phase metrics of one measured workload."""
+    per_kernel = res["per_kernel"]
+    value = res["el_step"] * res["steps"] * world / (res["total_ms_max"] * 1e-3)
+    all_ms = sum(x["ms"] for x in per_kernel.values())
+    kernels = {n: {"launches": v["launches"], "share": v["ms"] / all_ms, "avg_us": 1e3 * v["ms"] / v["launches"],
+                   "noise_elem_per_s": v["elements"] / (v["ms"] * 1e-3)} for n, v in per_kernel.items()}
+    fwd = [n for n in per_kernel if n.startswith("linear")]
+    grads = [n for n in per_kernel if n.startswith("grad")]
+    fwd_ms = sum(per_kernel[n]["ms"] for n in fwd)
+    grad_ms = sum(per_kernel[n]["ms"] for n in grads)
+    gw = sum(per_kernel[n]["grad_w_elems"] for n in grads)
+    return {
+        "value": value, "unit": UNIT, "ms_per_step": res["total_ms_max"] / res["steps"],
+        "steps": res["steps"], "noise_elements_per_step": res["el_step"],
+        "roofline": roofline_of(per_kernel, pk, wl.name),
+        "kernels": kernels,
+        "perturbed_linear_tflops": (sum(per_kernel[n]["flops"] for n in fwd) / (fwd_ms * 1e-3) / 1e12)
+                                   if fwd else None,
+        "grad_w_elem_per_s": (gw / (grad_ms * 1e-3)) if grads and gw else None,
+        "launch": ("step pass: one CUDA graph of the step's C-ABI calls per step" if res["graph"] else
+                   "step pass: direct C-ABI calls" + (f" (graph capture failed: {res['graph_error']})"
+                                                      if res["graph_error"] else "")),
+    }
+
+
+def measure_hash_peak(dev, stream, reps: int = 10):
+    """The hash-only kernel (vn_hash_probe) on every SM at full occupancy: 2048 threads
+    per SM, 4 rounds, 4096 elements per thread. Its element rate x 12 ALU-pipe
+    operations per element is the measured ceiling of the integer ALU pipe."""
+    import torch
+    from virtual_noise_perturbed_gb300 import _lib
+
+    lib = _lib.load()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    n_sums, m = sms * 2048 * 4, 4096
+    sums = torch.empty(n_sums, dtype=torch.float32, device=dev)
+    args = (0x5EED, 0, n_sums, m, ctypes.c_void_p(sums.data_ptr()), ctypes.c_void_p(stream.cuda_stream))
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            _lib.check(lib.vn_hash_probe(*args), "vn_hash_probe")
+        torch.cuda.synchronize(dev)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for a, b in ev:
+            a.record(stream)
+            _lib.check(lib.vn_hash_probe(*args), "vn_hash_probe")
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+    ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    el = n_sums * m
+    rate = el / (ms * 1e-3)
+    return {"kernel": "hash_probe", "elem_per_s": rate, "ops_per_element": ALU_OPS_PER_ELEMENT,
+            "tops": rate * ALU_OPS_PER_ELEMENT / 1e12, "ms": ms, "launches": reps,
+            "elements_per_launch": el,
+            "derived_tops": SMS_NOMINAL * ALU_LANES_PER_SM * SM_CLOCK_MAX_HZ / 1e12,
+            "launch": f"{sms} SMs x 2048 threads x 4 rounds, {m} elements per thread; median of {reps}"}
+
+
+def with_measured_peak(roof, hp):
+    """Add the measured ALU ceiling beside an alu-bound roofline's derived peak."""
+    if hp is not None and roof.get("bound") == "alu":
+        roof["peak_measured"] = hp["tops"]
+        roof["frac_of_measured"] = roof["achieved"] / hp["tops"]
+        roof["peak_measured_source"] = "measured: vn_hash_probe (the hash alone) in this run"
+    return roof
+
+
+EXTRA_DEFAULT = ["mid", "grad_only", "es_mlp", "tiny"]
+
+
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["vn", "reference"], default="vn")
-    ap.add_argument("--workload", default="es_mlp",
+    ap.add_argument("--workload", default="large_tc",
                     choices=["tiny", "es_mlp", "mid", "grad_only", "large_tc"])
-    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--extras", default="auto",
+                    help="workloads measured besides the headline: 'auto' (the other four when the "
+                         "headline is large_tc, else none), 'none', or a comma-separated list")
+    ap.add_argument("--extra-seconds", type=float, default=2.5,
+                    help="timed-region budget of each extra workload's step pass")
+    ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--no-graph", action="store_true",
                     help="step pass: direct C-ABI calls instead of a CUDA graph of them")
     ap.add_argument("--kernel-steps", type=int, default=None,
-                    help="steps of the per-kernel timing pass (default: --steps)")
+                    help="steps of the headline's per-kernel timing pass (default: --steps)")
     ap.add_argument("--pop", type=int, default=None,
-                    help="run only the workload's first POP individuals (smaller profiling cases)")
+                    help="run only the headline workload's first POP individuals (smaller profiling cases)")
     ap.add_argument("--noise", choices=["uniform", "gaussian"], default="uniform",
                     help="gaussian: the Box-Muller noise variant throughout (not on the tiny workload)")
     ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-hash-peak", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -563,14 +835,29 @@ def main(argv=None) -> int:
         ap.error("--noise gaussian applies to the es_mlp, mid, grad_only and large_tc workloads")
 
     from virtual_noise_perturbed_gb300 import workloads
-    number = {v: k for k, v in workloads.NAMES.items()}[args.workload]
+    numbers = {v: k for k, v in workloads.NAMES.items()}
+    if args.extras == "auto":
+        extras = [e for e in EXTRA_DEFAULT if e != args.workload] if args.workload == "large_tc" else []
+    elif args.extras == "none":
+        extras = []
+    else:
+        extras = [e.strip() for e in args.extras.split(",") if e.strip()]
+        bad = [e for e in extras if e not in numbers]
+        if bad:
+            ap.error(f"unknown workloads in --extras: {bad}")
+    if args.noise == "gaussian":
+        extras = [e for e in extras if e != "tiny"]
     world, rank, local = dist_env()
-    wl = workloads.make(number)
-    if args.pop is not None:
-        wl = wl.first(args.pop)
-    if rank > 0:  # independent population per rank
-        wl.seeds = wl.seeds + rank * wl.pop
 
+    def load(name, pop=None):
+        wl = workloads.make(numbers[name])
+        if pop is not None:
+            wl = wl.first(pop)
+        if rank > 0:  # independent population per rank
+            wl.seeds = wl.seeds + rank * wl.pop
+        return wl
+
+    wl = load(args.workload, args.pop)
     if args.impl == "reference":
         return run_reference(args, wl, world, rank)
 
@@ -586,131 +873,74 @@ def main(argv=None) -> int:
     from virtual_noise_perturbed_gb300 import _lib, build as vbuild
     vbuild.build()
     stream = torch.cuda.Stream(dev)
-    launches, bufs, outputs = build_step(wl, dev, stream.cuda_stream, args.noise)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    el_step = sum(l.elements for l in launches)
+    pk = peaks()
 
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            for l in launches:
-                l()
-            flush.zero_()
-        torch.cuda.synchronize(dev)
-        # Two timed passes over the same launches. The step pass brackets each step
-        # with one pair of events (an event pair around every launch would add its own
-        # gaps to the step); the kernel pass brackets every launch, for the per-kernel
-        # durations, shares and the roofline of the dominant kernel.
-        k_steps = args.steps
-        graph_error = None
-        k_kern = args.kernel_steps if args.kernel_steps is not None else args.steps
-        ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                   for _ in range(k_steps)]
-        # The step pass replays the step's C-ABI calls captured once as a CUDA graph
-        # (the same kernels and arguments; the graph only removes the host launch
-        # latency between them). If capture is refused, the calls are made directly.
-        graph = None
-        if not args.no_graph:
-            try:
-                graph = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(graph, stream=stream):
-                    for l in launches:
-                        l()
-                graph.replay()
-                torch.cuda.synchronize(dev)
-            except Exception as exc:  # noqa: BLE001 -- reported in the JSON line
-                graph = None
-                graph_error = f"{type(exc).__name__}: {exc}"[:200]
-                torch.cuda.synchronize(dev)
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(launches))]
-              for _ in range(k_kern)]
-        barrier(world)
-        torch.cuda.synchronize(dev)
-        sampler = ClockSampler(gpu_id(dev))
-        wall0 = time.perf_counter()
-        for k in range(k_steps):
-            ev_step[k][0].record(stream)
-            if graph is not None:
-                graph.replay()
-            else:
-                for l in launches:
-                    l()
-            ev_step[k][1].record(stream)
-            flush.zero_()
-        torch.cuda.synchronize(dev)
-        wall = time.perf_counter() - wall0
-        barrier(world)
-        torch.cuda.synchronize(dev)
-        for k in range(k_kern):
-            for j, l in enumerate(launches):
-                ev[k][2 * j].record(stream)
-                l()
-                ev[k][2 * j + 1].record(stream)
-            flush.zero_()
-        torch.cuda.synchronize(dev)
-        clocks = sampler.stop()
-        barrier(world)
+    sampler = ClockSampler(gpu_id(dev))
+    head = measure(wl, dev, stream, flush, args, world, args.noise)
+    launches_total = head["gpu_launches"]
+    extra_res = {}
+    for name in extras:
+        xw = load(name)
+        r = measure(xw, dev, stream, flush, args, world, args.noise, steps=args.steps)
+        extra_res[name] = (xw, r)
+        launches_total += r["gpu_launches"]
+    hp = None
+    if not args.no_hash_peak:
+        hp = measure_hash_peak(dev, stream)
+        launches_total += hp["launches"]
+    clocks = sampler.stop()
     status = _lib.load().vn_device_status(ctypes.c_void_p(stream.cuda_stream))
     if status != 0:
         raise _lib.VNError(status, "bench")
 
-    step_ms = [a.elapsed_time(b) for a, b in ev_step]
-    per_kernel = {}
-    for k in range(k_kern):
-        for j, l in enumerate(launches):
-            ms = ev[k][2 * j].elapsed_time(ev[k][2 * j + 1])
-            rec = per_kernel.setdefault(l.kernel, {"ms": 0.0, "launches": 0, "elements": 0, "flops": 0.0,
-                                                   "hbm_bytes": 0.0})
-            rec["ms"] += ms
-            rec["launches"] += 1
-            rec["elements"] += l.elements
-            rec["flops"] += l.flops
-            rec["hbm_bytes"] += l.hbm_bytes
-    total_ms = sum(step_ms)
-    total_ms_max = max_over_ranks(total_ms, world, dev)
-    value = el_step * args.steps * world / (total_ms_max * 1e-3)
-
-    # --- roofline of the dominant kernel
-    roofline = roofline_of(per_kernel, peaks(), wl.name)
-    kernels = {n: {"launches": v["launches"], "share": v["ms"] / sum(x["ms"] for x in per_kernel.values()),
-                   "avg_us": 1e3 * v["ms"] / v["launches"],
-                   "noise_elem_per_s": v["elements"] / (v["ms"] * 1e-3)} for n, v in per_kernel.items()}
-
-    # --- secondary metrics of the step (per phase)
-    fwd = [x for x in launches if x.kernel.startswith("linear")]
-    fwd_ms = sum(per_kernel[n]["ms"] for n in per_kernel if n.startswith("linear"))
-    grad_w_elems = sum(x.grad_w_elems for x in launches)
-    extra = {
-        "perturbed_linear_tflops": (sum(x.flops for x in fwd) * args.steps / (fwd_ms * 1e-3) / 1e12) if fwd else None,
-        "grad_w_elem_per_s": (grad_w_elems * args.steps / (sum(per_kernel[k]["ms"] for k in per_kernel if k.startswith("grad")) * 1e-3))
-                             if any(k.startswith("grad") for k in per_kernel) else None,
-        "noise_elements_per_step": el_step,
-    }
+    s_head = summarise(wl, head, world, pk)
+    with_measured_peak(s_head["roofline"], hp)
+    configs = {}
+    for name, (xw, r) in extra_res.items():
+        s = summarise(xw, r, world, pk)
+        with_measured_peak(s["roofline"], hp)
+        s["description"] = xw.description
+        s["dtype"] = compute_dtype(xw)
+        configs[name] = s
 
     # --- end to end: host buffers, copies inside the timed region
-    n_launches = len(launches)
-    del launches, bufs, outputs
-    e2e = run_e2e(wl, dev, stream, args.e2e_steps, world, el_step, args.noise)
+    e2e = run_e2e(wl, dev, stream, args.e2e_steps, world, head["el_step"], args.noise)
+    launches_total += head["n_launches"] * e2e["steps"]
+    for name, (xw, r) in extra_res.items():
+        steps = int(min(args.e2e_steps, max(3, args.extra_seconds * 1e3 / max(configs[name]["ms_per_step"], 1e-3))))
+        configs[name]["e2e"] = run_e2e(xw, dev, stream, steps, world, r["el_step"], args.noise)
+        launches_total += r["n_launches"] * steps
+        if xw.number in (1, 2):
+            # The same step without the noise dump: its 4-byte-per-element copy back
+            # dominates the host link, so the forward + ranks + gradient + update
+            # step is reported on its own as well.
+            el = step_elements(xw, include_dump=False)
+            configs[name]["e2e_no_dump"] = run_e2e(xw, dev, stream, steps, world, el, args.noise,
+                                                   include_dump=False)
+            launches_total += (r["n_launches"] - 1) * steps
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, inds, tt = time_oracle(wl, args.cpu_baseline_seconds, noise=args.noise)
-        cpu = {"value": rate, "unit": UNIT, "cores": cpu_cores_used(), "kind": "oracle",
-               "sample": f"one oracle pass over the first {inds} of {wl.pop} individuals "
-                         f"(forward, gradient sums, noise dump), {tt:.1f} s"}
+        rate, inds, tt, cores = time_oracle(wl, args.cpu_baseline_seconds, noise=args.noise)
+        cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": sample_text(wl, inds, cores) + f", {tt:.1f} s"}
 
     if rank == 0:
         cfg = config_for(wl, world, args.noise)
-        cfg["noise_elements_per_step"] = el_step
-        cfg["launch"] = ("step pass: one CUDA graph of the step's C-ABI calls per step"
-                         if graph is not None else
-                         "step pass: direct C-ABI calls" + (f" (graph capture failed: {graph_error})"
-                                                            if graph_error else ""))
-        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-                "warmup": args.warmup, "ms_per_step": total_ms_max / args.steps, "higher_is_better": True,
+        cfg["noise_elements_per_step"] = head["el_step"]
+        cfg["launch"] = s_head["launch"]
+        line = {"metric": METRIC, "value": s_head["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": s_head["ms_per_step"], "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": compute_dtype(wl),
-                "data": "synthetic", "config": cfg, "roofline": roofline, "cpu_baseline": cpu,
-                "e2e": e2e, "gpu_launches": n_launches * (k_steps + k_kern), "clocks": clocks,
-                "kernels": kernels, **extra, "wall_s_timed_region": wall}
+                "data": "synthetic", "config": cfg, "roofline": s_head["roofline"], "cpu_baseline": cpu,
+                "e2e": e2e, "gpu_launches": launches_total, "clocks": clocks,
+                "kernels": s_head["kernels"],
+                "perturbed_linear_tflops": s_head["perturbed_linear_tflops"],
+                "grad_w_elem_per_s": s_head["grad_w_elem_per_s"],
+                "noise_elements_per_step": head["el_step"],
+                "configs": configs, "alu_peak_measured": hp,
+                "wall_s_timed_region": head["wall_s"]}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -718,7 +948,7 @@ def main(argv=None) -> int:
     return 0
 
 
-def run_e2e(wl, dev, stream, steps, world, el_step, noise):
+def run_e2e(wl, dev, stream, steps, world, el_step, noise, include_dump=True):
     """The same step through the C ABI with inputs in pinned host memory: each step
     copies its inputs host -> device, runs, and copies every result back.
 
@@ -732,7 +962,7 @@ def run_e2e(wl, dev, stream, steps, world, el_step, noise):
     load_stream = torch.cuda.Stream(dev)   # host -> device
     sets = []
     for _ in range(2):
-        launches, bufs, outputs = build_step(wl, dev, stream.cuda_stream, noise)
+        launches, bufs, outputs = build_step(wl, dev, stream.cuda_stream, noise, include_dump)
         sets.append((launches, bufs, outputs))
     host_in = {k: v.detach().cpu().pin_memory() for k, v in sets[0][1].items()
                if v is not None and v.numel()}

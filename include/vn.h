@@ -306,6 +306,20 @@ vn_status vn_es_update(float* theta, const float* grad, int64_t n, double lr, vo
  * since the last call, VN_ERR_CUDA if synchronisation failed, else VN_OK. */
 vn_status vn_device_status(void* stream);
 
+/*
+ * vn_hash_probe -- a measurement kernel, not a step of the method: the noise
+ * hash and nothing else,
+ *     sums[t] = sum_{e < m} PRNG(seed, offset + t*m + e),  t < n_sums,
+ * accumulated in fp32 in order of e (PRNG as defined at the top of this file).
+ * One thread per t regenerates its m elements in registers and writes one
+ * float, so the launch time is the hash's own: its element rate is the
+ * measured ceiling of the integer ALU pipe for this hash, against which the
+ * other kernels' rates can be read. sums [n_sums] fp32, 4-byte aligned;
+ * 0 <= n_sums <= 2^31, m >= 0, n_sums * m < 2^63.
+ */
+vn_status vn_hash_probe(int64_t seed, uint64_t offset, int64_t n_sums, int64_t m, float* sums,
+                        void* stream);
+
 /* Test hook for the bounded-wait machinery of the tensor-core kernel; not part
  * of the method. Runs the tensor-core forward with the arguments of
  * vn_perturbed_linear (the same checks, with the real pop; VN_PATH_TC) but with every

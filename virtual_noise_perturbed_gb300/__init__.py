@@ -15,6 +15,7 @@ from .api import (  # noqa: F401
     device_status,
     es_update,
     gradient_update,
+    hash_probe,
     noise_dump,
     perturbed_linear_path,
     virtual_bias_gradient,
@@ -26,7 +27,7 @@ from .api import (  # noqa: F401
 )
 
 __all__ = [
-    "VNError", "centered_ranks", "compute_offsets", "device_status", "es_update", "gradient_update", "noise_dump", "perturbed_linear_path",
+    "VNError", "centered_ranks", "compute_offsets", "device_status", "es_update", "gradient_update", "hash_probe", "noise_dump", "perturbed_linear_path",
     "virtual_bias_gradient", "virtual_flat_gradient", "virtual_perturbed_linear", "virtual_perturbed_mlp",
     "virtual_reduce_metric",
     "virtual_weight_gradient",

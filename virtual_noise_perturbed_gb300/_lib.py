@@ -51,6 +51,7 @@ SIGNATURES = {
     "vn_gradient_ex": (_I, [_P, _P, _I64, _I64, _D, _U64, _I, _P, _P]),
     "vn_gradient_update": (_I, [_P, _P, _I64, _I64, _D, _U64, _I, _D, _P, _P, _P]),
     "vn_device_status": (_I, [_P]),
+    "vn_hash_probe": (_I, [_I64, _U64, _I64, _I64, _P, _P]),
     "vn_testhook_linear_tc_withhold": (_I, [_P, _I, _I, _P, _I, _P, _I, _P, _I64, _I64, _I64, _I64,
                                            _D, _U64, _P, _I, _I64, _D, _P]),
     "vn_status_string": (ctypes.c_char_p, [_I]),

@@ -370,6 +370,19 @@ def es_update(theta: torch.Tensor, grad: torch.Tensor, lr: float) -> torch.Tenso
     return theta
 
 
+def hash_probe(seed: int, offset: int, n_sums: int, m: int, *, device=None,
+               out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """The hash alone (``vn_hash_probe``, a measurement kernel): (n_sums,) fp32 with
+    sums[t] = sum_{e < m} PRNG(seed, offset + t*m + e)."""
+    lib = load()
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    s = _out(out, (int(n_sums),), dev)
+    with torch.cuda.device(dev):
+        st = lib.vn_hash_probe(int(seed), int(offset) & _M64, int(n_sums), int(m), _ptr(s), _stream(s))
+    check(st, "vn_hash_probe")
+    return s
+
+
 def compute_offsets(param_shapes: Sequence[Sequence[int]]) -> list:
     """Start offset of each parameter block: the element count of all blocks before it."""
     offsets, total = [], 0
@@ -404,5 +417,5 @@ def device_status(device=None) -> None:
 
 __all__ = ["virtual_perturbed_linear", "virtual_weight_gradient", "virtual_bias_gradient",
            "virtual_flat_gradient",
-           "noise_dump", "virtual_reduce_metric", "compute_offsets", "perturbed_linear_path",
+           "noise_dump", "virtual_reduce_metric", "compute_offsets", "perturbed_linear_path", "hash_probe",
            "device_status", "VNError"]

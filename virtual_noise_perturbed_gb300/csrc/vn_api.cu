@@ -450,6 +450,18 @@ vn_status vn_es_update(float* theta, const float* grad, int64_t n, double lr, vo
   return launched(vn::launch_es_update(theta, grad, n, lr_f, static_cast<cudaStream_t>(stream)));
 }
 
+vn_status vn_hash_probe(int64_t seed, uint64_t offset, int64_t n_sums, int64_t m, float* sums,
+                        void* stream) {
+  if (n_sums < 0 || n_sums > (int64_t{1} << 31) || m < 0) return VN_ERR_SHAPE;
+  int64_t elems;
+  if (!mul(n_sums, m, &elems)) return VN_ERR_OVERFLOW;
+  if (n_sums == 0) return VN_OK;
+  if (sums == nullptr) return VN_ERR_NULL;
+  if (!aligned(sums, 4)) return VN_ERR_ALIGN;
+  return launched(vn::launch_hash_probe(static_cast<uint64_t>(seed), offset, n_sums, m, sums,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
 vn_status vn_device_status(void* stream) {
   cudaError_t err = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
   if (err != cudaSuccess) return cuda_failure(err);

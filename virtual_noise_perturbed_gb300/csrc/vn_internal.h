@@ -106,6 +106,10 @@ cudaError_t launch_centered_ranks(const float* fitness, int64_t pop, float* out,
 cudaError_t launch_es_update(float* theta, const float* grad, int64_t n, float lr,
                              cudaStream_t stream);
 
+// sums[t] = sum_{e < m} PRNG(seed, offset + t*m + e), t < n_sums: the hash alone.
+cudaError_t launch_hash_probe(uint64_t seed, uint64_t offset, int64_t n_sums, int64_t m,
+                              float* sums, cudaStream_t stream);
+
 // Reads and clears the device status word of the bounded-wait kernels (0 = fine).
 cudaError_t take_device_status(unsigned int* status, cudaStream_t stream);
 
