@@ -18,7 +18,9 @@ Modules
               perturbed linear forward, the weight / bias gradient estimates,
               the mean-abs reduction metric, the centered ranks and the
               parameter update, all in float64 with the noise materialised
-              explicitly; the dump, the gradient and the forward also with the
+              explicitly; the bf16 model of the tensor-core forward (the perturbed
+              weight, and optionally the output, rounded to bfloat16) and the
+              floor that rounding sets on any bf16 implementation's deviation; the dump, the gradient and the forward also with the
               Gaussian variant of the noise (Box-Muller on the finalizer's
               two halves, ``splitmix.gaussian_*``).
 

@@ -124,6 +124,66 @@ def perturbed_linear(x, weight, bias, seeds, sigma: float, offset: int,
     return y
 
 
+def round_bf16(a) -> np.ndarray:
+    """Round float64 values to the nearest bfloat16 value, ties to the even one: keep 8
+    significant bits (bfloat16's implicit bit and 7 stored bits). Written out on the
+    binary exponent: a = m * 2**e with 0.5 <= |m| < 1, so m * 2**8 rounded to an integer
+    (numpy's rint: half to even) times 2**(e - 8) is the nearest 8-bit-significand value.
+    Defined here for zero and for |a| in bfloat16's normal range [2**-126, 2**128)
+    (raises otherwise), which covers every value the bf16 model below rounds."""
+    a = np.asarray(a, dtype=np.float64)
+    mag = np.abs(a[a != 0])
+    if mag.size and (mag.min() < 2.0 ** -126 or mag.max() >= 2.0 ** 128 or not np.all(np.isfinite(mag))):
+        raise ValueError("round_bf16: a value outside bfloat16's normal range")
+    m, e = np.frexp(a)
+    return np.ldexp(np.rint(m * 256.0), e - 8)
+
+
+def perturbed_linear_bf16(x, weight, bias, seeds, sigma: float, offset: int,
+                          individuals: Optional[Iterable[int]] = None,
+                          rows: Optional[Iterable[int]] = None, round_y: bool = False) -> np.ndarray:
+    """The bf16 model of the tensor-core forward: ``perturbed_linear`` with the perturbed
+    weight ``W + sigma*N_i`` rounded to bfloat16 (``round_bf16``) before the product and,
+    with ``round_y``, the output (after the bias) rounded to bfloat16 too. Everything else
+    is float64 from the exact inputs (bf16 X values are exact in float64), so the model
+    differs from ``perturbed_linear`` by those two roundings alone."""
+    w = np.asarray(weight, dtype=np.float64)
+    out_f, in_f = w.shape
+    x = np.asarray(x, dtype=np.float64)
+    s = np.asarray(seeds)
+    pop = s.shape[0]
+    shared = x.ndim == 2
+    if x.shape[-1] != in_f or (not shared and x.shape[0] != pop):
+        raise ValueError("x / weight / seeds shapes disagree")
+    inds = range(pop) if individuals is None else list(individuals)
+    rows = list(range(out_f)) if rows is None else list(rows)
+    b = None if bias is None else np.asarray(bias, dtype=np.float64)
+    y = np.empty((len(inds), x.shape[-2], len(rows)), dtype=np.float64)
+    for r, i in enumerate(inds):
+        n_i = weight_noise(s[i], out_f, in_f, offset, rows)
+        w_pert = round_bf16(w[rows] + sigma * n_i)                    # bf16(W + sigma*N_i)
+        xi = x if shared else x[i]
+        yi = xi @ w_pert.T
+        if b is not None:
+            nb_i = bias_noise(s[i], out_f, offset + out_f * in_f)[rows]
+            yi = yi + (b[rows] + sigma * nb_i)[None, :]
+        y[r] = round_bf16(yi) if round_y else yi
+    return y
+
+
+def bf16_floor(x, weight, bias, seeds, sigma: float, offset: int,
+               individuals: Optional[Iterable[int]] = None, round_y: bool = False) -> float:
+    """The deviation that rounding alone costs a bf16 implementation of the forward:
+    max |Y_model - Y| / RMS(Y), with Y = ``perturbed_linear`` (exact up to float64) and
+    Y_model = ``perturbed_linear_bf16`` (W + sigma*N_i, and Y when ``round_y``, rounded to
+    bfloat16), on the selected individuals."""
+    exact = perturbed_linear(x, weight, bias, seeds, sigma, offset, individuals=individuals)
+    model = perturbed_linear_bf16(x, weight, bias, seeds, sigma, offset, individuals=individuals,
+                                  round_y=round_y)
+    rms = float(np.sqrt(np.mean(exact ** 2)))
+    return float(np.max(np.abs(model - exact))) / rms
+
+
 def weight_gradient(fitness, seeds, weight_shape, sigma: float, pop_size: int,
                     offset: int, rows: Optional[Iterable[int]] = None) -> np.ndarray:
     """``virtual_weight_gradient`` in float64:

@@ -34,6 +34,18 @@ def _mix_np_wrong_shift(z):
         return z ^ (z >> np.uint64(31))
 
 
+def _round_bf16_truncating(a):
+    a = np.asarray(a, dtype=np.float64)
+    m, e = np.frexp(a)
+    return np.ldexp(np.trunc(m * 256.0), e - 8)
+
+
+def _bf16_model_w_unrounded(x, weight, bias, seeds, sigma, offset, individuals=None, rows=None,
+                            round_y=False):
+    y = es.perturbed_linear(x, weight, bias, seeds, sigma, offset, individuals=individuals, rows=rows)
+    return es.round_bf16(y) if round_y else y
+
+
 def _state_off_by_one(seed, idx):
     return ((seed & sm.MASK64) + (idx & sm.MASK64) * sm.GAMMA) & sm.MASK64
 
@@ -198,6 +210,10 @@ _ORIG = {
 
 MUTATIONS = [
     # (name, [(module, attribute, replacement)], pin that must fail)
+    ("bf16 rounding truncates", [(es, "round_bf16", _round_bf16_truncating)],
+     pins.test_round_bf16_matches_torchs_conversion_and_ties),
+    ("bf16 model leaves W' unrounded", [(es, "perturbed_linear_bf16", _bf16_model_w_unrounded)],
+     pins.test_bf16_model_one_hot_reads_the_rounded_noise),
     ("finalizer shift 30 -> 29", [(sm, "mix64", _mix_wrong_shift)],
      pins.test_finalizer_inverts_with_independent_inverse),
     ("numpy finalizer shift 27 -> 28", [(sm, "mix64_np", _mix_np_wrong_shift)],

@@ -500,3 +500,80 @@ def test_gaussian_forward_identity_and_linearity_in_sigma():
     np.testing.assert_allclose(e1, e2, rtol=0, atol=1e-12)
     eu = (es.perturbed_linear(x, w, b, seeds, 0.25, off) - plain) / 0.25       # the uniform kind
     assert np.max(np.abs(eu - e1)) > 0.1                                         # differs from it
+
+
+# --- the bf16 model of the tensor-core forward and its floor (the perturbed weight,
+# and optionally the output, rounded to bfloat16; module description of the page: the
+# noise is added to the weight tile that the bf16 contraction then reads)
+
+def test_round_bf16_matches_torchs_conversion_and_ties():
+    """On float32 inputs (exact in float64, so one rounding either way) the oracle's
+    rounding equals torch's float32 -> bfloat16 conversion (round to nearest, ties to
+    even), over many binades and both signs; ties worked by hand."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(11)
+    a = (rng.standard_normal(200_000) * np.exp2(rng.integers(-60, 60, 200_000))).astype(np.float32)
+    # values just around bf16 ties: a bf16 value plus half its spacing, and one float32 ulp either side
+    base = torch.tensor(rng.standard_normal(20_000), dtype=torch.bfloat16).float().numpy()
+    half = np.abs(base) * np.float32(2.0 ** -8)
+    ties = np.concatenate([base + half, np.nextafter(base + half, np.float32(np.inf)),
+                           np.nextafter(base + half, np.float32(-np.inf))]).astype(np.float32)
+    for v in (a, ties):
+        want = torch.from_numpy(v).to(torch.bfloat16).double().numpy()
+        assert np.array_equal(es.round_bf16(v.astype(np.float64)), want)
+    hand = es.round_bf16(np.array([1 + 2 ** -8, 1 + 3 * 2 ** -8, -(1 + 2 ** -8), 255.5, 0.0, 2 ** -126]))
+    assert list(hand) == [1.0, 1 + 2 ** -6, -1.0, 256.0, 0.0, 2 ** -126]
+    with pytest.raises(ValueError):
+        es.round_bf16(np.array([2.0 ** -130]))
+
+
+def test_bf16_model_special_cases():
+    """sigma = 0 and bf16-exact weights: rounding W' changes nothing, so the model is the
+    exact forward; with round_y it is that forward rounded to bfloat16."""
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal((3, 4, 24))
+    w = es.round_bf16(rng.standard_normal((10, 24)) / 5)
+    b = rng.standard_normal(10) * 0.1
+    seeds = np.array([1, 2, 3])
+    exact = es.perturbed_linear(x, w, b, seeds, 0.0, 7)
+    assert np.array_equal(es.perturbed_linear_bf16(x, w, b, seeds, 0.0, 7), exact)
+    assert np.array_equal(es.perturbed_linear_bf16(x, w, b, seeds, 0.0, 7, round_y=True), es.round_bf16(exact))
+    assert es.bf16_floor(x, w, b, seeds, 0.0, 7) == 0.0
+
+
+def test_bf16_model_one_hot_reads_the_rounded_noise():
+    """X rows one-hot at k, W = 0, sigma = 1, no bias: the model's Y[i, r, j] is the
+    bfloat16 rounding of noise element j*in + k, i.e. torch's bfloat16 of the float32
+    dump (the noise values are exact in float32)."""
+    torch = pytest.importorskip("torch")
+    pop, in_f, out_f, off = 3, 9, 13, 2 ** 40 + 5
+    seeds = np.array([4, -8, 15])
+    ks = [0, 4, 8]
+    x = np.zeros((pop, len(ks), in_f))
+    for r, k in enumerate(ks):
+        x[:, r, k] = 1.0
+    y = es.perturbed_linear_bf16(x, np.zeros((out_f, in_f)), None, seeds, 1.0, off)
+    dump = es.noise_dump(seeds, out_f * in_f, off).reshape(pop, out_f, in_f)
+    want = torch.from_numpy(dump).to(torch.bfloat16).double().numpy()
+    for r, k in enumerate(ks):
+        assert np.array_equal(y[:, r, :], want[:, :, k])
+
+
+def test_bf16_floor_is_within_the_rounding_bound():
+    """Each rounding to bfloat16 has relative error at most 2^-9, so the model deviates
+    from the exact forward by at most 2^-9 * (sum_k |x_k| |W'_jk| + |Y|) per output; the
+    floor is positive for a generic case and below that bound, and grows when Y is
+    rounded too."""
+    rng = np.random.default_rng(13)
+    x = es.round_bf16(rng.standard_normal((4, 16, 64)))
+    w = rng.standard_normal((32, 64)) / 8
+    b = rng.standard_normal(32) * 0.1
+    seeds = np.arange(4)
+    exact = es.perturbed_linear(x, w, b, seeds, 0.05, 3)
+    rms = np.sqrt(np.mean(exact ** 2))
+    wp = np.stack([w + 0.05 * es.weight_noise(s, 32, 64, 3) for s in seeds])  # [pop, out, in]
+    bound_w = 2.0 ** -9 * np.einsum("prk,pjk->prj", np.abs(x), np.abs(wp))
+    f_w = es.bf16_floor(x, w, b, seeds, 0.05, 3)
+    f_y = es.bf16_floor(x, w, b, seeds, 0.05, 3, round_y=True)
+    assert 0.0 < f_w <= np.max(bound_w) / rms
+    assert f_w < f_y <= np.max(bound_w * (1 + 2.0 ** -9) + 2.0 ** -9 * np.abs(exact)) / rms
