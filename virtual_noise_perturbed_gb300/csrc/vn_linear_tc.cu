@@ -55,7 +55,7 @@ constexpr int kHashWarps = 16;
 constexpr int kFirstHashWarp = 6;
 constexpr int kThreads = (kFirstHashWarp + kHashWarps) * 32;  // 704
 constexpr int kHashThreads = kHashWarps * 32;                 // 512
-constexpr int kKC = 64;                                       // k per stage (128 bytes of bf16)
+constexpr int kAtomK = 64;                                    // k per swizzle atom (128 bytes of bf16)
 constexpr uint32_t kHalfBytes = 128 * 128;                    // 128 rows x 128 bytes
 constexpr int kTmemCols = 512;
 constexpr unsigned long long kTimeoutNs = 4000000000ull;      // default limit of one wait: 4 s
@@ -80,7 +80,10 @@ struct TcParams {
   int b_bf16, act;
   int nt, g, nbuf, stages, k_chunks, x_shared;
   uint32_t stage_bytes, a_bytes, idesc;
-  uint32_t w_bytes;  // one W tile in shared memory: 128 rows x 64 k of W's dtype
+  uint32_t x_atom_bytes;  // one swizzle atom of the X tile: nt rows x 128 bytes
+  uint32_t w_bytes;       // one W tile in shared memory: 128 rows x (64 * atoms) k of W's dtype
+  int w_slots;            // W tiles in the ring (1 or 2)
+  int units32;            // the unit index and its decomposition fit in 32 bits
   unsigned long long timeout_ns;  // limit of every barrier wait
   uint32_t g_lo, g_hi, one;       // GAMMA's halves and 1, passed at run time: the state
                                   // step's carry half is then a multiply-add on the IMAD
@@ -319,10 +322,20 @@ struct Unit {
 };
 __device__ __forceinline__ Unit decode(const TcParams& p, int64_t u, int mh) {
   Unit r;
-  const int64_t mt = u % p.m_tiles;
-  const int64_t rest = u / p.m_tiles;
-  const int64_t ntile = rest % p.n_tiles;
-  const int64_t g = rest / p.n_tiles;
+  int64_t mt, ntile, g;
+  if (p.units32) {  // 32-bit divisions: a 64-bit one is a long instruction sequence
+    const uint32_t uu = static_cast<uint32_t>(u);
+    const uint32_t mtiles = static_cast<uint32_t>(p.m_tiles), ntiles = static_cast<uint32_t>(p.n_tiles);
+    const uint32_t rest = uu / mtiles;
+    mt = uu - rest * mtiles;
+    ntile = rest % ntiles;
+    g = rest / ntiles;
+  } else {
+    mt = u % p.m_tiles;
+    const int64_t rest = u / p.m_tiles;
+    ntile = rest % p.n_tiles;
+    g = rest / p.n_tiles;
+  }
   r.i0 = static_cast<int>(g * p.g);
   r.gcount = static_cast<int>(min(static_cast<int64_t>(p.g), p.pop - r.i0));
   r.n0 = static_cast<int>(ntile * p.nt);
@@ -332,18 +345,22 @@ __device__ __forceinline__ Unit decode(const TcParams& p, int64_t u, int mh) {
 
 // ---------------------------------------------------------------- the kernel
 // kHook: the test-hook instance (one hashing thread may withhold an arrive);
-// the ordinary instances carry no trace of it.
-template <int MH, bool kWBf16, bool kYBf16, bool kHook, int kKind, bool kG1>
+// the ordinary instances carry no trace of it. kAtoms: swizzle atoms of 64 k per
+// stage (K = 64 * kAtoms); two give every hashing thread 32 elements per stage,
+// so each stage's waits, fences and arrivals are paid once per 32 elements.
+template <int MH, bool kWBf16, bool kYBf16, bool kHook, int kKind, bool kG1, int kAtoms>
 __global__ void __launch_bounds__(kThreads, 1)
 linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
                  const TcParams p) {
+  constexpr int kKC = kAtomK * kAtoms;  // k per stage
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const int S = p.stages;
-  // layout: S stages (A tile, X tile), 2 W slots, barriers
+  // layout: S stages (A tile: kAtoms atoms of 128*MH rows x 128 bytes; X tile: kAtoms
+  // atoms of nt rows x 128 bytes), w_slots W tiles, barriers
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(S) * p.stage_bytes +
-                                               2 * static_cast<size_t>(p.w_bytes));
+                                               static_cast<size_t>(p.w_slots) * p.w_bytes);
   // barriers: full_a[S], full_x[S], empty[S], tmem_full[2], tmem_empty[2], drain,
   // full_w[2], empty_w[2]
   const uint32_t bar0 = smem_u32(bars);
@@ -398,7 +415,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
       uint32_t it = 0, wit = 0;
       Ring rg, wr;
       bool ok = true;
-      const uint32_t x_bytes = static_cast<uint32_t>(p.nt) * 128u;
+      const uint32_t x_bytes = p.x_atom_bytes;
       for (int64_t u = blockIdx.x; ok && u < p.units; u += gridDim.x) {
         const Unit un = decode(p, u, MH);
         for (int kc = 0; ok && kc < p.k_chunks; ++kc) {
@@ -407,14 +424,16 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
           mbar_expect_tx(full_w(wr.s), p.w_bytes);
           tma_load_2d(wslot0 + wr.s * p.w_bytes, &wmap, full_w(wr.s), kc * kKC, un.m0);
           ++wit;
-          wr.next(2);
+          wr.next(p.w_slots);
           for (int ii = 0; ii < (kG1 ? 1 : un.gcount); ++ii, ++it, rg.next(S)) {
             const int s = rg.s;
             if (!(ok = mbar_wait(empty(s), rg.ph ^ 1u, s_abort, kProducerSleepNs))) break;
-            mbar_expect_tx(full_x(s), x_bytes);
+            mbar_expect_tx(full_x(s), x_bytes * kAtoms);
             const int ind = p.x_shared ? 0 : static_cast<int>(un.i0 + ii);
-            tma_load_3d(stage0 + s * p.stage_bytes + p.a_bytes, &xmap, full_x(s), kc * kKC,
-                        static_cast<int>(un.n0), ind);
+#pragma unroll
+            for (int a = 0; a < kAtoms; ++a)
+              tma_load_3d(stage0 + s * p.stage_bytes + p.a_bytes + a * x_bytes, &xmap, full_x(s),
+                          kc * kKC + a * kAtomK, static_cast<int>(un.n0), ind);
           }
         }
       }
@@ -428,10 +447,11 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                  global_ns() - t0 < p.timeout_ns) {
           }
         }
-        for (uint32_t k = 0; k < 2u && k < wit; ++k) {
+        const uint32_t nw = static_cast<uint32_t>(p.w_slots);
+        for (uint32_t k = 0; k < nw && k < wit; ++k) {
           const uint32_t j = wit - 1 - k;
           const uint64_t t0 = global_ns();
-          while (!mbar_try_wait(full_w(static_cast<int>(j & 1u)), (j >> 1) & 1u) &&
+          while (!mbar_try_wait(full_w(static_cast<int>(j % nw)), (j / nw) & 1u) &&
                  global_ns() - t0 < p.timeout_ns) {
           }
         }
@@ -457,12 +477,16 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
             const uint32_t a0 = stage0 + s * p.stage_bytes;
             const uint32_t b0 = a0 + p.a_bytes;
 #pragma unroll
-            for (int ks = 0; ks < kKC / 16; ++ks) {
-              const uint64_t bdesc = sdesc_sw128(b0 + ks * 32);
+            for (int a = 0; a < kAtoms; ++a) {
 #pragma unroll
-              for (int h = 0; h < MH; ++h) {
-                umma_bf16(dcol + (ii * MH + h) * p.nt, sdesc_sw128(a0 + h * kHalfBytes + ks * 32),
-                          bdesc, p.idesc, (kc | ks) != 0);
+              for (int ks = 0; ks < kAtomK / 16; ++ks) {
+                const uint64_t bdesc = sdesc_sw128(b0 + a * p.x_atom_bytes + ks * 32);
+#pragma unroll
+                for (int h = 0; h < MH; ++h) {
+                  umma_bf16(dcol + (ii * MH + h) * p.nt,
+                            sdesc_sw128(a0 + (a * MH + h) * kHalfBytes + ks * 32), bdesc, p.idesc,
+                            (kc | a | ks) != 0);
+                }
               }
             }
             umma_commit(empty(s));
@@ -547,19 +571,23 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
   } else {
     // ----------------------------------------------------------------- hashing
     // Thread t writes 16-byte chunk (t & 7) of rows (t >> 3) + kRowsPerPass*q of
-    // the (128*MH)-row A tile, q < kCPT: one 128-byte row per 8 lanes, so each
-    // quarter-warp store covers all 32 banks once (the swizzle permutes the
-    // chunks within a row). The two 128-row halves of an MH=2 tile are
-    // contiguous, so row r sits at (r >> 3)*1024 + (r & 7)*128 for any r < 256.
+    // each atom of the (128*MH)-row A tile, q < kCPT: one 128-byte row per 8 lanes,
+    // so each quarter-warp store covers all 32 banks once (the swizzle permutes the
+    // chunks within a row). The two 128-row halves of an MH=2 atom are contiguous,
+    // so row r sits at (r >> 3)*1024 + (r & 7)*128 for any r < 256; atom a of the
+    // stage starts a*MH*16 KB in. A thread makes kCPT*kAtoms chunks of 8 elements
+    // per stage.
     constexpr int kRowsPerPass = kHashThreads / 8;          // rows covered by one chunk round
-    constexpr int kCPT = MH * 128 / kRowsPerPass;           // chunks per thread per stage
+    constexpr int kCPT = MH * 128 / kRowsPerPass;           // row passes per atom
     using Raw = typename std::conditional<kWBf16, RawBf16, RawF32>::type;
     const int t = threadIdx.x - kFirstHashWarp * 32;
     const int cc = t & 7;
     const int r8 = (t >> 3) & 7;
     const uint32_t soff0 = static_cast<uint32_t>(t >> 6) * 1024u + r8 * 128u + ((cc ^ r8) << 4);
     const int row0 = t >> 3;
-    auto soff = [&](int q) { return soff0 + q * (kRowsPerPass * 128u); };
+    auto soff = [&](int q, int a) {
+      return soff0 + q * (kRowsPerPass * 128u) + static_cast<uint32_t>(a * MH) * kHalfBytes;
+    };
     auto rowq = [&](int q) { return row0 + q * kRowsPerPass; };
     const float sigma = p.sigma;
     // Uniform kind: W + sigma*n = fma(sigma, 1 + u, W - 1.5*sigma). Gaussian kind:
@@ -568,12 +596,15 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
     const float sigma_unit = kKind == kGaussian ? sigma * kGaussScale : sigma;
     const uint32_t g_lo = p.g_lo, g_hi = p.g_hi, one = p.one;
 
-    // This thread's chunk q inside a staged W tile (rows of 64 k, 256 bytes in
-    // fp32, 128 in bf16). In fp32 the two 16-byte halves are read in an order
-    // that depends on cc, so the 8 threads of a row hit distinct banks.
-    constexpr uint32_t kWRow = kWBf16 ? 128u : 256u;
+    // This thread's chunk (q, a) inside a staged W tile (rows of kKC k: 128*kAtoms
+    // bytes in bf16, 256*kAtoms in fp32). In fp32 the two 16-byte halves are read in
+    // an order that depends on cc, so the 8 threads of a row hit distinct banks.
+    constexpr uint32_t kWElem = kWBf16 ? 2u : 4u;
+    constexpr uint32_t kWRow = kKC * kWElem;
     const uint32_t wfirst = kWBf16 ? 0u : ((cc >> 2) & 1u) * 16u;
-    auto woff = [&](int q) { return static_cast<uint32_t>(rowq(q)) * kWRow + cc * (kWRow / 8); };
+    auto woff = [&](int q, int a) {
+      return static_cast<uint32_t>(rowq(q)) * kWRow + (a * kAtomK + cc * 8) * kWElem;
+    };
     auto load_w = [&](uint32_t addr, Raw& r) {
       if constexpr (kWBf16) {
         r.a = ld_shared_v4(addr);
@@ -588,7 +619,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                           __uint_as_float(hi.w));
       }
     };
-    // State term step from one k chunk to the next: 64 * GAMMA mod 2^64.
+    // State term step from one k chunk to the next: kKC * GAMMA mod 2^64.
     constexpr uint64_t kChunkStep = static_cast<uint64_t>(kKC) * kGamma;
 
     // Ring positions (slot, parity) of the stages and of the W tiles; barrier
@@ -596,9 +627,10 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
     const uint32_t S32 = static_cast<uint32_t>(S);
     const uint32_t stage_bytes = p.stage_bytes;
     const uint32_t fa0 = full_a(0), em0 = empty(0), fw0 = full_w(0), ew0 = empty_w(0);
-    const uint32_t a_this = stage0 + soff0;   // this thread's first chunk in stage 0
-    const uint32_t w_this = wslot0 + woff(0);
+    const uint32_t a_this = stage0 + soff(0, 0);   // this thread's first chunk in stage 0
+    const uint32_t w_this = wslot0 + woff(0, 0);
     const uint32_t w_bytes = p.w_bytes;
+    const uint32_t w_slots = static_cast<uint32_t>(p.w_slots);
     const int k_chunks = p.k_chunks;
     uint32_t s = 0, ph = 0, ws = 0, wph = 0;
     // Test hook: the stage at which this thread skips its arrive (-1: never).
@@ -608,13 +640,19 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
       const Unit un = decode(p, u, MH);
       const int64_t* seedp = p.seeds + un.i0;
       // (offset + j*in + k + 1) * GAMMA of each chunk's first element, k chunk 0;
-      // advanced by kChunkStep per k chunk.
-      uint64_t bst[kCPT];
+      // advanced by kChunkStep per k chunk. With one individual per unit its seed
+      // is added here once, so a stage's chunks start from bst directly.
+      uint64_t bst[kCPT][kAtoms];
+      const uint64_t seed0 = kG1 ? static_cast<uint64_t>(__ldg(seedp)) : 0ull;
 #pragma unroll
       for (int q = 0; q < kCPT; ++q) {
-        bst[q] = index_term(p.offset +
-                            static_cast<uint64_t>(un.m0 + rowq(q)) * static_cast<uint64_t>(p.in) +
-                            static_cast<uint64_t>(cc * 8));
+#pragma unroll
+        for (int a = 0; a < kAtoms; ++a) {
+          bst[q][a] = seed0 + index_term(p.offset +
+                                         static_cast<uint64_t>(un.m0 + rowq(q)) *
+                                             static_cast<uint64_t>(p.in) +
+                                         static_cast<uint64_t>(a * kAtomK + cc * 8));
+        }
       }
       for (int kc = 0; kc < k_chunks; ++kc) {
         // This stage group's W chunks, shared by its G individuals: fp32 W is
@@ -626,14 +664,17 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
         // their X columns are zero fill too (k >= in) or their output rows are
         // never stored (row >= out), and no masking is needed below.
         if (!mbar_wait(fw0 + 8u * ws, wph, s_abort)) goto hashing_done;
-        float wm[kCPT][8];
-        Raw wraw[kCPT];
+        float wm[kCPT][kAtoms][8];
+        Raw wraw[kCPT][kAtoms];
         {
           const uint32_t wb = w_this + ws * w_bytes;
 #pragma unroll
           for (int q = 0; q < kCPT; ++q) {
-            load_w(wb + q * (kRowsPerPass * kWRow), wraw[q]);
-            if constexpr (!kWBf16) unpack_shift(wraw[q], shift, wm[q]);
+#pragma unroll
+            for (int a = 0; a < kAtoms; ++a) {
+              load_w(wb + woff(q, a) - woff(0, 0), wraw[q][a]);
+              if constexpr (!kWBf16) unpack_shift(wraw[q][a], shift, wm[q][a]);
+            }
           }
         }
         // The slot's next tile is written by TMA (the async proxy): order this
@@ -641,42 +682,45 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
         // fence a late warp's reads could return the next tile's values.
         fence_proxy_async_smem();
         mbar_arrive(ew0 + 8u * ws);
-        if (++ws == 2) { ws = 0; wph ^= 1u; }
+        if (++ws == w_slots) { ws = 0; wph ^= 1u; }
         for (int ii = 0; ii < (kG1 ? 1 : un.gcount); ++ii) {
-          const uint64_t seed = static_cast<uint64_t>(__ldg(seedp + ii));
+          const uint64_t seed = kG1 ? 0ull : static_cast<uint64_t>(__ldg(seedp + ii));
           if (!mbar_wait(em0 + 8u * s, ph ^ 1u, s_abort)) goto hashing_done;
           const uint32_t a0 = a_this + s * stage_bytes;
 #pragma unroll
           for (int q = 0; q < kCPT; ++q) {
-            const uint64_t st0 = bst[q] + seed;
-            uint32_t slo = static_cast<uint32_t>(st0), shi = static_cast<uint32_t>(st0 >> 32);
-            float pv[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              // The element's noise term: the uniform kind as 1 + u (its -1.5 rides on
-              // the shift), the Gaussian kind as the unit Box-Muller value.
-              float unit;
-              if constexpr (kKind == kGaussian) {
-                uint32_t zlo, zhi;
-                mix64_halves(slo, shi, zlo, zhi);
-                unit = gaussian_unit(zlo, zhi);
-              } else {
-                unit = __uint_as_float(mix_to_one_plus_u(slo, shi));
+            for (int a = 0; a < kAtoms; ++a) {
+              const uint64_t st0 = bst[q][a] + seed;
+              uint32_t slo = static_cast<uint32_t>(st0), shi = static_cast<uint32_t>(st0 >> 32);
+              float pv[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                // The element's noise term: the uniform kind as 1 + u (its -1.5 rides on
+                // the shift), the Gaussian kind as the unit Box-Muller value.
+                float unit;
+                if constexpr (kKind == kGaussian) {
+                  uint32_t zlo, zhi;
+                  mix64_halves(slo, shi, zlo, zhi);
+                  unit = gaussian_unit(zlo, zhi);
+                } else {
+                  unit = __uint_as_float(mix_to_one_plus_u(slo, shi));
+                }
+                if constexpr (kWBf16) {
+                  // sigma*n = fma(sigma, 1 + u, -1.5*sigma), then + W straight from its bf16 bits.
+                  const float tt = fmaf(sigma_unit, unit, shift);
+                  const uint32_t wv = (e & 4) ? ((e & 2) ? wraw[q][a].a.w : wraw[q][a].a.z)
+                                              : ((e & 2) ? wraw[q][a].a.y : wraw[q][a].a.x);
+                  pv[e] = (e & 1) ? add_bf16_f32<true>(wv, tt) : add_bf16_f32<false>(wv, tt);
+                } else {
+                  pv[e] = fmaf(sigma_unit, unit, wm[q][a][e]);
+                }
+                add64_madc(slo, shi, g_lo, g_hi, one);
               }
-              if constexpr (kWBf16) {
-                // sigma*n = fma(sigma, 1 + u, -1.5*sigma), then + W straight from its bf16 bits.
-                const float tt = fmaf(sigma_unit, unit, shift);
-                const uint32_t wv = (e & 4) ? ((e & 2) ? wraw[q].a.w : wraw[q].a.z)
-                                            : ((e & 2) ? wraw[q].a.y : wraw[q].a.x);
-                pv[e] = (e & 1) ? add_bf16_f32<true>(wv, tt) : add_bf16_f32<false>(wv, tt);
-              } else {
-                pv[e] = fmaf(sigma_unit, unit, wm[q][e]);
-              }
-              add64_madc(slo, shi, g_lo, g_hi, one);
+              st_shared_v4(a0 + soff(q, a) - soff(0, 0), pack_bf16x2(pv[0], pv[1]),
+                           pack_bf16x2(pv[2], pv[3]), pack_bf16x2(pv[4], pv[5]),
+                           pack_bf16x2(pv[6], pv[7]));
             }
-            st_shared_v4(a0 + q * (kRowsPerPass * 128u), pack_bf16x2(pv[0], pv[1]),
-                         pack_bf16x2(pv[2], pv[3]), pack_bf16x2(pv[4], pv[5]),
-                         pack_bf16x2(pv[6], pv[7]));
           }
           fence_proxy_async_smem();
           if constexpr (kHook) {
@@ -688,7 +732,10 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
           if (++s == S32) { s = 0; ph ^= 1u; }
         }
 #pragma unroll
-        for (int q = 0; q < kCPT; ++q) bst[q] += kChunkStep;
+        for (int q = 0; q < kCPT; ++q) {
+#pragma unroll
+          for (int a = 0; a < kAtoms; ++a) bst[q][a] += kChunkStep;
+        }
       }
     }
   hashing_done:;
@@ -717,10 +764,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-template <int MH, bool kW, bool kY, bool kHook, int kKind, bool kG1>
+template <int MH, bool kW, bool kY, bool kHook, int kKind, bool kG1, int kAtoms>
 cudaError_t launch_kernel(const CUtensorMap& xmap, const CUtensorMap& wmap, const TcParams& p,
                           int grid, size_t smem, cudaStream_t stream) {
-  auto fn = linear_tc_kernel<MH, kW, kY, kHook, kKind, kG1>;
+  auto fn = linear_tc_kernel<MH, kW, kY, kHook, kKind, kG1, kAtoms>;
   static SmemRecord configured;
   const cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), smem, configured);
   if (err != cudaSuccess) return err;
@@ -729,13 +776,19 @@ cudaError_t launch_kernel(const CUtensorMap& xmap, const CUtensorMap& wmap, cons
 }
 
 // One individual per unit (the whole TMEM buffer for one batch tile): the
-// individual loops of every role have a single, compile-time iteration.
+// individual loops of every role have a single, compile-time iteration. `atoms`:
+// 64-k swizzle atoms per stage (1 or 2).
 template <int MH, bool kW, bool kY, bool kHook, int kKind = kUniform>
 cudaError_t launch_typed(const CUtensorMap& xmap, const CUtensorMap& wmap, const TcParams& p,
-                         int grid, size_t smem, cudaStream_t stream) {
+                         int atoms, int grid, size_t smem, cudaStream_t stream) {
+  if (atoms == 2) {
+    if (p.g == 1 && !kHook)
+      return launch_kernel<MH, kW, kY, kHook, kKind, true, 2>(xmap, wmap, p, grid, smem, stream);
+    return launch_kernel<MH, kW, kY, kHook, kKind, false, 2>(xmap, wmap, p, grid, smem, stream);
+  }
   if (p.g == 1 && !kHook)
-    return launch_kernel<MH, kW, kY, kHook, kKind, true>(xmap, wmap, p, grid, smem, stream);
-  return launch_kernel<MH, kW, kY, kHook, kKind, false>(xmap, wmap, p, grid, smem, stream);
+    return launch_kernel<MH, kW, kY, kHook, kKind, true, 1>(xmap, wmap, p, grid, smem, stream);
+  return launch_kernel<MH, kW, kY, kHook, kKind, false, 1>(xmap, wmap, p, grid, smem, stream);
 }
 
 }  // namespace
@@ -781,21 +834,40 @@ cudaError_t launch_linear_tc_hook(const LinearArgs& a, cudaStream_t stream, long
   p.nt = static_cast<int>(nt);
   p.g = g;
   p.nbuf = (static_cast<int64_t>(g) * mh * nt <= kTmemCols / 2) ? 2 : 1;
-  p.a_bytes = static_cast<uint32_t>(mh) * kHalfBytes;
-  p.stage_bytes = p.a_bytes + static_cast<uint32_t>(nt) * 128u;
-  p.w_bytes = 128u * static_cast<uint32_t>(kKC) * (wbf ? 2u : 4u);
   // alignment slack + barriers (at most 8 stages) + TMEM address + wait control
   const size_t fixed = 1024 + 8 * (3 * 8 + 9) + 8 + 16;
-  const int stages = static_cast<int>(std::min<int64_t>(
-      8, (static_cast<int64_t>(dev.smem_optin) - static_cast<int64_t>(fixed) -
-          2 * static_cast<int64_t>(p.w_bytes)) / p.stage_bytes));
+  // Stage shape: two 64-k atoms per stage (32 elements per hashing thread per
+  // stage) with a ring of two W tiles, else with one W tile, else one atom per
+  // stage with two W tiles -- the first that leaves room for two stages.
+  const uint32_t welem = wbf ? 2u : 4u;
+  int atoms = 0, w_slots = 0, stages = 0;
+  static const int kPlans[3][2] = {{2, 2}, {2, 1}, {1, 2}};  // {atoms, W slots}
+  for (const auto& c : kPlans) {
+    const int64_t stage = static_cast<int64_t>(c[0]) * (static_cast<int64_t>(mh) * kHalfBytes + nt * 128);
+    const int64_t wtile = 128 * static_cast<int64_t>(kAtomK) * c[0] * welem;
+    const int64_t st = std::min<int64_t>(
+        8, (static_cast<int64_t>(dev.smem_optin) - static_cast<int64_t>(fixed) - c[1] * wtile) / stage);
+    if (st >= 2) {
+      atoms = c[0];
+      w_slots = c[1];
+      stages = static_cast<int>(st);
+      break;
+    }
+  }
   if (stages < 2) return cudaErrorInvalidConfiguration;
+  const int kc_len = kAtomK * atoms;
+  p.x_atom_bytes = static_cast<uint32_t>(nt) * 128u;
+  p.a_bytes = static_cast<uint32_t>(atoms * mh) * kHalfBytes;
+  p.stage_bytes = p.a_bytes + static_cast<uint32_t>(atoms) * p.x_atom_bytes;
+  p.w_bytes = 128u * static_cast<uint32_t>(kc_len) * welem;
+  p.w_slots = w_slots;
   p.stages = stages;
-  p.k_chunks = static_cast<int>((a.in + kKC - 1) / kKC);
+  p.k_chunks = static_cast<int>((a.in + kc_len - 1) / kc_len);
   p.m_tiles = (a.out + 128 * mh - 1) / (128 * mh);
   p.n_tiles = (a.batch + nt - 1) / nt;
   const int64_t groups = (a.pop + g - 1) / g;
   p.units = groups * p.n_tiles * p.m_tiles;
+  p.units32 = (p.units + dev.sm_count) <= 0xFFFFFFFFll ? 1 : 0;
   p.x_shared = a.x_shared;
   p.timeout_ns = timeout_ns;
   p.g_lo = kGammaLo;
@@ -807,14 +879,15 @@ cudaError_t launch_linear_tc_hook(const LinearArgs& a, cudaStream_t stream, long
   p.idesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(nt >> 3) << 17) |
             (static_cast<uint32_t>(128 >> 4) << 24);
 
-  // X as a 3-D tensor [pop or 1][batch][in] of bf16; box = 64 k x nt rows x 1.
+  // X as a 3-D tensor [pop or 1][batch][in] of bf16; box = 64 k (one swizzle atom)
+  // x nt rows x 1.
   CUtensorMap xmap;
   std::memset(&xmap, 0, sizeof(xmap));
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(a.in), static_cast<cuuint64_t>(a.batch),
                               static_cast<cuuint64_t>(a.x_shared ? 1 : a.pop)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(a.in) * 2,
                                  static_cast<cuuint64_t>(a.in) * 2 * static_cast<cuuint64_t>(a.batch)};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kKC), static_cast<cuuint32_t>(nt), 1};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(kAtomK), static_cast<cuuint32_t>(nt), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUresult cr = encode(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.x),
                              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -822,14 +895,14 @@ cudaError_t launch_linear_tc_hook(const LinearArgs& a, cudaStream_t stream, long
                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
 
-  // W as a 2-D tensor [out][in] of its dtype; box = 64 k x 128 rows, no
+  // W as a 2-D tensor [out][in] of its dtype; box = 64 * atoms k x 128 rows, no
   // swizzle (the hashing warps read it with plain shared loads). Rows >= out
   // and k >= in arrive as zeros.
   CUtensorMap wmap;
   std::memset(&wmap, 0, sizeof(wmap));
   const cuuint64_t wdims[2] = {static_cast<cuuint64_t>(a.in), static_cast<cuuint64_t>(a.out)};
   const cuuint64_t wstrides[1] = {static_cast<cuuint64_t>(a.in) * (wbf ? 2 : 4)};
-  const cuuint32_t wbox[2] = {static_cast<cuuint32_t>(kKC), 128};
+  const cuuint32_t wbox[2] = {static_cast<cuuint32_t>(kc_len), 128};
   const cuuint32_t westr[2] = {1, 1};
   const CUresult wr = encode(&wmap,
                              wbf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
@@ -838,26 +911,27 @@ cudaError_t launch_linear_tc_hook(const LinearArgs& a, cudaStream_t stream, long
                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (wr != CUDA_SUCCESS) return cudaErrorInvalidValue;
 
-  const size_t smem = fixed + static_cast<size_t>(stages) * p.stage_bytes + 2 * p.w_bytes;
+  const size_t smem = fixed + static_cast<size_t>(stages) * p.stage_bytes +
+                      static_cast<size_t>(w_slots) * p.w_bytes;
   const int grid = static_cast<int>(std::min<int64_t>(p.units, dev.sm_count));
   const bool ybf = a.y_dt == VN_BF16;
   if (withhold_stage >= 0) {
     // The test hook has one instance: bf16 W and Y.
     if (!(wbf && ybf)) return cudaErrorInvalidValue;
-    return launch_typed<1, true, true, true>(xmap, wmap, p, grid, smem, stream);
+    return launch_typed<1, true, true, true>(xmap, wmap, p, atoms, grid, smem, stream);
   }
   if (a.kind == kGaussian) {
     if (wbf) {
-      return ybf ? launch_typed<1, true, true, false, kGaussian>(xmap, wmap, p, grid, smem, stream)
-                 : launch_typed<1, true, false, false, kGaussian>(xmap, wmap, p, grid, smem, stream);
+      return ybf ? launch_typed<1, true, true, false, kGaussian>(xmap, wmap, p, atoms, grid, smem, stream)
+                 : launch_typed<1, true, false, false, kGaussian>(xmap, wmap, p, atoms, grid, smem, stream);
     }
-    return launch_typed<1, false, false, false, kGaussian>(xmap, wmap, p, grid, smem, stream);
+    return launch_typed<1, false, false, false, kGaussian>(xmap, wmap, p, atoms, grid, smem, stream);
   }
   if (wbf) {
-    return ybf ? launch_typed<1, true, true, false>(xmap, wmap, p, grid, smem, stream)
-               : launch_typed<1, true, false, false>(xmap, wmap, p, grid, smem, stream);
+    return ybf ? launch_typed<1, true, true, false>(xmap, wmap, p, atoms, grid, smem, stream)
+               : launch_typed<1, true, false, false>(xmap, wmap, p, atoms, grid, smem, stream);
   }
-  return launch_typed<1, false, false, false>(xmap, wmap, p, grid, smem, stream);
+  return launch_typed<1, false, false, false>(xmap, wmap, p, atoms, grid, smem, stream);
 }
 
 cudaError_t take_device_status(unsigned int* status, cudaStream_t stream) {
