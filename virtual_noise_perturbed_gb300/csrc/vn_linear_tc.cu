@@ -288,6 +288,17 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+// One output value, streamed to Y as bf16 (round to nearest even) or fp32.
+template <bool kYBf16, typename YT>
+__device__ __forceinline__ void store_y(YT* dst, float val) {
+  if constexpr (kYBf16) {
+    const __nv_bfloat16 hv = __float2bfloat16_rn(val);
+    __stcs(dst, *reinterpret_cast<const unsigned short*>(&hv));
+  } else {
+    __stcs(dst, val);
+  }
+}
+
 // W elements of one 16-byte output chunk (8 k): fp32 (two float4) or bf16 (one uint4).
 struct RawF32 { float4 a, b; };
 struct RawBf16 { uint4 a; };
@@ -548,16 +559,20 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
             tmem_wait_ld();
             if (jok) {
               const int valid = n_left - c0;  // columns of this group that are batch rows
+              // The epilogue warps share the schedulers with the hashing warps, so the
+              // common case (all 16 columns are batch rows, no activation) is one
+              // straight run of adds, conversions and stores; the activation and the
+              // ragged last group take the general loop.
+              if (valid >= 16 && !tanh_act) {
 #pragma unroll
-              for (int q = 0; q < 16; ++q) {
-                if (q < valid) {
-                  float val = __uint_as_float(v[q]) + bias;
-                  if (tanh_act) val = tanhf(val);
-                  if constexpr (kYBf16) {
-                    const __nv_bfloat16 hv = __float2bfloat16_rn(val);
-                    __stcs(yrow + q * ystride, *reinterpret_cast<const unsigned short*>(&hv));
-                  } else {
-                    __stcs(yrow + q * ystride, val);
+                for (int q = 0; q < 16; ++q) store_y<kYBf16>(yrow + q * ystride, __uint_as_float(v[q]) + bias);
+              } else {
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                  if (q < valid) {
+                    float val = __uint_as_float(v[q]) + bias;
+                    if (tanh_act) val = tanhf(val);
+                    store_y<kYBf16>(yrow + q * ystride, val);
                   }
                 }
               }
