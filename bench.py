@@ -93,6 +93,7 @@ ALU_LANES_PER_SM = 64             # integer ALU pipe: 16 lanes per scheduler, 4 
 ISSUE_LANES_PER_SM = 128          # 4 schedulers x 32 lanes, one instruction per clock each
 L2_FLUSH_BYTES = 256 << 20
 ES_LR = 0.01                      # learning rate of the bench's parameter update
+E2E_SETS = 3                      # device buffer sets the e2e loop rotates through
 
 
 def peaks():
@@ -952,16 +953,19 @@ def run_e2e(wl, dev, stream, steps, world, el_step, noise, include_dump=True):
     """The same step through the C ABI with inputs in pinned host memory: each step
     copies its inputs host -> device, runs, and copies every result back.
 
-    Two sets of device buffers alternate between steps, and the copies run on
+    Three sets of device buffers rotate between steps, and the copies run on
     streams of their own, so that step k+1's host->device copy and step k-1's
     device->host copy overlap step k's kernels (the two copy directions use
     separate engines). A set's inputs are rewritten only after the kernels that
-    read them have finished, and its outputs only after they have reached the host."""
+    read them have finished, and its outputs only after they have reached the host;
+    with three sets that waits on step k-2, so neither copy direction has to wait for
+    the other (with two, step k+1's inputs would wait for step k-1's results to reach
+    the host)."""
     import torch
     copy_stream = torch.cuda.Stream(dev)   # device -> host
     load_stream = torch.cuda.Stream(dev)   # host -> device
     sets = []
-    for _ in range(2):
+    for _ in range(E2E_SETS):
         launches, bufs, outputs = build_step(wl, dev, stream.cuda_stream, noise, include_dump)
         sets.append((launches, bufs, outputs))
     host_in = {k: v.detach().cpu().pin_memory() for k, v in sets[0][1].items()
@@ -974,31 +978,32 @@ def run_e2e(wl, dev, stream, steps, world, el_step, noise, include_dump=True):
     copied = [torch.cuda.Event() for _ in sets]
 
     def one(k):
-        launches, bufs, outputs = sets[k % 2]
+        j = k % E2E_SETS
+        launches, bufs, outputs = sets[j]
         with torch.cuda.stream(load_stream):
-            load_stream.wait_event(computed[k % 2])   # the kernels that read this set are done
-            load_stream.wait_event(copied[k % 2])     # and its results (theta is both) are out
+            load_stream.wait_event(computed[j])   # the kernels that read this set are done
+            load_stream.wait_event(copied[j])     # and its results (theta is both) are out
             for name, v in host_in.items():
                 bufs[name].copy_(v, non_blocking=True)
-            loaded[k % 2].record(load_stream)
+            loaded[j].record(load_stream)
         with torch.cuda.stream(stream):
-            stream.wait_event(loaded[k % 2])
-            stream.wait_event(copied[k % 2])          # this set's last results are on the host
+            stream.wait_event(loaded[j])
+            stream.wait_event(copied[j])          # this set's last results are on the host
             for l in launches:
                 l()
-            computed[k % 2].record(stream)
+            computed[j].record(stream)
         with torch.cuda.stream(copy_stream):
-            copy_stream.wait_event(computed[k % 2])
-            for o, h in zip(outputs, host_out[k % 2]):
+            copy_stream.wait_event(computed[j])
+            for o, h in zip(outputs, host_out[j]):
                 h.copy_(o, non_blocking=True)
-            copied[k % 2].record(copy_stream)
+            copied[j].record(copy_stream)
 
     for e in computed:
         e.record(stream)
     for c in copied:
         c.record(copy_stream)
-    one(0)
-    one(1)
+    for k in range(E2E_SETS):
+        one(k)
     torch.cuda.synchronize(dev)
     barrier(world)
     a = torch.cuda.Event(enable_timing=True)
@@ -1017,8 +1022,8 @@ def run_e2e(wl, dev, stream, steps, world, el_step, noise, include_dump=True):
     link["frac"] = link["bound_ms_per_step"] / (ms / steps)
     return {"value": el_step * steps * world / (ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": ms / steps,
-            "copies": "step k+1's inputs copied in and step k-1's results copied back on streams "
-                      "of their own while step k runs", "host_link": link}
+            "copies": f"step k+1's inputs copied in and step k-1's results copied back on streams "
+                      f"of their own while step k runs ({E2E_SETS} rotating buffer sets)", "host_link": link}
 
 
 def host_link(step_set, host_in, host_out, load_stream, copy_stream, dev, reps=5):
