@@ -94,3 +94,43 @@ def test_roofline_picks_the_tightest_bound():
     # a contraction with few elements and many flops: the tensor pipe binds
     r = bench.roofline_of({"linear_tc": _k(1.0, 1, 10 ** 6, flops=1.5e12)}, PK, "x")
     assert r["bound"] == "tensor" and abs(r["achieved"] - 1500.0) < 1e-9
+
+
+def test_summary_of_a_measured_workload():
+    """summarise(): value from the step pass over the max-over-ranks time, the dominant
+    kernel's roofline, shares and the phase metrics from the kernel pass."""
+    wl = workloads.make(3)
+    el_fwd = 4096 * 1024 * 1024
+    per_kernel = {"linear_tc": _k(41.3, 10, el_fwd * 10, 2.0 * el_fwd * 32 * 10),
+                  "grad": _k(33.6, 20, 4096 * (1024 * 1024 + 1024) * 10)}
+    per_kernel["grad"]["grad_w_elems"] = 1024 * 1024 * 10
+    per_kernel["linear_tc"]["grad_w_elems"] = 0
+    res = {"per_kernel": per_kernel, "el_step": bench.step_elements(wl), "steps": 10, "total_ms_max": 75.0,
+           "graph": True, "graph_error": None}
+    s = bench.summarise(wl, res, 1, PK)
+    assert abs(s["value"] - bench.step_elements(wl) * 10 / 75e-3) < 1.0
+    assert abs(s["ms_per_step"] - 7.5) < 1e-12 and s["steps"] == 10
+    assert s["roofline"]["kernel"] == "linear_tc" and s["roofline"]["bound"] == "alu"
+    assert abs(sum(k["share"] for k in s["kernels"].values()) - 1.0) < 1e-12
+    assert abs(s["perturbed_linear_tflops"] - 2.0 * el_fwd * 32 * 10 / 41.3e-3 / 1e12) < 1e-9
+    assert abs(s["grad_w_elem_per_s"] - 1024 * 1024 * 10 / 33.6e-3) < 1e-3
+    assert "CUDA graph" in s["launch"]
+
+
+def test_measured_ceiling_sits_beside_the_derived_peak():
+    r = bench.roofline_of({"grad": _k(1.0, 1, 10 ** 9)}, PK, "x")
+    hp = {"tops": 16.4}
+    bench.with_measured_peak(r, hp)
+    assert r["peak"] == PK["alu_ops"] / 1e12                       # the derived peak stays the peak
+    assert r["peak_measured"] == 16.4 and abs(r["frac_of_measured"] - r["achieved"] / 16.4) < 1e-12
+    h = bench.roofline_of({"noise_dump": _k(1.0, 1, 10 ** 9, hbm_bytes=4e9)}, PK, "x")
+    bench.with_measured_peak(h, hp)
+    assert "peak_measured" not in h                                 # only alu-bound rooflines
+    bench.with_measured_peak(r, None)                               # no probe run: unchanged
+
+
+def test_default_extras_and_refusals():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--extras", "mid,nope"],
+                         capture_output=True, text=True, timeout=120, cwd=ROOT)
+    assert out.returncode != 0 and "nope" in out.stderr
+    assert bench.EXTRA_DEFAULT == ["mid", "grad_only", "es_mlp", "tiny"]
