@@ -181,6 +181,10 @@ TC_CASES = [
     (2, 256, 128, 256, torch.bfloat16, False, True),   # N=256, two 128-row halves per unit
     (1, 300, 64, 160, torch.bfloat16, False, True),    # batch > 256: two N tiles
     (20, 24, 1032, 40, torch.float32, False, True),    # many k chunks, ragged last chunk
+    # Stage shapes (two 64-k atoms per stage unless they do not fit beside the W ring):
+    # the cases above take two atoms with two W tiles (batch <= 128) or one W tile
+    # (batch 256, bf16 W); fp32 W with a batch above 128 takes one-atom stages.
+    (2, 200, 96, 130, torch.float32, False, True),     # fp32 W, N=208: one-atom stages, ragged K and out
 ]
 
 
