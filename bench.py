@@ -826,7 +826,7 @@ def main(argv=None) -> int:
                     help="run only the headline workload's first POP individuals (smaller profiling cases)")
     ap.add_argument("--noise", choices=["uniform", "gaussian"], default="uniform",
                     help="gaussian: the Box-Muller noise variant throughout (not on the tiny workload)")
-    ap.add_argument("--cpu-baseline-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-baseline-seconds", type=float, default=16.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-hash-peak", action="store_true")
     args = ap.parse_args(argv)
