@@ -185,6 +185,13 @@ TC_CASES = [
     # the cases above take two atoms with two W tiles (batch <= 128) or one W tile
     # (batch 256, bf16 W); fp32 W with a batch above 128 takes one-atom stages.
     (2, 200, 96, 130, torch.float32, False, True),     # fp32 W, N=208: one-atom stages, ragged K and out
+    # bf16 W with a batch above 192: two stages beside one W tile. An even number
+    # of k chunks takes the instance with compile-time stage slots, an odd one the
+    # general ring.
+    (3, 200, 512, 200, torch.bfloat16, False, True),   # even (4 chunks), ragged batch and out
+    (2, 200, 392, 130, torch.bfloat16, False, True),   # even (4 chunks), ragged last k chunk
+    (3, 200, 384, 200, torch.bfloat16, False, True),   # odd (3 chunks): the general ring
+    (160, 200, 256, 128, torch.bfloat16, False, True), # even, 160 units on 152 CTAs: parity across units
 ]
 
 

@@ -359,7 +359,10 @@ __device__ __forceinline__ Unit decode(const TcParams& p, int64_t u, int mh) {
 // the ordinary instances carry no trace of it. kAtoms: swizzle atoms of 64 k per
 // stage (K = 64 * kAtoms); two give every hashing thread 32 elements per stage,
 // so each stage's waits, fences and arrivals are paid once per 32 elements.
-template <int MH, bool kWBf16, bool kYBf16, bool kHook, int kKind, bool kG1, int kAtoms>
+// kFix: two stages and one W tile with an even number of k chunks per unit (one
+// individual per unit): the hashing warps then address both stages and the W
+// tile with compile-time offsets and carry a single parity bit.
+template <int MH, bool kWBf16, bool kYBf16, bool kHook, int kKind, bool kG1, int kAtoms, bool kFix>
 __global__ void __launch_bounds__(kThreads, 1)
 linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
                  const TcParams p) {
@@ -636,6 +639,8 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
     };
     // State term step from one k chunk to the next: kKC * GAMMA mod 2^64.
     constexpr uint64_t kChunkStep = static_cast<uint64_t>(kKC) * kGamma;
+    // From a chunk's last element (k + 7) to the next k chunk's first (k + kKC).
+    constexpr uint64_t kChunkHop = static_cast<uint64_t>(kKC - 7) * kGamma;
 
     // Ring positions (slot, parity) of the stages and of the W tiles; barrier
     // addresses are formed from them directly.
@@ -656,8 +661,10 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
       const int64_t* seedp = p.seeds + un.i0;
       // (offset + j*in + k + 1) * GAMMA of each chunk's first element, k chunk 0;
       // advanced by kChunkStep per k chunk. With one individual per unit its seed
-      // is added here once, so a stage's chunks start from bst directly.
+      // is added here once, and the halves blo:bhi carry each chunk's state chain
+      // from one k chunk to the next.
       uint64_t bst[kCPT][kAtoms];
+      uint32_t blo[kCPT][kAtoms], bhi[kCPT][kAtoms];
       const uint64_t seed0 = kG1 ? static_cast<uint64_t>(__ldg(seedp)) : 0ull;
 #pragma unroll
       for (int q = 0; q < kCPT; ++q) {
@@ -667,89 +674,144 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant
                                          static_cast<uint64_t>(un.m0 + rowq(q)) *
                                              static_cast<uint64_t>(p.in) +
                                          static_cast<uint64_t>(a * kAtomK + cc * 8));
+          blo[q][a] = static_cast<uint32_t>(bst[q][a]);
+          bhi[q][a] = static_cast<uint32_t>(bst[q][a] >> 32);
         }
       }
-      for (int kc = 0; kc < k_chunks; ++kc) {
-        // This stage group's W chunks, shared by its G individuals: fp32 W is
-        // kept as W - 1.5*sigma and perturbed with one FMA per element; bf16 W
-        // stays packed and each element is formed as fp32(bf16 W) + sigma*n
-        // with one mixed-precision add (no unpacking on the integer pipe).
-        // Chunks outside the matrix (row >= out or k >= in, only
-        // at ragged edges) are TMA's zero fill, so their values are finite:
-        // their X columns are zero fill too (k >= in) or their output rows are
-        // never stored (row >= out), and no masking is needed below.
-        if (!mbar_wait(fw0 + 8u * ws, wph, s_abort)) goto hashing_done;
-        float wm[kCPT][kAtoms][8];
-        Raw wraw[kCPT][kAtoms];
-        {
-          const uint32_t wb = w_this + ws * w_bytes;
-#pragma unroll
-          for (int q = 0; q < kCPT; ++q) {
-#pragma unroll
-            for (int a = 0; a < kAtoms; ++a) {
-              load_w(wb + woff(q, a) - woff(0, 0), wraw[q][a]);
-              if constexpr (!kWBf16) unpack_shift(wraw[q][a], shift, wm[q][a]);
-            }
-          }
-        }
-        // The slot's next tile is written by TMA (the async proxy): order this
-        // thread's generic-proxy reads of it before that write. Without the
-        // fence a late warp's reads could return the next tile's values.
-        fence_proxy_async_smem();
-        mbar_arrive(ew0 + 8u * ws);
-        if (++ws == w_slots) { ws = 0; wph ^= 1u; }
-        for (int ii = 0; ii < (kG1 ? 1 : un.gcount); ++ii) {
-          const uint64_t seed = kG1 ? 0ull : static_cast<uint64_t>(__ldg(seedp + ii));
-          if (!mbar_wait(em0 + 8u * s, ph ^ 1u, s_abort)) goto hashing_done;
-          const uint32_t a0 = a_this + s * stage_bytes;
-#pragma unroll
-          for (int q = 0; q < kCPT; ++q) {
-#pragma unroll
-            for (int a = 0; a < kAtoms; ++a) {
-              const uint64_t st0 = bst[q][a] + seed;
-              uint32_t slo = static_cast<uint32_t>(st0), shi = static_cast<uint32_t>(st0 >> 32);
-              float pv[8];
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                // The element's noise term: the uniform kind as 1 + u (its -1.5 rides on
-                // the shift), the Gaussian kind as the unit Box-Muller value.
-                float unit;
-                if constexpr (kKind == kGaussian) {
-                  uint32_t zlo, zhi;
-                  mix64_halves(slo, shi, zlo, zhi);
-                  unit = gaussian_unit(zlo, zhi);
-                } else {
-                  unit = __uint_as_float(mix_to_one_plus_u(slo, shi));
-                }
-                if constexpr (kWBf16) {
-                  // sigma*n = fma(sigma, 1 + u, -1.5*sigma), then + W straight from its bf16 bits.
-                  const float tt = fmaf(sigma_unit, unit, shift);
-                  const uint32_t wv = (e & 4) ? ((e & 2) ? wraw[q][a].a.w : wraw[q][a].a.z)
-                                              : ((e & 2) ? wraw[q][a].a.y : wraw[q][a].a.x);
-                  pv[e] = (e & 1) ? add_bf16_f32<true>(wv, tt) : add_bf16_f32<false>(wv, tt);
-                } else {
-                  pv[e] = fmaf(sigma_unit, unit, wm[q][a][e]);
-                }
-                add64_madc(slo, shi, g_lo, g_hi, one);
-              }
-              st_shared_v4(a0 + soff(q, a) - soff(0, 0), pack_bf16x2(pv[0], pv[1]),
-                           pack_bf16x2(pv[2], pv[3]), pack_bf16x2(pv[4], pv[5]),
-                           pack_bf16x2(pv[6], pv[7]));
-            }
-          }
-          fence_proxy_async_smem();
-          if constexpr (kHook) {
-            if (withhold_at != 0) mbar_arrive(fa0 + 8u * s);
-            if (withhold_at >= 0) --withhold_at;
-          } else {
-            mbar_arrive(fa0 + 8u * s);
-          }
-          if (++s == S32) { s = 0; ph ^= 1u; }
-        }
+      // This thread's chunks of a staged W tile (wb: its first one). fp32 W is
+      // kept as W - 1.5*sigma and perturbed with one FMA per element; bf16 W
+      // stays packed and each element is formed as fp32(bf16 W) + sigma*n with
+      // one mixed-precision add (no unpacking on the integer pipe). Chunks
+      // outside the matrix (row >= out or k >= in, only at ragged edges) are
+      // TMA's zero fill, so their values are finite: their X columns are zero
+      // fill too (k >= in) or their output rows are never stored (row >= out),
+      // and no masking is needed below.
+      auto load_stage_w = [&](uint32_t wb, Raw (&wraw)[kCPT][kAtoms], float (&wm)[kCPT][kAtoms][8]) {
 #pragma unroll
         for (int q = 0; q < kCPT; ++q) {
 #pragma unroll
-          for (int a = 0; a < kAtoms; ++a) bst[q][a] += kChunkStep;
+          for (int a = 0; a < kAtoms; ++a) {
+            load_w(wb + woff(q, a) - woff(0, 0), wraw[q][a]);
+            if constexpr (!kWBf16) unpack_shift(wraw[q][a], shift, wm[q][a]);
+          }
+        }
+      };
+      // One stage of one individual: W'_i of this thread's chunks, packed to
+      // bf16 and stored to the A tile whose chunk for this thread is at a0.
+      auto hash_stage = [&](uint32_t a0, uint64_t seed, const Raw (&wraw)[kCPT][kAtoms],
+                            const float (&wm)[kCPT][kAtoms][8]) {
+#pragma unroll
+        for (int q = 0; q < kCPT; ++q) {
+#pragma unroll
+          for (int a = 0; a < kAtoms; ++a) {
+            // One individual per unit: the chunk's state chain runs in place in
+            // blo:bhi, and the step after its last element adds (kKC - 7) * GAMMA,
+            // which lands on the next k chunk's first. Otherwise each individual
+            // starts from bst + seed.
+            uint32_t slo, shi;
+            if constexpr (kG1) {
+              slo = blo[q][a];
+              shi = bhi[q][a];
+            } else {
+              const uint64_t st0 = bst[q][a] + seed;
+              slo = static_cast<uint32_t>(st0);
+              shi = static_cast<uint32_t>(st0 >> 32);
+            }
+            float pv[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              // The element's noise term: the uniform kind as 1 + u (its -1.5 rides on
+              // the shift), the Gaussian kind as the unit Box-Muller value.
+              float unit;
+              if constexpr (kKind == kGaussian) {
+                uint32_t zlo, zhi;
+                mix64_halves(slo, shi, zlo, zhi);
+                unit = gaussian_unit(zlo, zhi);
+              } else {
+                unit = __uint_as_float(mix_to_one_plus_u(slo, shi));
+              }
+              if constexpr (kWBf16) {
+                // sigma*n = fma(sigma, 1 + u, -1.5*sigma), then + W straight from its bf16 bits.
+                const float tt = fmaf(sigma_unit, unit, shift);
+                const uint32_t wv = (e & 4) ? ((e & 2) ? wraw[q][a].a.w : wraw[q][a].a.z)
+                                            : ((e & 2) ? wraw[q][a].a.y : wraw[q][a].a.x);
+                pv[e] = (e & 1) ? add_bf16_f32<true>(wv, tt) : add_bf16_f32<false>(wv, tt);
+              } else {
+                pv[e] = fmaf(sigma_unit, unit, wm[q][a][e]);
+              }
+              if (e < 7)
+                add64_madc(slo, shi, g_lo, g_hi, one);
+              else if constexpr (kG1)
+                add64_madc(slo, shi, static_cast<uint32_t>(kChunkHop),
+                           static_cast<uint32_t>(kChunkHop >> 32), one);
+            }
+            if constexpr (kG1) {
+              blo[q][a] = slo;
+              bhi[q][a] = shi;
+            }
+            st_shared_v4(a0 + soff(q, a) - soff(0, 0), pack_bf16x2(pv[0], pv[1]),
+                         pack_bf16x2(pv[2], pv[3]), pack_bf16x2(pv[4], pv[5]),
+                         pack_bf16x2(pv[6], pv[7]));
+          }
+        }
+      };
+
+      if constexpr (kFix) {
+        // Two stages, one W tile, an even number of k chunks per unit: every
+        // unit starts on stage 0 with W parity 0, so within a pair of k chunks
+        // the stage slot and the W parity are both h, and only the stage
+        // parity (flipped once per pair) is carried.
+        for (int kc = 0; kc < k_chunks; kc += 2) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            if (!mbar_wait(fw0, static_cast<uint32_t>(h), s_abort)) goto hashing_done;
+            float wm[kCPT][kAtoms][8];
+            Raw wraw[kCPT][kAtoms];
+            load_stage_w(w_this, wraw, wm);
+            // The W tile is rewritten by TMA (the async proxy): order this
+            // thread's generic-proxy reads of it before that write.
+            fence_proxy_async_smem();
+            mbar_arrive(ew0);
+            if (!mbar_wait(em0 + 8u * h, ph ^ 1u, s_abort)) goto hashing_done;
+            hash_stage(h ? a_this + stage_bytes : a_this, 0ull, wraw, wm);
+            fence_proxy_async_smem();
+            mbar_arrive(fa0 + 8u * h);
+          }
+          ph ^= 1u;
+        }
+      } else {
+        for (int kc = 0; kc < k_chunks; ++kc) {
+          // This stage group's W chunks, shared by its G individuals.
+          if (!mbar_wait(fw0 + 8u * ws, wph, s_abort)) goto hashing_done;
+          float wm[kCPT][kAtoms][8];
+          Raw wraw[kCPT][kAtoms];
+          load_stage_w(w_this + ws * w_bytes, wraw, wm);
+          // The slot's next tile is written by TMA (the async proxy): order this
+          // thread's generic-proxy reads of it before that write. Without the
+          // fence a late warp's reads could return the next tile's values.
+          fence_proxy_async_smem();
+          mbar_arrive(ew0 + 8u * ws);
+          if (++ws == w_slots) { ws = 0; wph ^= 1u; }
+          for (int ii = 0; ii < (kG1 ? 1 : un.gcount); ++ii) {
+            const uint64_t seed = kG1 ? 0ull : static_cast<uint64_t>(__ldg(seedp + ii));
+            if (!mbar_wait(em0 + 8u * s, ph ^ 1u, s_abort)) goto hashing_done;
+            hash_stage(a_this + s * stage_bytes, seed, wraw, wm);
+            fence_proxy_async_smem();
+            if constexpr (kHook) {
+              if (withhold_at != 0) mbar_arrive(fa0 + 8u * s);
+              if (withhold_at >= 0) --withhold_at;
+            } else {
+              mbar_arrive(fa0 + 8u * s);
+            }
+            if (++s == S32) { s = 0; ph ^= 1u; }
+          }
+          if constexpr (!kG1) {
+#pragma unroll
+            for (int q = 0; q < kCPT; ++q) {
+#pragma unroll
+              for (int a = 0; a < kAtoms; ++a) bst[q][a] += kChunkStep;
+            }
+          }
         }
       }
     }
@@ -779,10 +841,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-template <int MH, bool kW, bool kY, bool kHook, int kKind, bool kG1, int kAtoms>
+template <int MH, bool kW, bool kY, bool kHook, int kKind, bool kG1, int kAtoms, bool kFix = false>
 cudaError_t launch_kernel(const CUtensorMap& xmap, const CUtensorMap& wmap, const TcParams& p,
                           int grid, size_t smem, cudaStream_t stream) {
-  auto fn = linear_tc_kernel<MH, kW, kY, kHook, kKind, kG1, kAtoms>;
+  auto fn = linear_tc_kernel<MH, kW, kY, kHook, kKind, kG1, kAtoms, kFix>;
   static SmemRecord configured;
   const cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(fn), smem, configured);
   if (err != cudaSuccess) return err;
@@ -797,6 +859,10 @@ template <int MH, bool kW, bool kY, bool kHook, int kKind = kUniform>
 cudaError_t launch_typed(const CUtensorMap& xmap, const CUtensorMap& wmap, const TcParams& p,
                          int atoms, int grid, size_t smem, cudaStream_t stream) {
   if (atoms == 2) {
+    if constexpr (kW && !kHook) {
+      if (p.g == 1 && p.stages == 2 && p.w_slots == 1 && p.k_chunks % 2 == 0)
+        return launch_kernel<MH, kW, kY, kHook, kKind, true, 2, true>(xmap, wmap, p, grid, smem, stream);
+    }
     if (p.g == 1 && !kHook)
       return launch_kernel<MH, kW, kY, kHook, kKind, true, 2>(xmap, wmap, p, grid, smem, stream);
     return launch_kernel<MH, kW, kY, kHook, kKind, false, 2>(xmap, wmap, p, grid, smem, stream);

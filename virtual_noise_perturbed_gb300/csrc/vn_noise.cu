@@ -29,6 +29,8 @@ constexpr int64_t kDumpStride = kDumpThreads * 4;               // columns betwe
 constexpr int64_t kDumpChunk = kDumpStride * kDumpGroups;       // elements per CTA step
 // GAMMA * kDumpStride mod 2^64: the state difference between a thread's consecutive groups.
 constexpr uint64_t kDumpStep = kGamma * static_cast<uint64_t>(kDumpStride);
+// GAMMA * (kDumpStride - 3): from a group's last element to the next group's first.
+constexpr uint64_t kDumpGroupHop = kGamma * static_cast<uint64_t>(kDumpStride - 3);
 
 // Grid-stride over (row i, chunk of kDumpChunk columns). Thread t makes the
 // 4-element groups at columns c + 4t + 1024g, g < 8: one 16-byte store per group,
@@ -65,19 +67,23 @@ noise_dump_kernel(const int64_t* __restrict__ seeds, int64_t n, uint64_t offset,
     float* row = out + i * n;
     uint64_t gst = index_term(offset + static_cast<uint64_t>(t0)) + seed;  // first element of the group
     if (vec4 && t0 - threadIdx.x * 4 + kDumpChunk <= n) {
-      // The whole chunk lies inside the row: no per-group checks.
+      // The whole chunk lies inside the row: no per-group checks. One state chain
+      // runs through the thread's groups: the step after a group's last element
+      // adds (kDumpStride - 3) * GAMMA, which lands on the next group's first.
+      uint32_t slo = static_cast<uint32_t>(gst), shi = static_cast<uint32_t>(gst >> 32);
 #pragma unroll
       for (int g = 0; g < kDumpGroups; ++g) {
-        uint32_t slo = static_cast<uint32_t>(gst), shi = static_cast<uint32_t>(gst >> 32);
         float v[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           v[q] = dump_value<kKind>((static_cast<uint64_t>(shi) << 32) | slo);
-          add64_madc(slo, shi, g_lo, g_hi, one);
+          if (q < 3)
+            add64_madc(slo, shi, g_lo, g_hi, one);
+          else if (g + 1 < kDumpGroups)
+            add64_madc(slo, shi, static_cast<uint32_t>(kDumpGroupHop), static_cast<uint32_t>(kDumpGroupHop >> 32), one);
         }
         __stcs(reinterpret_cast<float4*>(row + t0 + g * kDumpStride),
                make_float4(v[0], v[1], v[2], v[3]));
-        gst += kDumpStep;
       }
       continue;
     }
