@@ -141,22 +141,14 @@ def round_bf16(a) -> np.ndarray:
 
 def perturbed_linear_bf16(x, weight, bias, seeds, sigma: float, offset: int,
                           individuals: Optional[Iterable[int]] = None,
-                          rows: Optional[Iterable[int]] = None, round_y: bool = False,
-                          split: bool = False) -> np.ndarray:
-    """The bf16 models of the tensor-core forward: ``perturbed_linear`` with the perturbed
+                          rows: Optional[Iterable[int]] = None, round_y: bool = False) -> np.ndarray:
+    """The bf16 model of the tensor-core forward: ``perturbed_linear`` with the perturbed
     weight ``W + sigma*N_i`` rounded to bfloat16 (``round_bf16``) before the product and,
     with ``round_y``, the output (after the bias) rounded to bfloat16 too. Everything else
     is float64 from the exact inputs (bf16 X values are exact in float64), so the model
-    differs from ``perturbed_linear`` by those two roundings alone.
-
-    ``split``: the perturbed weight kept as the sum of two bfloat16 operands, the weight
-    itself (whose values must already be bfloat16 values; raises otherwise) and the
-    perturbation rounded alone, ``W + bf16(sigma*N_i)``; only the perturbation and, with
-    ``round_y``, the output are rounded."""
+    differs from ``perturbed_linear`` by those two roundings alone."""
     w = np.asarray(weight, dtype=np.float64)
     out_f, in_f = w.shape
-    if split and not np.array_equal(round_bf16(w), w):
-        raise ValueError("perturbed_linear_bf16(split=True): the weight is not bfloat16-valued")
     x = np.asarray(x, dtype=np.float64)
     s = np.asarray(seeds)
     pop = s.shape[0]
@@ -169,10 +161,7 @@ def perturbed_linear_bf16(x, weight, bias, seeds, sigma: float, offset: int,
     y = np.empty((len(inds), x.shape[-2], len(rows)), dtype=np.float64)
     for r, i in enumerate(inds):
         n_i = weight_noise(s[i], out_f, in_f, offset, rows)
-        if split:
-            w_pert = w[rows] + round_bf16(sigma * n_i)                # W + bf16(sigma*N_i)
-        else:
-            w_pert = round_bf16(w[rows] + sigma * n_i)                # bf16(W + sigma*N_i)
+        w_pert = round_bf16(w[rows] + sigma * n_i)                    # bf16(W + sigma*N_i)
         xi = x if shared else x[i]
         yi = xi @ w_pert.T
         if b is not None:
@@ -183,15 +172,14 @@ def perturbed_linear_bf16(x, weight, bias, seeds, sigma: float, offset: int,
 
 
 def bf16_floor(x, weight, bias, seeds, sigma: float, offset: int,
-               individuals: Optional[Iterable[int]] = None, round_y: bool = False,
-               split: bool = False) -> float:
+               individuals: Optional[Iterable[int]] = None, round_y: bool = False) -> float:
     """The deviation that rounding alone costs a bf16 implementation of the forward:
     max |Y_model - Y| / RMS(Y), with Y = ``perturbed_linear`` (exact up to float64) and
-    Y_model = ``perturbed_linear_bf16`` (W + sigma*N_i, or with ``split`` only sigma*N_i,
-    and Y when ``round_y``, rounded to bfloat16), on the selected individuals."""
+    Y_model = ``perturbed_linear_bf16`` (W + sigma*N_i, and Y when ``round_y``, rounded to
+    bfloat16), on the selected individuals."""
     exact = perturbed_linear(x, weight, bias, seeds, sigma, offset, individuals=individuals)
     model = perturbed_linear_bf16(x, weight, bias, seeds, sigma, offset, individuals=individuals,
-                                  round_y=round_y, split=split)
+                                  round_y=round_y)
     rms = float(np.sqrt(np.mean(exact ** 2)))
     return float(np.max(np.abs(model - exact))) / rms
 

@@ -17,7 +17,6 @@ import tests.test_oracle_pins as pins
 from oracle import es, splitmix as sm
 
 _G = np.uint64(sm.GAMMA)
-_ORIG_BF16 = es.perturbed_linear_bf16
 
 
 def _mix_wrong_shift(z):
@@ -44,19 +43,6 @@ def _round_bf16_truncating(a):
 def _bf16_model_w_unrounded(x, weight, bias, seeds, sigma, offset, individuals=None, rows=None,
                             round_y=False):
     y = es.perturbed_linear(x, weight, bias, seeds, sigma, offset, individuals=individuals, rows=rows)
-    return es.round_bf16(y) if round_y else y
-
-
-def _bf16_split_rounds_whole_weight(x, weight, bias, seeds, sigma, offset, individuals=None, rows=None,
-                                    round_y=False, split=False):
-    return _ORIG_BF16(x, weight, bias, seeds, sigma, offset, individuals, rows, round_y, split=False)
-
-
-def _bf16_split_perturbation_unrounded(x, weight, bias, seeds, sigma, offset, individuals=None, rows=None,
-                                       round_y=False, split=False):
-    if not split:
-        return _ORIG_BF16(x, weight, bias, seeds, sigma, offset, individuals, rows, round_y)
-    y = es.perturbed_linear(x, weight, bias, seeds, sigma, offset, individuals, rows)
     return es.round_bf16(y) if round_y else y
 
 
@@ -228,10 +214,6 @@ MUTATIONS = [
      pins.test_round_bf16_matches_torchs_conversion_and_ties),
     ("bf16 model leaves W' unrounded", [(es, "perturbed_linear_bf16", _bf16_model_w_unrounded)],
      pins.test_bf16_model_one_hot_reads_the_rounded_noise),
-    ("split bf16 model rounds the whole weight", [(es, "perturbed_linear_bf16", _bf16_split_rounds_whole_weight)],
-     pins.test_bf16_split_model_one_hot_reads_weight_plus_rounded_perturbation),
-    ("split bf16 model leaves sigma*N unrounded", [(es, "perturbed_linear_bf16", _bf16_split_perturbation_unrounded)],
-     pins.test_bf16_split_model_one_hot_reads_weight_plus_rounded_perturbation),
     ("finalizer shift 30 -> 29", [(sm, "mix64", _mix_wrong_shift)],
      pins.test_finalizer_inverts_with_independent_inverse),
     ("numpy finalizer shift 27 -> 28", [(sm, "mix64_np", _mix_np_wrong_shift)],

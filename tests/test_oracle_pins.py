@@ -577,63 +577,3 @@ def test_bf16_floor_is_within_the_rounding_bound():
     f_y = es.bf16_floor(x, w, b, seeds, 0.05, 3, round_y=True)
     assert 0.0 < f_w <= np.max(bound_w) / rms
     assert f_w < f_y <= np.max(bound_w * (1 + 2.0 ** -9) + 2.0 ** -9 * np.abs(exact)) / rms
-
-
-# --- the split bf16 model: the weight (bfloat16-valued) and the perturbation rounded
-# alone, W + bf16(sigma*N_i), two bfloat16 operands whose products the contraction sums
-
-def test_bf16_split_model_special_cases():
-    """sigma = 0: nothing is rounded but Y, so the split model is the exact forward; a
-    weight that is not bfloat16-valued is refused."""
-    rng = np.random.default_rng(14)
-    x = rng.standard_normal((3, 4, 24))
-    w = es.round_bf16(rng.standard_normal((10, 24)) / 5)
-    b = rng.standard_normal(10) * 0.1
-    seeds = np.array([1, 2, 3])
-    exact = es.perturbed_linear(x, w, b, seeds, 0.0, 7)
-    assert np.array_equal(es.perturbed_linear_bf16(x, w, b, seeds, 0.0, 7, split=True), exact)
-    assert np.array_equal(es.perturbed_linear_bf16(x, w, b, seeds, 0.0, 7, round_y=True, split=True),
-                          es.round_bf16(exact))
-    with pytest.raises(ValueError):
-        es.perturbed_linear_bf16(x, w + 2.0 ** -20, b, seeds, 0.1, 7, split=True)
-
-
-def test_bf16_split_model_one_hot_reads_weight_plus_rounded_perturbation():
-    """X rows one-hot at k, a nonzero bfloat16 weight, sigma = 1/4 (so sigma*N is exact in
-    float32), no bias: Y[i, r, j] = W[j, k] + bf16(sigma*N_i[j, k]) exactly, with the
-    rounding taken by torch's float32 -> bfloat16 conversion; the weight itself is not
-    rounded together with the perturbation."""
-    torch = pytest.importorskip("torch")
-    pop, in_f, out_f, off, sig = 3, 9, 13, 2 ** 33 + 1, 0.25
-    rng = np.random.default_rng(15)
-    w = torch.tensor(rng.standard_normal((out_f, in_f)) / 3, dtype=torch.bfloat16).double().numpy()
-    seeds = np.array([4, -8, 15])
-    ks = [0, 5, 8]
-    x = np.zeros((pop, len(ks), in_f))
-    for r, k in enumerate(ks):
-        x[:, r, k] = 1.0
-    y = es.perturbed_linear_bf16(x, w, None, seeds, sig, off, split=True)
-    dump = es.noise_dump(seeds, out_f * in_f, off).reshape(pop, out_f, in_f)
-    pert = torch.from_numpy((np.float32(sig) * dump).astype(np.float32)).to(torch.bfloat16).double().numpy()
-    for r, k in enumerate(ks):
-        assert np.array_equal(y[:, r, :], w[None, :, k] + pert[:, :, k])
-
-
-def test_bf16_split_floor_is_within_its_rounding_bound_and_below_the_whole_weight_rounding():
-    """Only sigma*N is rounded (relative error at most 2^-9), so the split model deviates
-    from the exact forward by at most 2^-9 * sum_k |x_k| |sigma N_jk| per output; where the
-    perturbation is small against the weight that floor is below the whole-weight model's."""
-    rng = np.random.default_rng(16)
-    x = es.round_bf16(rng.standard_normal((4, 16, 64)))
-    w = es.round_bf16(rng.standard_normal((32, 64)) / 8)
-    b = rng.standard_normal(32) * 0.1
-    seeds = np.arange(4)
-    sig = 0.05
-    exact = es.perturbed_linear(x, w, b, seeds, sig, 3)
-    rms = np.sqrt(np.mean(exact ** 2))
-    pn = np.stack([sig * es.weight_noise(s, 32, 64, 3) for s in seeds])
-    bound = 2.0 ** -9 * np.einsum("prk,pjk->prj", np.abs(x), np.abs(pn))
-    f_split = es.bf16_floor(x, w, b, seeds, sig, 3, split=True)
-    f_whole = es.bf16_floor(x, w, b, seeds, sig, 3)
-    assert 0.0 < f_split <= np.max(bound) / rms
-    assert f_split < f_whole
