@@ -221,6 +221,25 @@ def test_tc_forward_one_hot_reads_bf16_noise_exactly():
         assert torch.equal(y[i].cpu(), want)
 
 
+@pytest.mark.parametrize("in_f", [64, 192, 320])
+def test_tc_one_hot_with_zero_sigma_reads_w_exactly(in_f):
+    """With sigma = 0, no bias and X rows one-hot at k, the perturbed weight is W itself
+    (bf16(W + 0) = W), so Y[i, k, :] = W[:, k] bit for bit. Pins how the hashing warps
+    read the staged W tile: its rows (two M tiles, the second ragged), its 64-k atoms
+    and its k chunks, on each stage schedule. Sizes:
+    in = 64 (batch 64: four individuals per unit, one a partial group), 192 (one
+    individual per unit, two stages, an even number of k chunks: the fixed loop) and 320
+    (an odd number of k chunks, and a batch above 256: two N tiles)."""
+    pop, out_f = 3, 200
+    gen = torch.Generator().manual_seed(in_f)
+    w = (torch.randn(out_f, in_f, generator=gen) / 3).to(torch.bfloat16)
+    x = torch.eye(in_f).repeat(pop, 1, 1).to(torch.bfloat16)
+    seeds = torch.tensor([5, -6, 7], dtype=torch.int64)
+    y = virtual_perturbed_linear(x.to(DEV), w.to(DEV), None, seeds.to(DEV), 0.0, 99, path="tc")
+    want = w.T.unsqueeze(0).expand(pop, in_f, out_f)
+    assert torch.equal(y.cpu(), want)
+
+
 def test_tc_and_auto_path_selection():
     x = torch.randn(2, 32, 64, device=DEV).to(torch.bfloat16)
     w = torch.randn(16, 64, device=DEV)
