@@ -859,7 +859,9 @@ template <int MH, bool kW, bool kY, bool kHook, int kKind = kUniform>
 cudaError_t launch_typed(const CUtensorMap& xmap, const CUtensorMap& wmap, const TcParams& p,
                          int atoms, int grid, size_t smem, cudaStream_t stream) {
   if (atoms == 2) {
-    if constexpr (kW && !kHook) {
+    // The fixed loop for the uniform kind only: the Gaussian kind's longer chunk
+    // body runs slower in it (5.75 against 5.51 ms on 256 x 256 x 4096^2).
+    if constexpr (kW && !kHook && kKind == kUniform) {
       if (p.g == 1 && p.stages == 2 && p.w_slots == 1 && p.k_chunks % 2 == 0)
         return launch_kernel<MH, kW, kY, kHook, kKind, true, 2, true>(xmap, wmap, p, grid, smem, stream);
     }
