@@ -87,14 +87,27 @@ grad_kernel(const float* __restrict__ fitness, const int64_t* __restrict__ seeds
         const uint4 v = s_ind[q];
         // (the Gaussian variant's constant factor rides on the fitness weight)
         const float f = kKind == kGaussian ? kGaussScale * __uint_as_float(v.z) : __uint_as_float(v.z);
+        // Element pairs: the noise values' -1.5 and the weighted sum each as one packed
+        // two-lane operation (each lane rounds as fadd / fmaf do).
+        const float2 f2 = make_float2(f, f);
 #pragma unroll
-        for (int e = 0; e < kE; ++e) {
-          uint32_t lo = blo[e], hi = bhi[e];
-          add64(lo, hi, v.x, v.y);
-          if constexpr (kKind == kGaussian)
-            acc[e] = fmaf(f, noise_value<kGaussian>(lo, hi), acc[e]);
-          else
-            acc[e] = fmaf(f, noise_from_bits(mix_to_one_plus_u(lo, hi)), acc[e]);
+        for (int e = 0; e < kE; e += 2) {
+          float2 nz;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t lo = blo[e + h], hi = bhi[e + h];
+            add64(lo, hi, v.x, v.y);
+            float r;
+            if constexpr (kKind == kGaussian)
+              r = noise_value<kGaussian>(lo, hi);
+            else
+              r = __uint_as_float(mix_to_one_plus_u(lo, hi));
+            if (h == 0) nz.x = r; else nz.y = r;
+          }
+          if constexpr (kKind != kGaussian) nz = __fadd2_rn(nz, make_float2(-1.5f, -1.5f));
+          const float2 s = __ffma2_rn(f2, nz, make_float2(acc[e], acc[e + 1]));
+          acc[e] = s.x;
+          acc[e + 1] = s.y;
         }
       }
     }
