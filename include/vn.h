@@ -310,7 +310,8 @@ vn_status vn_device_status(void* stream);
  * vn_hash_probe -- a measurement kernel, not a step of the method: the noise
  * hash and nothing else,
  *     sums[t] = sum_{e < m} PRNG(seed, offset + t*m + e),  t < n_sums,
- * accumulated in fp32 in order of e (PRNG as defined at the top of this file).
+ * accumulated in fp32 as two partial sums, over the even e and over the odd e
+ * (each in order of e), added at the end (PRNG as defined at the top of this file).
  * One thread per t regenerates its m elements in registers and writes one
  * float, so the launch time is the hash's own: its element rate is the
  * measured ceiling of the integer ALU pipe for this hash, against which the

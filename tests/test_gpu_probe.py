@@ -2,8 +2,10 @@
 
 sums[t] = sum_{e < m} PRNG(seed, offset + t*m + e): the oracle side is its noise dump
 of the whole index range (bit-exact to the library's dump, pinned elsewhere), cut into
-rows of m and summed in float64. The kernel adds in fp32 in order of e, so each sum
-is within m * 2^-24 * (largest partial sum + 1) of the exact one."""
+rows of m and summed in float64. The kernel adds in fp32 as two partial sums (even e
+and odd e, each in order of e) and then adds those. The noise values are exact in fp32
+and each addition rounds by at most 2^-24 of its result, so each sum is within
+m * 2^-24 * (largest even partial sum + largest odd partial sum + 1) of the exact one."""
 
 import numpy as np
 import pytest
@@ -28,9 +30,10 @@ def _want(seed, offset, ts, m):
     for t in ts:
         d = es.noise_dump(np.array([seed], dtype=np.int64), m, (offset + t * m) % (1 << 64))[0]
         d = d.astype(np.float64)
-        part = np.cumsum(d)
-        rows.append(part[-1] if m else 0.0)
-        bounds.append(m * 2.0 ** -24 * ((np.max(np.abs(part)) if m else 0.0) + 1.0))
+        rows.append(float(np.sum(d)) if m else 0.0)
+        ev, od = np.cumsum(d[0::2]), np.cumsum(d[1::2])
+        big = (np.max(np.abs(ev)) if ev.size else 0.0) + (np.max(np.abs(od)) if od.size else 0.0)
+        bounds.append(m * 2.0 ** -24 * (big + 1.0))
     return np.array(rows), np.array(bounds)
 
 

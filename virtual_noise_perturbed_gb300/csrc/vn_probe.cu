@@ -1,17 +1,22 @@
 // vn_probe.cu -- the hash alone, as a measurement kernel (not a step of the method).
 //
-//   sums[t] = sum_{e < m} PRNG(seed, offset + t*m + e),  t < n_sums   (fp32, in order of e)
+//   sums[t] = sum_{e < m} PRNG(seed, offset + t*m + e),  t < n_sums
+//
+// in fp32 as two partial sums, one over the even e and one over the odd e (each in
+// order of e), added at the end.
 //
 // PRNG is the noise of the EvoX API page "evox.triton_kernels.kernels.virtual_noise"
 // (entries "_splitmix64_step", "_cpu_normal_noise"; state reading in vn_hash.cuh).
-// Every thread regenerates its m consecutive elements in registers and writes
-// one float, so the launch costs the hash and nothing else: per element the
-// state step (a 64-bit add: one ALU add, one IMAD carry-add), the finalizer
-// (12 ALU-pipe and 6 IMAD-pipe operations on 32-bit halves, counting the state
-// add's low word) and one FADD into the sum. Its element rate is therefore the
-// measured ceiling of the integer ALU pipe for this hash, the figure the other
-// kernels' rooflines are compared against beside the one derived from the
-// pipe's width and the clock.
+// Every thread regenerates its m consecutive elements in registers and writes one
+// float, so the launch costs the hash and little else. Per element:
+//   - the state step: a 64-bit add, one ALU add and one IMAD carry-add;
+//   - the finalizer: 12 ALU-pipe and 6 IMAD-pipe operations on 32-bit halves,
+//     counting the state add's low word;
+//   - half a packed two-lane fp32 add for the -1.5 and half of one for the sum.
+// That is the least the other kernels spend besides the hash, so its element rate is
+// the measured ceiling of the integer ALU pipe for this hash. The other kernels'
+// rooflines are read against it, beside the figure derived from the pipe's width
+// and the clock.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -32,20 +37,29 @@ hash_probe_kernel(uint64_t seed, uint64_t offset, int64_t n_sums, int64_t m,
   if (t >= n_sums) return;
   const uint64_t st = seed + index_term(offset + static_cast<uint64_t>(t) * static_cast<uint64_t>(m));
   uint32_t slo = static_cast<uint32_t>(st), shi = static_cast<uint32_t>(st >> 32);
-  float acc = 0.f;
+  float2 acc = make_float2(0.f, 0.f);  // the even and the odd elements' partial sums
+  const float2 shift = make_float2(-1.5f, -1.5f);
   int64_t e = 0;
   for (; e + kProbeUnroll <= m; e += kProbeUnroll) {
 #pragma unroll
-    for (int q = 0; q < kProbeUnroll; ++q) {
-      acc += noise_from_bits(mix_to_one_plus_u(slo, shi));
+    for (int q = 0; q < kProbeUnroll; q += 2) {
+      float2 r;
+      r.x = __uint_as_float(mix_to_one_plus_u(slo, shi));
       add64_madc(slo, shi, g_lo, g_hi, one);
+      r.y = __uint_as_float(mix_to_one_plus_u(slo, shi));
+      add64_madc(slo, shi, g_lo, g_hi, one);
+      acc = __fadd2_rn(acc, __fadd2_rn(r, shift));
     }
   }
   for (; e < m; ++e) {
-    acc += noise_from_bits(mix_to_one_plus_u(slo, shi));
+    const float v = noise_from_bits(mix_to_one_plus_u(slo, shi));
+    if (e & 1)
+      acc.y += v;
+    else
+      acc.x += v;
     add64_madc(slo, shi, g_lo, g_hi, one);
   }
-  sums[t] = acc;
+  sums[t] = acc.x + acc.y;
 }
 
 }  // namespace
