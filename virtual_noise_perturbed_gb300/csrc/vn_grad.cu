@@ -11,7 +11,9 @@
 //   * A CTA owns a tile of 256 consecutive elements; lane l of every warp owns
 //     elements [8l, 8l + 8) of the tile. The per-element part of the state,
 //     (offset + e + 1) * GAMMA, is computed once; per individual the state is
-//     that plus the seed (one 64-bit add), then the finalizer, then one FMA.
+//     that plus the seed (one 64-bit add), then the finalizer; each pair of
+//     elements then takes one packed two-lane add (the noise's -1.5) and one
+//     packed two-lane FMA into its two sums (each lane rounding as fadd / fmaf).
 //   * The 8 warps of the CTA split the CTA's share of the population
 //     (individuals are staged in shared memory 256 at a time and read back as
 //     one 16-byte broadcast per individual), and their partial sums are added

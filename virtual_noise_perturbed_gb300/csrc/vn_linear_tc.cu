@@ -9,10 +9,11 @@
 // (the module description adds it to the tile in registers); no noise tensor exists.
 //
 // Per individual the product is D = W'_i X_i^T with D[j, n] = Y_i[n, j]:
-//   A = W'_i tile, 128 output rows x 64 k (bf16, K-major), written into shared
-//       memory by "hashing" warps in the 128-byte-swizzled canonical layout
-//       from the W tile (fp32 or bf16, 128 rows x 64 k), which TMA stages once
-//       per (unit, k chunk) into a two-slot ring shared by all hashing warps;
+//   A = W'_i tile, 128 output rows x 64 k per swizzle atom (bf16, K-major),
+//       written into shared memory by "hashing" warps in the 128-byte-swizzled
+//       canonical layout from the W tile (fp32 or bf16, 128 rows x the stage's
+//       64 or 128 k), which TMA stages once per (unit, k chunk) into a ring of one
+//       or two slots shared by all hashing warps;
 //   B = X_i tile, NT batch rows x 64 k (bf16, K-major), loaded by TMA with the
 //       same 128-byte swizzle;
 //   D = fp32 accumulator in TMEM, 128 lanes (output rows) x NT columns (batch).
@@ -24,8 +25,9 @@
 //   warps 2..5  epilogue: TMEM -> registers -> + b + sigma*nb -> Y (one per TMEM lane quarter);
 //   warps 6..21 hashing: W'_i = bf16(W + sigma*N_i), 16 bytes (8 k) per store.
 // A work unit is (group of G individuals, N tile, M tile of 128*MH output rows;
-// the host uses MH = 1); per k-chunk of 64 the unit's W tile is staged once and
-// perturbed for each of the G individuals, whose accumulators sit
+// the host uses MH = 1); per k chunk (one stage: 64 k per swizzle atom, one or
+// two atoms) the unit's W tile is staged once and perturbed for each of the G
+// individuals, whose accumulators sit
 // side by side in TMEM (G*MH*NT <= 256 columns, so two units can be in flight:
 // double-buffered TMEM).
 // Every barrier wait is bounded; a wait that runs out records a status word,

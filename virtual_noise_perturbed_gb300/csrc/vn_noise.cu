@@ -35,8 +35,11 @@ constexpr uint64_t kDumpGroupHop = kGamma * static_cast<uint64_t>(kDumpStride - 
 // Grid-stride over (row i, chunk of kDumpChunk columns). Thread t makes the
 // 4-element groups at columns c + 4t + 1024g, g < 8: one 16-byte store per group,
 // consecutive lanes on consecutive 16-byte segments. The state of the next
-// element is the previous plus GAMMA and the state of the next group the
-// previous group's plus 1024*GAMMA, so no 64-bit multiply is needed per group.
+// element is the previous plus GAMMA; in a chunk that lies inside its row one
+// state chain runs through the thread's groups (the step after a group's last
+// element adds (1024 - 3)*GAMMA, landing on the next group's first), and at a
+// ragged row end the next group's state is the previous group's plus
+// 1024*GAMMA, so no 64-bit multiply is needed per group.
 // vec4: every row starts 16-byte aligned (out aligned and n % 4 == 0).
 // kIdx32: the chunk count fits in 32 bits, so the row of a chunk is a 32-bit
 // division (a 64-bit one costs several instructions per element).
