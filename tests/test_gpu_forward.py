@@ -202,6 +202,30 @@ def test_tc_forward_matches_oracle(pop, batch, in_f, out_f, wdt, shared, bias):
     _run_and_check(x, w, b, s, sig, off, TOL_BF16, path="tc")
 
 
+def _random_tc_shapes(n, seed):
+    """Seeded random shapes for the tensor-core path: batches from the minimum N to two N
+    tiles, in any multiple of 8 up to 632 (even and odd numbers of k chunks, ragged last
+    chunks), ragged out, both W dtypes, shared X, with and without bias, any 64-bit offset.
+    They land on every stage schedule: grouped individuals, one individual per unit on the
+    fixed two-stage loop or the general ring, one-atom stages."""
+    rng = np.random.default_rng(seed)
+    shapes = []
+    for _ in range(n):
+        shapes.append((int(rng.integers(1, 4)), int(rng.integers(16, 300)), 8 * int(rng.integers(1, 80)),
+                       int(rng.integers(1, 300)),
+                       torch.bfloat16 if rng.random() < 0.7 else torch.float32,
+                       bool(rng.random() < 0.2), bool(rng.random() < 0.8),
+                       int(rng.integers(0, 1 << 62)) * 4 + int(rng.integers(0, 4))))
+    return shapes
+
+
+@pytest.mark.parametrize("pop,batch,in_f,out_f,wdt,shared,bias,offset", _random_tc_shapes(16, 2026))
+def test_tc_forward_random_shapes(pop, batch, in_f, out_f, wdt, shared, bias, offset):
+    x, w, b, s, sig, _ = _case(pop, batch, in_f, out_f, shared=shared, bias=bias,
+                               xdt=torch.bfloat16, wdt=wdt, bdt=wdt, seed=in_f + out_f)
+    _run_and_check(x, w, b, s, sig, offset, TOL_BF16, path="tc")
+
+
 def test_tc_forward_one_hot_reads_bf16_noise_exactly():
     """X rows = e_k, W = 0, b = 0, sigma = 1 on the tensor-core path: the perturbed
     weight is bf16(N_i[j, k]) and the fp32 accumulation of one product is exact, so
