@@ -369,6 +369,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 linear_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap wmap,
                  const TcParams p) {
   constexpr int kKC = kAtomK * kAtoms;  // k per stage
+  // The fixed loop carries each chunk's state chain from one k chunk to the next
+  // and takes no per-individual seed: one individual per unit only.
+  static_assert(!kFix || kG1, "the fixed two-stage loop serves one individual per unit");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
